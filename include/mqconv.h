@@ -1,0 +1,177 @@
+/*
+ * mqconv.h -- C ABI of the MicroQonv quantize-once convolution library (sm_103a).
+ *
+ * The method (paper "MicroQonv: Reshaping Convolution Tensors for Efficient
+ * Microscaling in Training and Inference", Facq, Ben Ali, Sentieys):
+ * every convolution tensor -- activations X, weights W, output gradients
+ * G_Y -- is quantized exactly once into square 8x8 microscaling blocks stored
+ * channel-batch-first, and the three GEMMs of a training step run on those
+ * packed blocks with an on-chip (implicit) im2col, so no im2col matrix and no
+ * second quantization ever reaches device memory.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers documented as "device" are CUDA device pointers owned by the
+ *     caller.  The library never allocates or frees memory.
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream).
+ *     Argument errors are reported synchronously by the return value and
+ *     nothing is launched.  Errors found on the device (non-finite input, a
+ *     bounded wait that expired) are OR-ed into a device status word that
+ *     mqconv_device_status() reads and clears.
+ *   - Batch N and every channel count must be multiples of 8 (the block edge);
+ *     callers zero-pad otherwise.  All device pointers must be 16-byte aligned.
+ *   - Element formats (codes): E2M1 (NVFP4), E2M3 (6-bit), E4M3 (8-bit).  Block
+ *     scales are always E4M3; the per-tensor scale is one fp32.
+ *
+ * Packed tensor layout (mq_packed)
+ *   Activations (role ACT) and gradients (role GRAD) with dims (N, C, H, W):
+ *     blocks ordered [H][W][N/8][C/8]; inside a block element i = 8*n + c
+ *     (channel fastest) -- "each spatial location (h, w) contains a contiguous
+ *     block of all channels across all batch elements", values consecutive
+ *     along C_in (MicroQonv §IV-A, Fig. 3).
+ *   Weights (role WEIGHT) with dims (Cout, Cin, Kh, Kw):
+ *     blocks ordered [Kh][Kw][Cout/8][Cin/8]; element i = 8*co + ci (§IV-B:
+ *     weights quantized along C_in and C_out).
+ *   Code payload per block: E2M1 32 bytes (element i in byte i/2, low nibble
+ *     for even i); E2M3 48 bytes (little-endian bit stream, element i at bits
+ *     6i..6i+5); E4M3 64 bytes (byte i).  Scales: one E4M3 byte per block, in
+ *     block order, in a separate array.
+ *
+ * Quantization (MicroQonv §II-D, §III-A, §IV-B)
+ *   T_scale = fl32(amax / (maxB_ef * 448)), maxB_ef = 6 (E2M1), 7.5 (E2M3),
+ *   448 (E4M3 codes); B_scale = RN_E4M3(amax_block / (maxB_ef * T_scale));
+ *   code = RN(x / (B_scale * T_scale)).  Both roundings act on the exact real
+ *   quotient, ties to even, saturating at the largest finite value.  A block
+ *   whose scale rounds to zero (or T_scale = 0) gets magnitude-0 codes.  The
+ *   sign bit of each code is the sign bit of its input.
+ */
+#ifndef MQCONV_H
+#define MQCONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MQCONV_ABI_VERSION 1
+
+/* cudaStream_t without including CUDA headers */
+typedef struct CUstream_st *mq_stream;
+
+typedef enum {
+  MQ_OK = 0,
+  MQ_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, inconsistent shapes */
+  MQ_ERR_UNSUPPORTED = 2,   /* N or a channel count not a multiple of 8, too large */
+  MQ_ERR_ALIGNMENT = 3,     /* a device pointer not 16-byte aligned */
+  MQ_ERR_NONFINITE = 4,     /* device: Inf or NaN in a quantized input */
+  MQ_ERR_TIMEOUT = 5,       /* device: a bounded wait inside a kernel expired */
+  MQ_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch error) */
+  MQ_ERR_WORKSPACE = 7      /* workspace null or smaller than required */
+} mq_status;
+
+typedef enum { MQ_FMT_E2M1 = 4, MQ_FMT_E2M3 = 6, MQ_FMT_E4M3 = 8 } mq_format;
+typedef enum { MQ_ROLE_ACT = 0, MQ_ROLE_WEIGHT = 1, MQ_ROLE_GRAD = 2 } mq_role;
+typedef enum { MQ_DT_F32 = 0, MQ_DT_BF16 = 1 } mq_dtype;
+typedef enum { MQ_LAYOUT_NCHW = 0, MQ_LAYOUT_HWCN = 1, MQ_LAYOUT_OIHW = 2 } mq_layout;
+
+/* A tensor quantized once into packed 8x8 blocks (layout above). */
+typedef struct {
+  int32_t fmt;       /* mq_format of the codes */
+  int32_t role;      /* mq_role */
+  int64_t dims[4];   /* ACT/GRAD: (N, C, H, W); WEIGHT: (Cout, Cin, Kh, Kw) */
+  void *codes;       /* device, mqconv_packed_code_bytes() bytes */
+  uint8_t *scales;   /* device, mqconv_packed_scale_bytes() bytes */
+  float *s_t;        /* device, one float: T_scale */
+} mq_packed;
+
+/* One convolution layer: cross-correlation, zero padding, square stride/pad.
+ * Ho = (H + 2 pad - Kh) / stride + 1, Wo likewise (paperlayer summary of the
+ * paper, §II-A "Forward Pass", generalised to stride and padding as §II-A
+ * states the method allows). */
+typedef struct {
+  int64_t N, Cin, H, W, Cout, Kh, Kw, stride, pad;
+} mq_conv_desc;
+
+/* Optional fused epilogue of mqconv_fwd: requantize Y straight from the
+ * accumulators into the next layer's activation blocks (role ACT, dims
+ * (N, Cout, Ho, Wo)).  A global amax of Y cannot exist before Y does, so
+ * T_scale is built from a caller-supplied statistic (e.g. the previous step's
+ * amax, the Hindsight scheme the paper uses in §VII); the true amax of Y is
+ * written to amax_out for the next step. */
+typedef struct {
+  int32_t fmt;            /* mq_format of the requantized Y */
+  const float *amax_in;   /* device, 1 float: statistic T_scale is built from */
+  const mq_packed *out;   /* packed Y (its fmt/role/dims must match) */
+  float *amax_out;        /* device, 1 float or NULL: receives max|Y| */
+} mq_requant;
+
+int32_t mqconv_abi_version(void);
+const char *mqconv_status_string(mq_status status);
+
+/* Bytes of the code payload / scale array of a packed tensor.  dims as in
+ * mq_packed.  Returns 0 for invalid arguments. */
+size_t mqconv_packed_code_bytes(int32_t fmt, const int64_t dims[4]);
+size_t mqconv_packed_scale_bytes(const int64_t dims[4]);
+
+/*
+ * Quantize one dense tensor once (MicroQonv §III-A, §IV-B).
+ *   src      device, fp32 or bf16 (dtype), dense in `layout`:
+ *            ACT/GRAD: NCHW or HWCN ([H][W][C][N]); WEIGHT: OIHW.
+ *   dst      packed output; dst->role, dst->fmt, dst->dims say what to produce.
+ *   amax_in  device or NULL.  NULL: exact two-pass mode, T_scale from the
+ *            tensor's own amax (amax_out must then be non-NULL; it receives
+ *            that amax).  Non-NULL: one pass, T_scale from *amax_in; amax_out,
+ *            if non-NULL, receives the measured amax.
+ *   Non-finite input sets MQ_ERR_NONFINITE in the device status word (the
+ *   output is then unspecified).
+ */
+mq_status mqconv_quantize_cbf(const void *src, int32_t dtype, int32_t layout, const mq_packed *dst,
+                              const float *amax_in, float *amax_out, mq_stream stream);
+
+/*
+ * Forward convolution on packed operands: Y = W_f * X' with X' the on-chip
+ * channel-batch-first im2col of Xq (MicroQonv §IV-A:
+ * Y_{fCout,N} = W_{fCout,Cin} . X'_{Cin,N}).
+ *   xq  packed activations, role ACT, dims (N, Cin, H, W).
+ *   wq  packed weights, role WEIGHT, dims (Cout, Cin, Kh, Kw).
+ *   y   device fp32 [Ho][Wo][Cout][N] (HWCN), or NULL when rq is given.
+ *   rq  NULL, or the fused requantizing epilogue (see mq_requant).
+ */
+mq_status mqconv_fwd(const mq_conv_desc *desc, const mq_packed *xq, const mq_packed *wq, float *y,
+                     const mq_requant *rq, mq_stream stream);
+
+/*
+ * Data gradient: G_X = col2im(W_f^T * G_Y) computed directly as the adjoint
+ * convolution ("convolving the output gradient with transposed kernels",
+ * paperlayer summary §II-A "Backward Pass"; MicroQonv §IV-A:
+ * G_X'_{Cin,N} = W^T_{fCout,Cin} . G_Y_{fCout,N}).
+ *   wq   packed weights, role WEIGHT, dims (Cout, Cin, Kh, Kw).
+ *   dyq  packed output gradient, role GRAD, dims (N, Cout, Ho, Wo).
+ *   dx   device fp32 [H][W][Cin][N] (HWCN).
+ */
+mq_status mqconv_dgrad(const mq_conv_desc *desc, const mq_packed *wq, const mq_packed *dyq, float *dx,
+                       mq_stream stream);
+
+/*
+ * Weight gradient: G_W = G_Y * X'^T (MicroQonv §IV-A: G_W_{fCout,Cin} =
+ * G_Y_{fCout,N} . X'^T_{Cin,N}), reduced over (Ho, Wo, N).
+ *   dyq  packed output gradient, role GRAD, dims (N, Cout, Ho, Wo).
+ *   xq   packed activations, role ACT, dims (N, Cin, H, W).
+ *   dw   device fp32 [Cout][Cin][Kh][Kw] (OIHW).
+ *   workspace / ws_bytes  device scratch of at least
+ *        mqconv_wgrad_workspace_bytes(desc) bytes for the split-K partial
+ *        sums (reduced in a fixed order: results are deterministic).
+ */
+size_t mqconv_wgrad_workspace_bytes(const mq_conv_desc *desc);
+mq_status mqconv_wgrad(const mq_conv_desc *desc, const mq_packed *dyq, const mq_packed *xq, float *dw,
+                       void *workspace, size_t ws_bytes, mq_stream stream);
+
+/* Synchronize `stream`, copy the device status word (an OR of mq_status bit
+ * flags 1 << MQ_ERR_*) to *host_status, and clear it. */
+mq_status mqconv_device_status(mq_stream stream, int32_t *host_status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MQCONV_H */

@@ -1,0 +1,195 @@
+"""Python binding of libmqconv (the C ABI in include/mqconv.h).
+
+Argument marshalling only: every step of quantization and convolution runs in
+the library's CUDA kernels.  PyTorch supplies device memory and streams.  There
+is no fallback: if libmqconv.so is missing or a call fails, this module raises.
+
+Entry points mirror the C names: quantize_cbf, fwd, dgrad, wgrad,
+wgrad_workspace_bytes, packed_code_bytes, packed_scale_bytes, device_status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+
+FMT = {"e2m1": 4, "e2m3": 6, "e4m3": 8}
+ROLE = {"act": 0, "weight": 1, "grad": 2}
+DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+LAYOUT = {"nchw": 0, "hwcn": 1, "oihw": 2}
+ERR_BITS = {4: "non-finite input", 5: "bounded wait expired"}
+
+
+class MQError(RuntimeError):
+    pass
+
+
+class _Packed(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("role", ctypes.c_int32), ("dims", ctypes.c_int64 * 4),
+                ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("s_t", ctypes.c_void_p)]
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("N", "Cin", "H", "W", "Cout", "Kh", "Kw", "stride", "pad")]
+
+
+class _Requant(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("amax_in", ctypes.c_void_p), ("out", ctypes.POINTER(_Packed)),
+                ("amax_out", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmqconv.so (built by __graft_entry__.build() / build.py)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MQError(f"libmqconv.so not built ({LIB_PATH}); run build.py")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32 = ctypes.c_void_p, ctypes.c_int32
+        L.mqconv_abi_version.restype = i32
+        L.mqconv_status_string.argtypes = [i32]
+        L.mqconv_status_string.restype = ctypes.c_char_p
+        L.mqconv_packed_code_bytes.argtypes = [i32, P]
+        L.mqconv_packed_code_bytes.restype = ctypes.c_size_t
+        L.mqconv_packed_scale_bytes.argtypes = [P]
+        L.mqconv_packed_scale_bytes.restype = ctypes.c_size_t
+        L.mqconv_quantize_cbf.argtypes = [P, i32, i32, ctypes.POINTER(_Packed), P, P, P]
+        L.mqconv_fwd.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P,
+                                 ctypes.POINTER(_Requant), P]
+        L.mqconv_dgrad.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P, P]
+        L.mqconv_wgrad_workspace_bytes.argtypes = [ctypes.POINTER(_Desc)]
+        L.mqconv_wgrad_workspace_bytes.restype = ctypes.c_size_t
+        L.mqconv_wgrad.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P, P,
+                                   ctypes.c_size_t, P]
+        L.mqconv_device_status.argtypes = [P, ctypes.POINTER(i32)]
+        for f in ("mqconv_quantize_cbf", "mqconv_fwd", "mqconv_dgrad", "mqconv_wgrad", "mqconv_device_status"):
+            getattr(L, f).restype = i32
+        _lib = L
+    return _lib
+
+
+def abi_version() -> int:
+    return int(lib().mqconv_abi_version())
+
+
+def status_string(code: int) -> str:
+    return lib().mqconv_status_string(code).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise MQError(f"{what}: {status_string(rc)} (status {rc})")
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dims(d: Sequence[int]):
+    return (ctypes.c_int64 * 4)(*[int(v) for v in d])
+
+
+def packed_code_bytes(fmt: str, dims: Sequence[int]) -> int:
+    return int(lib().mqconv_packed_code_bytes(FMT[fmt], ctypes.cast(_dims(dims), ctypes.c_void_p)))
+
+
+def packed_scale_bytes(dims: Sequence[int]) -> int:
+    return int(lib().mqconv_packed_scale_bytes(ctypes.cast(_dims(dims), ctypes.c_void_p)))
+
+
+class Packed:
+    """A packed 8x8-block tensor whose buffers are torch device tensors.
+
+    dims: act/grad (N, C, H, W); weight (Cout, Cin, Kh, Kw)."""
+
+    def __init__(self, fmt: str, role: str, dims: Sequence[int], device="cuda", codes=None, scales=None, s_t=None):
+        self.fmt, self.role, self.dims = fmt, role, tuple(int(v) for v in dims)
+        nc, ns = packed_code_bytes(fmt, self.dims), packed_scale_bytes(self.dims)
+        if nc == 0:
+            raise MQError(f"invalid packed dims {self.dims} for {fmt}")
+        self.codes = codes if codes is not None else torch.empty(nc, dtype=torch.uint8, device=device)
+        self.scales = scales if scales is not None else torch.empty(ns, dtype=torch.uint8, device=device)
+        self.s_t = s_t if s_t is not None else torch.zeros(1, dtype=torch.float32, device=device)
+
+    def c(self) -> _Packed:
+        return _Packed(FMT[self.fmt], ROLE[self.role], _dims(self.dims), self.codes.data_ptr(),
+                       self.scales.data_ptr(), self.s_t.data_ptr())
+
+
+def desc(layer) -> _Desc:
+    """mq_conv_desc from any object with N, Cin, H, W, Cout, k (or Kh, Kw), stride, pad."""
+    kh = getattr(layer, "Kh", None) or layer.k
+    kw = getattr(layer, "Kw", None) or layer.k
+    return _Desc(layer.N, layer.Cin, layer.H, layer.W, layer.Cout, kh, kw, layer.stride, layer.pad)
+
+
+def quantize_cbf(src: torch.Tensor, layout: str, dst: Packed, amax_in: Optional[torch.Tensor] = None,
+                 amax_out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """mqconv_quantize_cbf: quantize `src` (fp32/bf16, dense in `layout`) once into `dst`."""
+    if not src.is_contiguous():
+        raise MQError("src must be contiguous")
+    c = dst.c()
+    rc = lib().mqconv_quantize_cbf(src.data_ptr(), DTYPE[src.dtype], LAYOUT[layout], ctypes.byref(c),
+                                   _ptr(amax_in), _ptr(amax_out), _stream(stream))
+    _check(rc, "mqconv_quantize_cbf")
+
+
+def fwd(layer, xq: Packed, wq: Packed, y: Optional[torch.Tensor], rq_out: Optional[Packed] = None,
+        rq_amax_in: Optional[torch.Tensor] = None, rq_amax_out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """mqconv_fwd: Y (fp32, [Ho][Wo][Cout][N]) and/or the fused requantization of Y into rq_out."""
+    d, x, w = desc(layer), xq.c(), wq.c()
+    rq_p = None
+    if rq_out is not None:
+        out_c = rq_out.c()
+        rq = _Requant(FMT[rq_out.fmt], _ptr(rq_amax_in), ctypes.pointer(out_c), _ptr(rq_amax_out))
+        rq_p = ctypes.byref(rq)
+    rc = lib().mqconv_fwd(ctypes.byref(d), ctypes.byref(x), ctypes.byref(w), _ptr(y), rq_p, _stream(stream))
+    _check(rc, "mqconv_fwd")
+
+
+def dgrad(layer, wq: Packed, dyq: Packed, dx: torch.Tensor, stream=None) -> None:
+    """mqconv_dgrad: dX (fp32, [H][W][Cin][N])."""
+    d, w, g = desc(layer), wq.c(), dyq.c()
+    rc = lib().mqconv_dgrad(ctypes.byref(d), ctypes.byref(w), ctypes.byref(g), _ptr(dx), _stream(stream))
+    _check(rc, "mqconv_dgrad")
+
+
+def wgrad_workspace_bytes(layer) -> int:
+    d = desc(layer)
+    return int(lib().mqconv_wgrad_workspace_bytes(ctypes.byref(d)))
+
+
+def wgrad(layer, dyq: Packed, xq: Packed, dw: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """mqconv_wgrad: dW (fp32, [Cout][Cin][Kh][Kw]); workspace >= wgrad_workspace_bytes(layer) bytes."""
+    d, g, x = desc(layer), dyq.c(), xq.c()
+    rc = lib().mqconv_wgrad(ctypes.byref(d), ctypes.byref(g), ctypes.byref(x), _ptr(dw), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "mqconv_wgrad")
+
+
+def device_status(stream=None) -> int:
+    """mqconv_device_status: synchronize, read and clear the device status word."""
+    v = ctypes.c_int32(0)
+    _check(lib().mqconv_device_status(_stream(stream), ctypes.byref(v)), "mqconv_device_status")
+    return int(v.value)
+
+
+def check_device_status(stream=None) -> None:
+    v = device_status(stream)
+    if v:
+        bits = [name for b, name in ERR_BITS.items() if v & (1 << b)]
+        raise MQError(f"device status {v:#x}: {', '.join(bits) or 'unknown'}")

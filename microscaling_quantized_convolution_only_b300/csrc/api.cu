@@ -1,0 +1,297 @@
+// api.cu -- the C ABI declared in include/mqconv.h: argument checks, launch
+// planning and launches.  The library never allocates device memory.
+#include <algorithm>
+#include <climits>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mqconv.h"
+#include "kernels.h"
+
+namespace {
+
+// Device status word: kernels OR error bits into it; mqconv_device_status()
+// reads and clears it.  One copy per device that loads the library.
+__device__ uint32_t g_status_word;
+
+constexpr int kMaxDevices = 64;
+struct DevInfo {
+  bool ready = false;
+  uint32_t *status = nullptr;
+  int num_sms = 0;
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+mq_status dev_info(DevInfo **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo &d = g_dev[dev];
+  if (!d.ready) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MQ_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MQ_ERR_CUDA;
+    d.status = static_cast<uint32_t *>(p);
+    d.num_sms = sms;
+    d.ready = true;
+  }
+  *out = &d;
+  return MQ_OK;
+}
+
+bool fmt_ok(int32_t f) { return f == MQ_FMT_E2M1 || f == MQ_FMT_E2M3 || f == MQ_FMT_E4M3; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t out_dim(int64_t in, int64_t k, int64_t s, int64_t pad) { return (in + 2 * pad - k) / s + 1; }
+
+mq_status check_packed(const mq_packed *t, int32_t role, int64_t d0, int64_t d1, int64_t d2, int64_t d3) {
+  if (!t || !t->codes || !t->scales || !t->s_t) return MQ_ERR_INVALID_ARG;
+  if (!fmt_ok(t->fmt) || t->role != role) return MQ_ERR_INVALID_ARG;
+  if (t->dims[0] != d0 || t->dims[1] != d1 || t->dims[2] != d2 || t->dims[3] != d3) return MQ_ERR_INVALID_ARG;
+  if (!aligned16(t->codes) || (reinterpret_cast<uintptr_t>(t->s_t) & 3u)) return MQ_ERR_ALIGNMENT;
+  return MQ_OK;
+}
+
+mq_status check_desc(const mq_conv_desc *d) {
+  if (!d) return MQ_ERR_INVALID_ARG;
+  if (d->N <= 0 || d->Cin <= 0 || d->Cout <= 0 || d->H <= 0 || d->W <= 0 || d->Kh <= 0 || d->Kw <= 0 ||
+      d->stride <= 0 || d->pad < 0)
+    return MQ_ERR_INVALID_ARG;
+  if (d->N % 8 || d->Cin % 8 || d->Cout % 8) return MQ_ERR_UNSUPPORTED;
+  const int64_t Ho = out_dim(d->H, d->Kh, d->stride, d->pad), Wo = out_dim(d->W, d->Kw, d->stride, d->pad);
+  if (Ho <= 0 || Wo <= 0) return MQ_ERR_INVALID_ARG;
+  // the kernels index positions, block groups and columns with 32-bit integers
+  const int64_t lim = INT_MAX / 16;
+  if (d->H * d->W * (d->N / 8) > lim || Ho * Wo * (d->N / 8) > lim || d->Kh * d->Kw * d->Cin > lim ||
+      d->Cin > 65536 || d->Cout > 65536 || d->stride > 16 || d->Kh > 64 || d->Kw > 64)
+    return MQ_ERR_UNSUPPORTED;
+  return MQ_OK;
+}
+
+mq::ConvParams base_params(const mq_conv_desc *d, int op, uint32_t *status) {
+  mq::ConvParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.op = op;
+  p.N = (int)d->N;
+  p.Cin = (int)d->Cin;
+  p.H = (int)d->H;
+  p.W = (int)d->W;
+  p.Cout = (int)d->Cout;
+  p.Kh = (int)d->Kh;
+  p.Kw = (int)d->Kw;
+  p.stride = (int)d->stride;
+  p.pad = (int)d->pad;
+  p.Ho = (int)out_dim(d->H, d->Kh, d->stride, d->pad);
+  p.Wo = (int)out_dim(d->W, d->Kw, d->stride, d->pad);
+  p.NG = p.N / 8;
+  p.CIG = p.Cin / 8;
+  p.COG = p.Cout / 8;
+  p.status = status;
+  return p;
+}
+
+mq::Operand operand(const mq_packed *t) {
+  mq::Operand o;
+  o.codes = static_cast<const uint8_t *>(t->codes);
+  o.scales = t->scales;
+  o.s_t = t->s_t;
+  o.fmt = t->fmt;
+  return o;
+}
+
+float pre_mult(int fa, int fb) { return (fa == MQ_FMT_E4M3 ? 4.0f : 1.0f) * (fb == MQ_FMT_E4M3 ? 4.0f : 1.0f); }
+
+size_t wgrad_ws_bytes(const mq_conv_desc *d) {
+  mq::ConvParams p = base_params(d, mq::OP_WGRAD, nullptr);
+  mq::conv_plan(p);
+  return (size_t)p.k_splits * (size_t)p.Cout * (size_t)p.ncols * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t mqconv_abi_version(void) { return MQCONV_ABI_VERSION; }
+
+const char *mqconv_status_string(mq_status s) {
+  switch (s) {
+    case MQ_OK: return "ok";
+    case MQ_ERR_INVALID_ARG: return "invalid argument";
+    case MQ_ERR_UNSUPPORTED: return "unsupported shape (batch and channels must be multiples of 8)";
+    case MQ_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    case MQ_ERR_NONFINITE: return "non-finite value in a quantized input";
+    case MQ_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
+    case MQ_ERR_CUDA: return "CUDA runtime error";
+    case MQ_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+size_t mqconv_packed_code_bytes(int32_t fmt, const int64_t dims[4]) {
+  if (!dims || !fmt_ok(fmt) || dims[0] <= 0 || dims[1] <= 0 || dims[2] <= 0 || dims[3] <= 0 || dims[0] % 8 ||
+      dims[1] % 8)
+    return 0;
+  return (size_t)(dims[0] / 8) * (size_t)(dims[1] / 8) * (size_t)dims[2] * (size_t)dims[3] *
+         (size_t)mq::block_bytes(fmt);
+}
+
+size_t mqconv_packed_scale_bytes(const int64_t dims[4]) {
+  if (!dims || dims[0] <= 0 || dims[1] <= 0 || dims[2] <= 0 || dims[3] <= 0 || dims[0] % 8 || dims[1] % 8) return 0;
+  return (size_t)(dims[0] / 8) * (size_t)(dims[1] / 8) * (size_t)dims[2] * (size_t)dims[3];
+}
+
+mq_status mqconv_quantize_cbf(const void *src, int32_t dtype, int32_t layout, const mq_packed *dst,
+                              const float *amax_in, float *amax_out, mq_stream stream) {
+  if (!src || !dst || !dst->codes || !dst->scales || !dst->s_t) return MQ_ERR_INVALID_ARG;
+  if (!fmt_ok(dst->fmt) || (dtype != MQ_DT_F32 && dtype != MQ_DT_BF16)) return MQ_ERR_INVALID_ARG;
+  if (dst->role != MQ_ROLE_ACT && dst->role != MQ_ROLE_WEIGHT && dst->role != MQ_ROLE_GRAD) return MQ_ERR_INVALID_ARG;
+  if (layout != MQ_LAYOUT_NCHW && layout != MQ_LAYOUT_HWCN && layout != MQ_LAYOUT_OIHW) return MQ_ERR_INVALID_ARG;
+  if ((dst->role == MQ_ROLE_WEIGHT) != (layout == MQ_LAYOUT_OIHW)) return MQ_ERR_INVALID_ARG;
+  const int64_t *d = dst->dims;
+  if (d[0] <= 0 || d[1] <= 0 || d[2] <= 0 || d[3] <= 0) return MQ_ERR_INVALID_ARG;
+  if (d[0] % 8 || d[1] % 8) return MQ_ERR_UNSUPPORTED;
+  if (!amax_in && !amax_out) return MQ_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst->codes) || (reinterpret_cast<uintptr_t>(dst->s_t) & 3u) ||
+      (amax_in && (reinterpret_cast<uintptr_t>(amax_in) & 3u)) ||
+      (amax_out && (reinterpret_cast<uintptr_t>(amax_out) & 3u)))
+    return MQ_ERR_ALIGNMENT;
+  const int64_t n = d[0] * d[1] * d[2] * d[3];
+  if (n / d[0] / d[1] != d[2] * d[3] || n > (int64_t)1 << 40) return MQ_ERR_UNSUPPORTED;
+
+  DevInfo *di = nullptr;
+  mq_status st = dev_info(&di);
+  if (st != MQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  mq::QuantParams p;
+  p.d0 = d[0];
+  p.d1 = d[1];
+  p.d2 = d[2];
+  p.d3 = d[3];
+  p.codes = static_cast<uint8_t *>(dst->codes);
+  p.scales = dst->scales;
+  p.s_t_out = dst->s_t;
+  p.status = di->status;
+  if (!amax_in) {
+    uint32_t *bits = reinterpret_cast<uint32_t *>(amax_out);
+    if (cudaMemsetAsync(bits, 0, sizeof(uint32_t), s) != cudaSuccess) return MQ_ERR_CUDA;
+    if (mq::launch_amax(src, dtype, n, bits, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
+    p.amax_src_bits = bits;
+    p.amax_meas_bits = nullptr;
+  } else {
+    p.amax_src_bits = reinterpret_cast<const uint32_t *>(amax_in);
+    p.amax_meas_bits = reinterpret_cast<uint32_t *>(amax_out);
+    if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), s) != cudaSuccess) return MQ_ERR_CUDA;
+  }
+  if (mq::launch_quantize(src, dtype, layout, dst->fmt, p, s) != cudaSuccess) return MQ_ERR_CUDA;
+  return MQ_OK;
+}
+
+mq_status mqconv_fwd(const mq_conv_desc *desc, const mq_packed *xq, const mq_packed *wq, float *y,
+                     const mq_requant *rq, mq_stream stream) {
+  mq_status st = check_desc(desc);
+  if (st != MQ_OK) return st;
+  const int64_t Ho = out_dim(desc->H, desc->Kh, desc->stride, desc->pad);
+  const int64_t Wo = out_dim(desc->W, desc->Kw, desc->stride, desc->pad);
+  if ((st = check_packed(xq, MQ_ROLE_ACT, desc->N, desc->Cin, desc->H, desc->W)) != MQ_OK) return st;
+  if ((st = check_packed(wq, MQ_ROLE_WEIGHT, desc->Cout, desc->Cin, desc->Kh, desc->Kw)) != MQ_OK) return st;
+  if (!y && !rq) return MQ_ERR_INVALID_ARG;
+  if (y && !aligned16(y)) return MQ_ERR_ALIGNMENT;
+  if (rq) {
+    if (!rq->amax_in || !fmt_ok(rq->fmt) || !rq->out || rq->out->fmt != rq->fmt) return MQ_ERR_INVALID_ARG;
+    if ((st = check_packed(rq->out, MQ_ROLE_ACT, desc->N, desc->Cout, Ho, Wo)) != MQ_OK) return st;
+    if ((reinterpret_cast<uintptr_t>(rq->amax_in) & 3u) || (rq->amax_out && (reinterpret_cast<uintptr_t>(rq->amax_out) & 3u)))
+      return MQ_ERR_ALIGNMENT;
+  }
+  DevInfo *di = nullptr;
+  if ((st = dev_info(&di)) != MQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mq::ConvParams p = base_params(desc, mq::OP_FWD, di->status);
+  p.a = operand(xq);
+  p.b = operand(wq);
+  p.pre_mult = pre_mult(xq->fmt, wq->fmt);
+  p.out = y;
+  if (rq) {
+    p.rq.codes = static_cast<uint8_t *>(rq->out->codes);
+    p.rq.scales = rq->out->scales;
+    p.rq.s_t_out = rq->out->s_t;
+    p.rq.amax_in = rq->amax_in;
+    p.rq.amax_out_bits = reinterpret_cast<uint32_t *>(rq->amax_out);
+    p.rq.fmt = rq->fmt;
+    if (rq->amax_out && cudaMemsetAsync(rq->amax_out, 0, sizeof(float), s) != cudaSuccess) return MQ_ERR_CUDA;
+  }
+  mq::conv_plan(p);
+  if (mq::launch_conv(p, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
+  return MQ_OK;
+}
+
+mq_status mqconv_dgrad(const mq_conv_desc *desc, const mq_packed *wq, const mq_packed *dyq, float *dx,
+                       mq_stream stream) {
+  mq_status st = check_desc(desc);
+  if (st != MQ_OK) return st;
+  const int64_t Ho = out_dim(desc->H, desc->Kh, desc->stride, desc->pad);
+  const int64_t Wo = out_dim(desc->W, desc->Kw, desc->stride, desc->pad);
+  if ((st = check_packed(wq, MQ_ROLE_WEIGHT, desc->Cout, desc->Cin, desc->Kh, desc->Kw)) != MQ_OK) return st;
+  if ((st = check_packed(dyq, MQ_ROLE_GRAD, desc->N, desc->Cout, Ho, Wo)) != MQ_OK) return st;
+  if (!dx) return MQ_ERR_INVALID_ARG;
+  if (!aligned16(dx)) return MQ_ERR_ALIGNMENT;
+  DevInfo *di = nullptr;
+  if ((st = dev_info(&di)) != MQ_OK) return st;
+  mq::ConvParams p = base_params(desc, mq::OP_DGRAD, di->status);
+  p.a = operand(dyq);
+  p.b = operand(wq);
+  p.pre_mult = pre_mult(dyq->fmt, wq->fmt);
+  p.out = dx;
+  mq::conv_plan(p);
+  if (mq::launch_conv(p, di->num_sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MQ_ERR_CUDA;
+  return MQ_OK;
+}
+
+size_t mqconv_wgrad_workspace_bytes(const mq_conv_desc *desc) {
+  if (check_desc(desc) != MQ_OK) return 0;
+  return wgrad_ws_bytes(desc);
+}
+
+mq_status mqconv_wgrad(const mq_conv_desc *desc, const mq_packed *dyq, const mq_packed *xq, float *dw,
+                       void *workspace, size_t ws_bytes, mq_stream stream) {
+  mq_status st = check_desc(desc);
+  if (st != MQ_OK) return st;
+  const int64_t Ho = out_dim(desc->H, desc->Kh, desc->stride, desc->pad);
+  const int64_t Wo = out_dim(desc->W, desc->Kw, desc->stride, desc->pad);
+  if ((st = check_packed(dyq, MQ_ROLE_GRAD, desc->N, desc->Cout, Ho, Wo)) != MQ_OK) return st;
+  if ((st = check_packed(xq, MQ_ROLE_ACT, desc->N, desc->Cin, desc->H, desc->W)) != MQ_OK) return st;
+  if (!dw) return MQ_ERR_INVALID_ARG;
+  if (!aligned16(dw)) return MQ_ERR_ALIGNMENT;
+  if (!workspace || ws_bytes < wgrad_ws_bytes(desc)) return MQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MQ_ERR_ALIGNMENT;
+  DevInfo *di = nullptr;
+  if ((st = dev_info(&di)) != MQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mq::ConvParams p = base_params(desc, mq::OP_WGRAD, di->status);
+  p.a = operand(dyq);
+  p.b = operand(xq);
+  p.pre_mult = pre_mult(dyq->fmt, xq->fmt);
+  p.out = static_cast<float *>(workspace);
+  mq::conv_plan(p);
+  if (mq::launch_conv(p, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
+  if (mq::launch_wgrad_reduce(p, dw, s) != cudaSuccess) return MQ_ERR_CUDA;
+  return MQ_OK;
+}
+
+mq_status mqconv_device_status(mq_stream stream, int32_t *host_status) {
+  if (!host_status) return MQ_ERR_INVALID_ARG;
+  DevInfo *di = nullptr;
+  mq_status st = dev_info(&di);
+  if (st != MQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, di->status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MQ_ERR_CUDA;
+  if (cudaMemsetAsync(di->status, 0, sizeof(uint32_t), s) != cudaSuccess) return MQ_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MQ_ERR_CUDA;
+  *host_status = (int32_t)v;
+  return MQ_OK;
+}
+
+}  // extern "C"

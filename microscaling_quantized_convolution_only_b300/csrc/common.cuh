@@ -1,0 +1,210 @@
+// common.cuh -- device helpers shared by the quantizer and the convolution kernels.
+//
+//  * element-format traits and exact round-to-nearest of a real quotient
+//    (MicroQonv §III-A: B_scale = CastE4M3(amax / (maxB_ef T_scale)),
+//    X^q = Round(X / (B_scale T_scale))), built on the sm_100-family
+//    conversion instructions plus an exact fma-sign tie-break;
+//  * decode of one packed 8x8 block row into eight fp16 values (code x B_scale
+//    is exact in fp16 for every format used here, see DecodeScale below);
+//  * bounded mbarrier waits and the tcgen05 / TMEM PTX wrappers.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace mq {
+
+// status bits, OR-ed into the device status word (mirror of mq_status values)
+constexpr uint32_t ST_NONFINITE = 1u << 4;
+constexpr uint32_t ST_TIMEOUT = 1u << 5;
+
+// ------------------------------------------------------------------ formats
+template <int FMT> struct Fmt;
+template <> struct Fmt<4> {   // E2M1 (NVFP4 element)
+  static constexpr int BLOCK_BYTES = 32;
+  static constexpr float EMAX = 6.0f;
+  static constexpr float DENOM = 2688.0f;     // maxB_ef * 448
+  static constexpr uint32_t SBIT = 0x8, MAG = 0x7;
+};
+template <> struct Fmt<6> {   // E2M3 (6-bit element)
+  static constexpr int BLOCK_BYTES = 48;
+  static constexpr float EMAX = 7.5f;
+  static constexpr float DENOM = 3360.0f;
+  static constexpr uint32_t SBIT = 0x20, MAG = 0x1F;
+};
+template <> struct Fmt<8> {   // E4M3 element (8-bit variant)
+  static constexpr int BLOCK_BYTES = 64;
+  static constexpr float EMAX = 448.0f;
+  static constexpr float DENOM = 200704.0f;
+  static constexpr uint32_t SBIT = 0x80, MAG = 0x7F;
+};
+
+// Two fp32 -> two codes, round-to-nearest-even, saturating.  The returned
+// value holds the code of `lo` in its low container (low nibble for E2M1,
+// low byte for E2M3/E4M3) and the code of `hi` in the next one.
+template <int FMT> __device__ __forceinline__ uint32_t cvt2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t cvt2<4>(float lo, float hi) {
+  uint32_t r;
+  asm("{ .reg .b8 q; cvt.rn.satfinite.e2m1x2.f32 q, %1, %2; cvt.u32.u8 %0, q; }" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+template <> __device__ __forceinline__ uint32_t cvt2<6>(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+template <> __device__ __forceinline__ uint32_t cvt2<8>(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two codes (low / high container as above) -> two exact fp16 values.
+template <int FMT> __device__ __forceinline__ uint32_t dec2(uint32_t pair);
+template <> __device__ __forceinline__ uint32_t dec2<4>(uint32_t pair) {
+  uint32_t r;
+  asm("{ .reg .b8 q; .reg .b16 w; cvt.u16.u32 w, %1; cvt.u8.u16 q, w; cvt.rn.f16x2.e2m1x2 %0, q; }"
+      : "=r"(r) : "r"(pair));
+  return r;
+}
+template <> __device__ __forceinline__ uint32_t dec2<6>(uint32_t pair) {
+  uint32_t r;
+  asm("{ .reg .b16 w; cvt.u16.u32 w, %1; cvt.rn.f16x2.e2m3x2 %0, w; }" : "=r"(r) : "r"(pair));
+  return r;
+}
+template <> __device__ __forceinline__ uint32_t dec2<8>(uint32_t pair) {
+  uint32_t r;
+  asm("{ .reg .b16 w; cvt.u16.u32 w, %1; cvt.rn.f16x2.e4m3x2 %0, w; }" : "=r"(r) : "r"(pair));
+  return r;
+}
+
+// magnitude value of one code of format FMT (exact)
+template <int FMT> __device__ __forceinline__ float code_value(uint32_t mag) {
+  uint32_t h = dec2<FMT>(mag);
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
+// Relative half-width of the bracket [q(1-eps), q(1+eps)] that is sure to
+// contain the exact quotient when q is computed with a few fp32 roundings.
+constexpr float QEPS = 9.5367431640625e-07f;   // 2^-20
+
+// Exact RN-even of the real quotient a / (k * s_t) onto the format grid, given
+// the codes c_lo, c_hi of the bracket ends.  When they differ, the two are
+// adjacent grid points and the one whose side of their midpoint `a` lies on
+// is chosen; the comparison a <> mid * k * s_t is exact because mid * k is
+// exact in fp32 (few significant bits) and fma rounds the exact difference
+// once, which preserves its sign (and zero).  Inputs non-negative.
+template <int FMT> __device__ __noinline__ uint32_t resolve_tie(float a, float k, float s_t, uint32_t c_lo,
+                                                                 uint32_t c_hi) {
+  uint32_t lo = c_lo < c_hi ? c_lo : c_hi, hi = c_lo < c_hi ? c_hi : c_lo;
+  float mid = 0.5f * (code_value<FMT>(lo) + code_value<FMT>(hi));
+  float r = fmaf(-(mid * k), s_t, a);
+  if (r > 0.0f) return hi;
+  if (r < 0.0f) return lo;
+  return (lo & 1u) ? hi : lo;
+}
+
+// Block scale code: RN_E4M3(amax_b / (maxB_ef * s_t)), satfinite, exact.
+template <int FMT> __device__ __forceinline__ uint32_t block_scale_code(float amax_b, float s_t) {
+  if (!(s_t > 0.0f)) return 0u;
+  float q = __fdiv_rn(amax_b, Fmt<FMT>::EMAX * s_t);
+  uint32_t c_lo = cvt2<8>(q * (1.0f - QEPS), 0.0f) & 0xFFu;
+  uint32_t c_hi = cvt2<8>(q * (1.0f + QEPS), 0.0f) & 0xFFu;
+  if (c_lo == c_hi) return c_lo;
+  return resolve_tie<8>(amax_b, Fmt<FMT>::EMAX, s_t, c_lo, c_hi);
+}
+
+// ------------------------------------------------------------- misc device
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; gives up after
+// `limit_ns` of wall time, sets ST_TIMEOUT in *status and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                          uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (globaltimer_ns() - t0 > limit_ns) {
+        atomicOr(status, ST_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// whole warp: allocate `ncols` TMEM columns (power of two >= 32), address -> *slot
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+
+// Shared-memory matrix descriptor, no swizzle.  lbo: byte distance between
+// core matrices adjacent along K; sbo: along M/N.  Bits 46-48 = 0b001.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+// arrive on `bar` once every tcgen05 op issued so far by this thread completed
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns per thread
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+}  // namespace mq

@@ -1,0 +1,69 @@
+// kernels.h -- host-side launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mq {
+
+// bytes of one packed 8x8 block for element format fmt (4, 6 or 8 bits)
+__host__ __device__ constexpr int block_bytes(int fmt) { return fmt == 4 ? 32 : fmt == 6 ? 48 : 64; }
+
+struct QuantParams {
+  int64_t d0, d1, d2, d3;          // ACT/GRAD: N, C, H, W; WEIGHT: Cout, Cin, Kh, Kw
+  uint8_t *codes;
+  uint8_t *scales;
+  float *s_t_out;
+  const uint32_t *amax_src_bits;   // statistic T_scale is built from (fp32 bits)
+  uint32_t *amax_meas_bits;        // nullable: receives max |x| (atomic max of fp32 bits)
+  uint32_t *status;
+};
+
+enum ConvOp : int { OP_FWD = 0, OP_DGRAD = 1, OP_WGRAD = 2 };
+
+struct Operand {
+  const uint8_t *codes;
+  const uint8_t *scales;
+  const float *s_t;
+  int fmt;
+};
+
+struct Requant {                   // fused requantizing epilogue of the forward conv
+  uint8_t *codes;
+  uint8_t *scales;
+  float *s_t_out;
+  const float *amax_in;
+  uint32_t *amax_out_bits;         // nullable
+  int fmt;
+};
+
+struct ConvParams {
+  int op;
+  // geometry
+  int N, Cin, H, W, Cout, Kh, Kw, stride, pad, Ho, Wo;
+  int NG, CIG, COG;
+  // operands: fwd (A = X, B = W), dgrad (A = dY, B = W), wgrad (A = dY, B = X)
+  Operand a, b;
+  float pre_mult;                  // undoes the operand pre-scaling of the decode
+  float *out;                      // fwd: Y HWCN (nullable with rq); dgrad: dX HWCN; wgrad: partial sums
+  Requant rq;                      // rq.codes == nullptr: no fused epilogue
+  // tiling
+  int BN;                          // columns per tile (multiple of 16, <= 256)
+  int acc_stride;                  // TMEM columns per accumulator buffer (power of two)
+  int m_tiles, n_tiles, k_splits;
+  int kg_total;                    // fwd: taps*CIG; wgrad: Ho*Wo*NG
+  int kg_per_split;                // wgrad
+  int wg_rows;                     // wgrad: Cout rounded to 128 (partial-sum row pitch = Cout)
+  int ncols;                       // wgrad: Kh*Kw*Cin
+  uint32_t *status;
+};
+
+cudaError_t launch_amax(const void *src, int dtype, int64_t n, uint32_t *amax_bits, int num_sms, cudaStream_t s);
+cudaError_t launch_quantize(const void *src, int dtype, int layout, int fmt, const QuantParams &p, cudaStream_t s);
+
+// Fills the tiling fields of p for `num_sms` and returns the number of tiles.
+int64_t conv_plan(ConvParams &p);
+size_t conv_smem_bytes(const ConvParams &p);
+cudaError_t launch_conv(const ConvParams &p, int num_sms, cudaStream_t s);
+cudaError_t launch_wgrad_reduce(const ConvParams &p, float *dw, cudaStream_t s);
+
+}  // namespace mq

@@ -1,0 +1,276 @@
+// quantize.cu -- quantize a dense tensor once into packed square 8x8 blocks.
+//
+// MicroQonv §III-A / §IV-B: T_scale = amax / (maxB_ef * 448); per 8x8 block
+// B_scale = CastE4M3(amax_block / (maxB_ef * T_scale)); codes
+// Round(x / (B_scale * T_scale)).  Blocks span (N, C_in) for activations,
+// (C_out, C_in) for weights and (N, C_out) for output gradients and are stored
+// channel-batch-first (§IV-A): block order [H][W][N/8][C/8], element i = 8n + c.
+//
+// One thread owns one block: it loads the block's 64 inputs straight from
+// global memory (for NCHW inputs consecutive lanes own consecutive spatial
+// positions, so each of the 64 loads is a coalesced warp-wide row segment; for
+// HWCN inputs each lane reads eight 8-element rows), reduces the block amax in
+// registers, derives the E4M3 block scale exactly, converts the codes with the
+// hardware RN conversions on a bracket [q(1-eps), q(1+eps)] of the quotient
+// and resolves the rare bracket that straddles a rounding midpoint with an
+// exact fma-sign test.  Codes and the scale byte are written once.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mq {
+
+__device__ __forceinline__ float load_elem(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float load_elem(const __nv_bfloat16 *p) { return __bfloat162float(__ldg(p)); }
+
+// ------------------------------------------------------------------ amax
+// max |x| over a flat array; the fp32 bit patterns of |x| order like the
+// values (Inf and NaN above every finite value), so an unsigned max works.
+template <typename T>
+__global__ void __launch_bounds__(256) amax_kernel(const T *__restrict__ src, int64_t n, uint32_t *amax_bits) {
+  uint32_t m = 0;
+  constexpr int V = 16 / sizeof(T);
+  int64_t nv = n / V;
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nv; i += (int64_t)gridDim.x * blockDim.x) {
+    uint4 v = __ldg(s4 + i);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (sizeof(T) == 4) {
+        m = max(m, w[j] & 0x7FFFFFFFu);
+      } else {
+        m = max(m, (w[j] << 16) & 0x7FFFFFFFu);
+        m = max(m, w[j] & 0x7FFF0000u);
+      }
+    }
+  }
+  for (int64_t i = nv * V + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    m = max(m, __float_as_uint(fabsf(load_elem(src + i))));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (threadIdx.x == 0 && m) atomicMax(amax_bits, m);
+  }
+}
+
+// ------------------------------------------------------------- codes
+// Pack 64 codes of one block into its payload (layout in mqconv.h).
+template <int FMT> struct Packer;
+
+template <> struct Packer<4> {   // two codes per byte, element 2j in the low nibble
+  uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  __device__ __forceinline__ void put_pair(int j, uint32_t pair) {   // pair = c(2j) | c(2j+1) << 4
+    const int word = j >> 2, sh = (j & 3) * 8;
+    w[word] = (w[word] & ~(0xFFu << sh)) | (pair << sh);
+  }
+  __device__ __forceinline__ void store(uint8_t *dst) const {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+};
+
+template <> struct Packer<6> {   // little-endian stream of 6-bit codes
+  uint32_t p[32];                // pair j: c(2j) | c(2j+1) << 8 (8-bit containers)
+  __device__ __forceinline__ void put_pair(int j, uint32_t pair) { p[j] = pair; }
+  __device__ __forceinline__ void store(uint8_t *dst) const {
+    uint32_t w[12];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {     // 16 codes -> 96 bits -> 3 words
+      uint32_t t[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t a = p[g * 8 + 2 * k], b = p[g * 8 + 2 * k + 1];
+        t[k] = (a & 0x3Fu) | (((a >> 8) & 0x3Fu) << 6) | ((b & 0x3Fu) << 12) | (((b >> 8) & 0x3Fu) << 18);
+      }
+      w[g * 3 + 0] = t[0] | (t[1] << 24);
+      w[g * 3 + 1] = (t[1] >> 8) | (t[2] << 16);
+      w[g * 3 + 2] = (t[2] >> 16) | (t[3] << 8);
+    }
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    d[2] = make_uint4(w[8], w[9], w[10], w[11]);
+  }
+};
+
+template <> struct Packer<8> {   // one byte per code
+  uint32_t w[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+  __device__ __forceinline__ void put_pair(int j, uint32_t pair) {   // pair = c(2j) | c(2j+1) << 8
+    const int word = j >> 1, sh = (j & 1) * 16;
+    w[word] = (w[word] & ~(0xFFFFu << sh)) | (pair << sh);
+  }
+  __device__ __forceinline__ void store(uint8_t *dst) const {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) d[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  }
+};
+
+template <int FMT> __device__ __forceinline__ uint32_t pair_shift() { return FMT == 4 ? 4u : 8u; }
+
+// Codes of one block whose inputs are x[0..63] (in-block order), given its
+// scale value bs (fp32) and T_scale.  Returns nothing; fills the packer.
+template <int FMT>
+__device__ __forceinline__ void encode_block(const float (&x)[64], float bs, float s_t, Packer<FMT> &pk) {
+  float inv_lo = 0.0f, inv_hi = 0.0f;
+  if (bs > 0.0f) {
+    const float inv = __frcp_rn(bs * s_t);
+    inv_lo = inv * (1.0f - QEPS);
+    inv_hi = inv * (1.0f + QEPS);
+  }
+  uint32_t diff = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t lo = cvt2<FMT>(x[2 * j] * inv_lo, x[2 * j + 1] * inv_lo);
+    const uint32_t hi = cvt2<FMT>(x[2 * j] * inv_hi, x[2 * j + 1] * inv_hi);
+    diff |= lo ^ hi;
+    pk.put_pair(j, lo);
+  }
+  if (diff) {   // some quotient lies within the bracket of a rounding midpoint
+    const float k = bs;
+    const uint32_t cmask = (FMT == 4) ? 0xFu : 0xFFu;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t lo = cvt2<FMT>(x[2 * j] * inv_lo, x[2 * j + 1] * inv_lo);
+      const uint32_t hi = cvt2<FMT>(x[2 * j] * inv_hi, x[2 * j + 1] * inv_hi);
+      if (lo == hi) continue;
+      uint32_t pair = 0;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t sh = e * pair_shift<FMT>();
+        uint32_t cl = (lo >> sh) & cmask, ch = (hi >> sh) & cmask;
+        uint32_t c = cl;
+        if (cl != ch) {
+          const float v = x[2 * j + e];
+          c = resolve_tie<FMT>(fabsf(v), k, s_t, cl & Fmt<FMT>::MAG, ch & Fmt<FMT>::MAG) |
+              (signbit(v) ? Fmt<FMT>::SBIT : 0u);
+        }
+        pair |= c << sh;
+      }
+      pk.put_pair(j, pair);
+    }
+  }
+}
+
+// -------------------------------------------------------------- quantize
+// Thread order: NCHW/OIHW -- spatial position fastest; HWCN -- n-group fastest.
+template <int FMT, typename T, int LAYOUT>
+__global__ void __launch_bounds__(256) quantize_kernel(const T *__restrict__ src, QuantParams p) {
+  const int64_t GA = p.d0 / 8, GB = p.d1 / 8, HW = p.d2 * p.d3;
+  const int64_t nblk = GA * GB * HW;
+  const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+
+  // T_scale from the statistic (identical in every thread: one fp32 division)
+  const float amax_src = __uint_as_float(*p.amax_src_bits);
+  const float s_t = __fdiv_rn(amax_src, Fmt<FMT>::DENOM);
+  if (t == 0) {
+    *p.s_t_out = s_t;
+    if (!(amax_src <= 3.4028234663852886e38f)) atomicOr(p.status, ST_NONFINITE);
+  }
+
+  uint32_t my_amax = 0;
+  if (t < nblk) {
+    int64_t hw, ga, gb;
+    if (LAYOUT == 1) {   // HWCN
+      ga = t % GA;
+      gb = (t / GA) % GB;
+      hw = t / (GA * GB);
+    } else {
+      hw = t % HW;
+      gb = (t / HW) % GB;
+      ga = t / (HW * GB);
+    }
+    float x[64];
+    if (LAYOUT == 1) {
+      // [H][W][C][N]: row c holds 8 contiguous n
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const T *row = src + ((hw * p.d1 + gb * 8 + c) * p.d0 + ga * 8);
+        if (sizeof(T) == 4) {
+          const float4 a = __ldg(reinterpret_cast<const float4 *>(row));
+          const float4 b = __ldg(reinterpret_cast<const float4 *>(row) + 1);
+          x[0 * 8 + c] = a.x; x[1 * 8 + c] = a.y; x[2 * 8 + c] = a.z; x[3 * 8 + c] = a.w;
+          x[4 * 8 + c] = b.x; x[5 * 8 + c] = b.y; x[6 * 8 + c] = b.z; x[7 * 8 + c] = b.w;
+        } else {
+          const uint4 a = __ldg(reinterpret_cast<const uint4 *>(row));
+          const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            x[(2 * k) * 8 + c] = __uint_as_float(w[k] << 16);
+            x[(2 * k + 1) * 8 + c] = __uint_as_float(w[k] & 0xFFFF0000u);
+          }
+        }
+      }
+    } else {
+      // NCHW / OIHW: element (a, b) at ((a * d1 + b) * HW + hw)
+      const T *base = src + ((ga * 8) * p.d1 + gb * 8) * HW + hw;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) x[i] = load_elem(base + ((i >> 3) * p.d1 + (i & 7)) * HW);
+    }
+    // |x| bit patterns order like the values, with Inf and NaN above all finite ones
+    uint32_t mb = 0;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) mb = max(mb, __float_as_uint(x[i]) & 0x7FFFFFFFu);
+    my_amax = mb;
+    if (mb >= 0x7F800000u) atomicOr(p.status, ST_NONFINITE);
+    const float amax_b = __uint_as_float(mb);
+
+    const uint32_t bs_code = block_scale_code<FMT>(amax_b, s_t);
+    const float bs = code_value<8>(bs_code);
+    Packer<FMT> pk;
+    encode_block<FMT>(x, bs, s_t, pk);
+    const int64_t b = (hw * GA + ga) * GB + gb;
+    pk.store(p.codes + b * Fmt<FMT>::BLOCK_BYTES);
+    p.scales[b] = (uint8_t)bs_code;
+  }
+
+  if (p.amax_meas_bits) {
+    uint32_t m = my_amax;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0 && m) atomicMax(p.amax_meas_bits, m);
+  }
+}
+
+// ----------------------------------------------------------------- launch
+template <int FMT, typename T>
+static cudaError_t launch_q(const void *src, int layout, const QuantParams &p, cudaStream_t s) {
+  const int64_t nblk = (p.d0 / 8) * (p.d1 / 8) * p.d2 * p.d3;
+  const unsigned grid = (unsigned)((nblk + 255) / 256);
+  const T *x = static_cast<const T *>(src);
+  if (layout == 1) quantize_kernel<FMT, T, 1><<<grid, 256, 0, s>>>(x, p);
+  else quantize_kernel<FMT, T, 0><<<grid, 256, 0, s>>>(x, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax(const void *src, int dtype, int64_t n, uint32_t *amax_bits, int num_sms, cudaStream_t s) {
+  const int64_t per = dtype == 0 ? 4 : 8;
+  int64_t want = (n / per + 255) / 256;
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
+  if (dtype == 0) amax_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(src), n, amax_bits);
+  else amax_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), n, amax_bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const void *src, int dtype, int layout, int fmt, const QuantParams &p, cudaStream_t s) {
+  if (dtype == 0) {
+    if (fmt == 4) return launch_q<4, float>(src, layout, p, s);
+    if (fmt == 6) return launch_q<6, float>(src, layout, p, s);
+    return launch_q<8, float>(src, layout, p, s);
+  }
+  if (fmt == 4) return launch_q<4, __nv_bfloat16>(src, layout, p, s);
+  if (fmt == 6) return launch_q<6, __nv_bfloat16>(src, layout, p, s);
+  return launch_q<8, __nv_bfloat16>(src, layout, p, s);
+}
+
+}  // namespace mq

@@ -1,0 +1,117 @@
+"""GPU parity of mqconv_quantize_cbf: codes, scales and T_scale bit-exact
+against the oracle (MicroQonv §III-A, §IV-B), for every format, source layout
+and dtype, both statistic modes, edge cases, and the full-size tensors of the
+workloads."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as S
+from mqtest import assert_packed_equal, gpu_quantize, to_dev
+
+pytestmark = pytest.mark.gpu
+FMTS = ["e2m1", "e2m3", "e4m3"]
+
+
+def rand(shape, seed, scale=1.0):
+    return (np.random.default_rng(seed).standard_normal(shape) * scale).astype(np.float32)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(8, 16, 8, 8), (16, 24, 7, 5), (64, 32, 3, 9), (8, 8, 1, 1)])
+def test_nchw(cuda_device, fmt, dtype, shape):
+    x = rand(shape, sum(shape))
+    if dtype == "bf16":
+        x = S.to_bf16_rne(x)
+    x.ravel()[::5] = 0.0
+    x.ravel()[1::7] = -0.0
+    p, amax = gpu_quantize(to_dev(x, dtype, cuda_device), fmt, "act", "nchw", shape)
+    ref = oracle.quantize(x, fmt, "act", "nchw")
+    assert amax == ref["amax"]
+    assert_packed_equal(p, ref, f"nchw {fmt} {dtype} {shape}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 3, 16, 8), (5, 4, 24, 32), (1, 1, 8, 64)])
+def test_hwcn(cuda_device, fmt, dtype, shape):
+    x = rand(shape, 7 + sum(shape), 3.0)
+    if dtype == "bf16":
+        x = S.to_bf16_rne(x)
+    H, W, C, N = shape
+    p, _ = gpu_quantize(to_dev(x, dtype, cuda_device), fmt, "grad", "hwcn", (N, C, H, W))
+    assert_packed_equal(p, oracle.quantize(x, fmt, "grad", "hwcn"), f"hwcn {fmt} {dtype} {shape}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(16, 16, 3, 3), (32, 8, 1, 1), (8, 64, 5, 5)])
+def test_oihw(cuda_device, fmt, shape):
+    x = rand(shape, 3 + sum(shape), 0.05)
+    p, _ = gpu_quantize(to_dev(x, "f32", cuda_device), fmt, "weight", "oihw", shape)
+    assert_packed_equal(p, oracle.quantize(x, fmt, "weight", "oihw"), f"oihw {fmt} {shape}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_supplied_statistic(cuda_device, fmt):
+    x = rand((16, 16, 4, 4), 99)
+    for factor in (1.7, 0.3):
+        amax_in = float(np.float32(np.abs(x).max() * factor))
+        p, amax = gpu_quantize(to_dev(x, "f32", cuda_device), fmt, "act", "nchw", x.shape, amax_in=amax_in)
+        ref = oracle.quantize(x, fmt, "act", "nchw", amax_in=amax_in)
+        assert amax == ref["amax"]
+        assert_packed_equal(p, ref, f"supplied statistic x{factor}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_rounding_midpoints(cuda_device, fmt):
+    """Inputs exactly on, and one ulp either side of, every rounding midpoint."""
+    from test_oracle_quantizer import midpoint_tensor
+    x = midpoint_tensor(fmt)
+    p, _ = gpu_quantize(to_dev(x, "f32", cuda_device), fmt, "act", "nchw", x.shape)
+    assert_packed_equal(p, oracle.quantize(x, fmt, "act", "nchw"), "midpoints")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_lossless_round_trip_values(cuda_device, fmt):
+    """Quotients landing exactly on grid points and scale midpoints (a dense
+    sweep of values k * 2^-j with few significant bits)."""
+    rng = np.random.default_rng(5)
+    x = (rng.integers(-64, 65, (16, 16, 4, 4)) * 2.0 ** -5).astype(np.float32)
+    x[0, 0, 0, 0] = 448.0
+    p, _ = gpu_quantize(to_dev(x, "f32", cuda_device), fmt, "act", "nchw", x.shape)
+    assert_packed_equal(p, oracle.quantize(x, fmt, "act", "nchw"), "grid values")
+
+
+def test_zero_tensor(cuda_device):
+    x = np.zeros((8, 8, 2, 2), dtype=np.float32)
+    x[:4] = -0.0
+    p, amax = gpu_quantize(to_dev(x, "f32", cuda_device), "e2m1", "act", "nchw", x.shape)
+    assert amax == 0.0
+    assert_packed_equal(p, oracle.quantize(x, "e2m1", "act", "nchw"), "zeros")
+
+
+def test_nonfinite_sets_status(cuda_device):
+    import microscaling_quantized_convolution_only_b300 as mq
+    x = np.ones((8, 8, 2, 2), dtype=np.float32)
+    x[1, 2, 1, 0] = np.nan
+    xd = to_dev(x, "f32", cuda_device)
+    p = mq.Packed("e2m1", "act", x.shape, device=cuda_device)
+    amax = torch.zeros(1, device=cuda_device)
+    mq.quantize_cbf(xd, "nchw", p, amax_out=amax)
+    st = mq.device_status()
+    assert st & (1 << 4)
+    assert mq.device_status() == 0    # cleared by the read
+
+
+@pytest.mark.parametrize("wl_layer", [(2, 0), (3, 0), (4, 0), (5, 0)], ids=["r18-56", "yolo-320", "stack-fp4", "stack-fp6"])
+def test_full_size_activation(cuda_device, wl_layer):
+    """The largest activation tensor of each big workload, compared in full."""
+    wl = S.WORKLOADS[wl_layer[0]]
+    L = wl.layers[wl_layer[1]]
+    x = S.draw_x(wl, wl_layer[1])
+    p, amax = gpu_quantize(to_dev(x, wl.dtype, cuda_device), wl.fmt, "act", "nchw", L.x_shape())
+    ref = oracle.quantize(x, wl.fmt, "act", "nchw")
+    assert amax == ref["amax"]
+    assert_packed_equal(p, ref, f"{wl.name} X")
