@@ -1,0 +1,599 @@
+"""Benchmark of the MicroQonv quantize-once convolution hot path on B300.
+
+A step is one pass of the whole path over one batch of synthetic input: every
+tensor quantized once into 8x8 channel-batch-first blocks, then the forward,
+data-gradient and weight-gradient implicit-im2col GEMMs on the packed blocks.
+
+Default workload: the chained 4-layer stack (N=256, 56x56, C 128->128, 3x3,
+stride 1, pad 1, bf16 inputs, NVFP4): quantize X0 and W0..W3, forward through
+the four layers with the fused epilogue requantizing Y_l into X_{l+1} (its
+T_scale from the previous step's amax, Hindsight-style), quantize dY3, then
+wgrad + dgrad of layers 3..0 with each dX_l (fp32) requantized into dY_{l-1}.
+
+value = algorithmic conv TFLOP/s of the whole step (quantization included in
+the step time); per-op throughputs, the quantizer's GB/s and the roofline of
+the dominant kernel are reported beside it.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                       [--workload NAME]
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU
+(replicas; no data-path collective), value sums all ranks' work over the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic as S  # noqa: E402
+
+METRIC = "conv fwd/dgrad/wgrad TFLOP/s + quantizer GB/s, % of roofline, 1 B300"
+BITS = {"e2m1": 4.125, "e2m3": 6.125, "e4m3": 8.125}
+WORKLOADS = {
+    "stack4-nvfp4": 4, "stack4-fp6": 5, "resnet32-cifar": 1, "resnet18-224": 2, "yolov8n-640-fp8": 3,
+    "tiny-3x3": 0,
+}
+
+
+def packed_bytes(fmt, elems):
+    return elems * BITS[fmt] / 8.0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of this GPU's clocks and throttle reasons every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        import torch
+        self.proc = None
+        self.lines = []
+        try:
+            prop = torch.cuda.get_device_properties(device_index)
+            bus = f"{prop.pci_domain_id:08X}:{prop.pci_bus_id:02X}:{prop.pci_device_id:02X}.0"
+            self.cmd = ["nvidia-smi", f"--id={bus}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                        "-lms", "200"]
+        except Exception:
+            self.cmd = None
+
+    def start(self):
+        if not self.cmd:
+            return
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- timing
+class NullTimer:
+    def begin(self, name):
+        pass
+
+    def end(self):
+        pass
+
+
+class OpTimer:
+    """CUDA events around each op group, on the current (launching) stream."""
+
+    def __init__(self):
+        import torch
+        self.torch = torch
+        self.pairs = []
+        self.cur = None
+
+    def begin(self, name):
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.cur = (name, e)
+
+    def end(self):
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.pairs.append((self.cur[0], self.cur[1], e))
+
+    def times(self):
+        out = {}
+        for name, a, b in self.pairs:
+            out.setdefault(name, []).append(a.elapsed_time(b))
+        return out
+
+
+# --------------------------------------------------------------- workloads
+class StackStep:
+    """The chained-stack training step (see module docstring)."""
+
+    def __init__(self, wl, device):
+        import torch
+        import microscaling_quantized_convolution_only_b300 as mq
+        self.mq, self.torch, self.wl, self.dev = mq, torch, wl, device
+        L = wl.layers[0]
+        self.L = L
+        fmt = wl.fmt
+        self.fmt = fmt
+        tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        nl = len(wl.layers)
+        # inputs resident in HBM: X0, W0..W3 (bf16), dY3 (bf16)
+        self.h_x0 = torch.from_numpy(S.draw_x(wl, 0)).to(tdt)
+        self.h_w = [torch.from_numpy(S.draw_w(wl, l)).to(tdt) for l in range(nl)]
+        self.h_dy = torch.from_numpy(S.draw_dy(wl, nl - 1)).to(tdt)
+        self.x0 = self.h_x0.to(device)
+        self.w = [t.to(device) for t in self.h_w]
+        self.dy = self.h_dy.to(device)
+        self.xq = [mq.Packed(fmt, "act", L.x_shape(), device=device) for _ in range(nl)]
+        self.wq = [mq.Packed(fmt, "weight", L.w_shape(), device=device) for _ in range(nl)]
+        self.gq = [mq.Packed(fmt, "grad", L.y_shape(), device=device) for _ in range(nl)]
+        self.y_last = torch.empty((L.Ho, L.Wo, L.Cout, L.N), dtype=torch.float32, device=device)
+        self.dx = torch.empty((L.H, L.W, L.Cin, L.N), dtype=torch.float32, device=device)
+        self.dw = [torch.empty(L.w_shape(), dtype=torch.float32, device=device) for _ in range(nl)]
+        self.ws = torch.empty(mq.wgrad_workspace_bytes(L), dtype=torch.uint8, device=device)
+        self.amax = torch.zeros(16, dtype=torch.float32, device=device)        # exact-mode amax outputs
+        self.y_stat = torch.ones(nl, dtype=torch.float32, device=device)       # hindsight statistics of Y_l
+        self.y_amax = torch.zeros(nl, dtype=torch.float32, device=device)
+        self.nl = nl
+        # accounting
+        n_el = int(np.prod(L.x_shape()))
+        w_el = int(np.prod(L.w_shape()))
+        self.flops = {"fwd": nl * L.flops, "dgrad": nl * L.flops, "wgrad": nl * L.flops}
+        in_b = 2 if wl.dtype == "bf16" else 4
+        self.qbytes = {   # algorithmic bytes: one read of the input + the packed output
+            "quant_bf16": 2 * (n_el * in_b + packed_bytes(fmt, n_el)) + nl * (w_el * in_b + packed_bytes(fmt, w_el)),
+            "quant_f32": (nl - 1) * (n_el * 4 + packed_bytes(fmt, n_el)),
+        }
+        self.conv_bytes = {
+            "fwd": (nl - 1) * (2 * packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el)) +
+                   (packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el) + 4 * n_el),
+            "dgrad": nl * (packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el) + 4 * n_el),
+            "wgrad": nl * (2 * packed_bytes(fmt, n_el) + 4 * w_el),
+        }
+        self.launches_per_step = (2 + 2 * nl) + nl + 2 + 2 * nl + nl + 2 * (nl - 1)
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in [self.h_x0, self.h_dy] + self.h_w)
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.dw)
+
+    def run(self, tm=None):
+        """Enqueue one step on the current stream.  tm: optional OpTimer
+        bracketing each op with CUDA events."""
+        mq, L, nl = self.mq, self.L, self.nl
+        tm = tm or NullTimer()
+        # quantize X0 and the weights (exact two-pass statistics)
+        tm.begin("quant")
+        mq.quantize_cbf(self.x0, "nchw", self.xq[0], amax_out=self.amax[0:1])
+        for l in range(nl):
+            mq.quantize_cbf(self.w[l], "oihw", self.wq[l], amax_out=self.amax[1 + l:2 + l])
+        tm.end()
+        # forward: fused requantization of Y_l into X_{l+1}
+        for l in range(nl):
+            tm.begin("fwd")
+            if l < nl - 1:
+                mq.fwd(L, self.xq[l], self.wq[l], None, rq_out=self.xq[l + 1], rq_amax_in=self.y_stat[l:l + 1],
+                       rq_amax_out=self.y_amax[l:l + 1])
+            else:
+                mq.fwd(L, self.xq[l], self.wq[l], self.y_last)
+            tm.end()
+        # backward
+        tm.begin("quant")
+        mq.quantize_cbf(self.dy, "nchw", self.gq[nl - 1], amax_out=self.amax[8:9])
+        tm.end()
+        for l in range(nl - 1, -1, -1):
+            tm.begin("wgrad")
+            mq.wgrad(L, self.gq[l], self.xq[l], self.dw[l], self.ws)
+            tm.end()
+            tm.begin("dgrad")
+            mq.dgrad(L, self.wq[l], self.gq[l], self.dx)
+            tm.end()
+            if l > 0:
+                tm.begin("quant")
+                mq.quantize_cbf(self.dx, "hwcn", self.gq[l - 1], amax_out=self.amax[9 + l:10 + l])
+                tm.end()
+        # hindsight: next step's statistics are this step's measured amax
+        self.y_stat.copy_(self.y_amax)
+
+    def upload(self, pinned):
+        """e2e: host -> device copies of the step's inputs."""
+        self.x0.copy_(pinned["x0"], non_blocking=True)
+        self.dy.copy_(pinned["dy"], non_blocking=True)
+        for l in range(self.nl):
+            self.w[l].copy_(pinned["w"][l], non_blocking=True)
+
+    def download(self, pinned):
+        for l in range(self.nl):
+            pinned["dw"][l].copy_(self.dw[l], non_blocking=True)
+
+    def pinned(self):
+        return {"x0": self.h_x0.pin_memory(), "dy": self.h_dy.pin_memory(),
+                "w": [t.pin_memory() for t in self.h_w], "dw": [t.cpu().pin_memory() for t in self.dw]}
+
+
+class LayersStep:
+    """Per-layer workloads (configs 0-3): every layer's X, W, dY quantized once
+    from fp32/bf16 NCHW/OIHW, then fwd, dgrad and wgrad of every layer."""
+
+    def __init__(self, wl, device):
+        import torch
+        import microscaling_quantized_convolution_only_b300 as mq
+        self.mq, self.torch, self.wl, self.dev = mq, torch, wl, device
+        tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        self.layers = []
+        self.flops = {"fwd": 0, "dgrad": 0, "wgrad": 0}
+        self.conv_bytes = {"fwd": 0.0, "dgrad": 0.0, "wgrad": 0.0}
+        self.qbytes = {"quant": 0.0}
+        self.h2d_bytes = self.d2h_bytes = 0
+        in_b = 2 if wl.dtype == "bf16" else 4
+        fmt = wl.fmt
+        for li, L in enumerate(wl.layers):
+            h = [torch.from_numpy(a).to(tdt) for a in (S.draw_x(wl, li), S.draw_w(wl, li), S.draw_dy(wl, li))]
+            d = dict(L=L, h=h, x=h[0].to(device), w=h[1].to(device), dy=h[2].to(device),
+                     xq=mq.Packed(fmt, "act", L.x_shape(), device=device),
+                     wq=mq.Packed(fmt, "weight", L.w_shape(), device=device),
+                     gq=mq.Packed(fmt, "grad", L.y_shape(), device=device),
+                     y=torch.empty((L.Ho, L.Wo, L.Cout, L.N), device=device),
+                     dx=torch.empty((L.H, L.W, L.Cin, L.N), device=device),
+                     dw=torch.empty(L.w_shape(), device=device),
+                     ws=torch.empty(max(16, mq.wgrad_workspace_bytes(L)), dtype=torch.uint8, device=device),
+                     amax=torch.zeros(4, device=device))
+            self.layers.append(d)
+            xe, we, ye = (int(np.prod(s)) for s in (L.x_shape(), L.w_shape(), L.y_shape()))
+            for k in self.flops:
+                self.flops[k] += L.flops
+            self.conv_bytes["fwd"] += packed_bytes(fmt, xe) + packed_bytes(fmt, we) + 4 * ye
+            self.conv_bytes["dgrad"] += packed_bytes(fmt, we) + packed_bytes(fmt, ye) + 4 * xe
+            self.conv_bytes["wgrad"] += packed_bytes(fmt, ye) + packed_bytes(fmt, xe) + 4 * we
+            self.qbytes["quant"] += (xe + we + ye) * in_b + packed_bytes(fmt, xe + we + ye)
+            self.h2d_bytes += (xe + we + ye) * in_b
+            self.d2h_bytes += we * 4
+        self.launches_per_step = len(self.layers) * (6 + 1 + 1 + 2)
+
+    def run(self, tm=None):
+        mq = self.mq
+        tm = tm or NullTimer()
+        for d in self.layers:
+            L = d["L"]
+            tm.begin("quant")
+            mq.quantize_cbf(d["x"], "nchw", d["xq"], amax_out=d["amax"][0:1])
+            mq.quantize_cbf(d["w"], "oihw", d["wq"], amax_out=d["amax"][1:2])
+            mq.quantize_cbf(d["dy"], "nchw", d["gq"], amax_out=d["amax"][2:3])
+            tm.end()
+            tm.begin("fwd")
+            mq.fwd(L, d["xq"], d["wq"], d["y"])
+            tm.end()
+            tm.begin("dgrad")
+            mq.dgrad(L, d["wq"], d["gq"], d["dx"])
+            tm.end()
+            tm.begin("wgrad")
+            mq.wgrad(L, d["gq"], d["xq"], d["dw"], d["ws"])
+            tm.end()
+
+    def upload(self, pinned):
+        for d, p in zip(self.layers, pinned["in"]):
+            for dst, src in zip((d["x"], d["w"], d["dy"]), p):
+                dst.copy_(src, non_blocking=True)
+
+    def download(self, pinned):
+        for d, p in zip(self.layers, pinned["dw"]):
+            p.copy_(d["dw"], non_blocking=True)
+
+    def pinned(self):
+        return {"in": [[t.pin_memory() for t in d["h"]] for d in self.layers],
+                "dw": [d["dw"].cpu().pin_memory() for d in self.layers]}
+
+
+def make_step(wl, device):
+    return StackStep(wl, device) if wl.chained else LayersStep(wl, device)
+
+
+# -------------------------------------------------------------- GPU arm
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value, world, device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_gpu(args):
+    import torch
+    import microscaling_quantized_convolution_only_b300 as mq
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    wl = S.WORKLOADS[WORKLOADS[args.workload]]
+    step = make_step(wl, device)
+    peaks = load_peaks()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)   # > 126 MB L2
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    mq.check_device_status()
+
+    # ---- device-timed steps (inputs resident in HBM)
+    groups = ["quant", "fwd", "dgrad", "wgrad"]
+    per_kernel = {g: [] for g in groups}
+    step_ms = []
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    for _ in range(args.steps):
+        flush.zero_()                                   # L2 flush between steps (outside the timing)
+        tm = OpTimer()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        step.run(tm)
+        s1.record()
+        torch.cuda.synchronize()
+        step_ms.append(s0.elapsed_time(s1))
+        for g, v in tm.times().items():
+            per_kernel[g].extend(v)
+    clk = clocks.stop()
+    barrier(world)
+    mq.check_device_status()
+
+    total_ms = sum(step_ms)
+    total_ms_max = max_over_ranks(total_ms, world, device)
+    flops_step = sum(step.flops.values())
+    value = world * flops_step * args.steps / (total_ms_max * 1e-3) / 1e12
+
+    def mean(v):
+        return sum(v) / len(v) if v else float("nan")
+
+    ops = {}
+    for op in ("fwd", "dgrad", "wgrad"):
+        t_ms = mean(per_kernel[op]) * len(per_kernel[op]) / args.steps    # per step
+        n_launch = len(per_kernel[op]) / args.steps
+        ops[op] = {"ms_per_step": t_ms, "tflops": step.flops[op] / (t_ms * 1e-3) / 1e12,
+                   "gbs": step.conv_bytes[op] / (t_ms * 1e-3) / 1e9, "launches_per_step": n_launch,
+                   "ms_per_launch": t_ms / n_launch}
+    qt = sum(per_kernel["quant"]) / args.steps
+    qbytes = sum(step.qbytes.values())
+    ops["quantize"] = {"ms_per_step": qt, "gbs": qbytes / (qt * 1e-3) / 1e9,
+                       "frac_hbm": qbytes / (qt * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    for op in ("fwd", "dgrad", "wgrad"):
+        tf, gb = ops[op]["tflops"], ops[op]["gbs"]
+        t_roof = max(step.flops[op] / (peaks["bf16_tflops_sustained"] * 1e12),
+                     step.conv_bytes[op] / (peaks["hbm_gbs"] * 1e9))
+        ops[op]["frac_roofline"] = t_roof / (ops[op]["ms_per_step"] * 1e-3)
+        ops[op]["bound"] = "tensor" if step.flops[op] / (peaks["bf16_tflops_sustained"] * 1e12) >= \
+            step.conv_bytes[op] / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    dom = max(("fwd", "dgrad", "wgrad"), key=lambda o: ops[o]["ms_per_step"])
+    d = ops[dom]
+    if d["bound"] == "tensor":
+        achieved = step.flops[dom] / d["launches_per_step"] / (d["ms_per_launch"] * 1e-3) / 1e12
+        roof = {"kernel": f"conv_{dom}", "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 dense, sustained (fp16 MMA runs at the bf16 rate)"}
+    else:
+        achieved = step.conv_bytes[dom] / d["launches_per_step"] / (d["ms_per_launch"] * 1e-3) / 1e9
+        roof = {"kernel": f"conv_{dom}", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": f"{peaks['source']} HBM copy"}
+
+    # ---- end to end through the public API with host buffers
+    pinned = step.pinned()
+    e2e_ms = []
+    for _ in range(max(1, args.steps)):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        step.upload(pinned)
+        step.run()
+        step.download(pinned)
+        t1.record()
+        torch.cuda.synchronize()
+        e2e_ms.append(t0.elapsed_time(t1))
+    e2e_max = max_over_ranks(sum(e2e_ms), world, device)
+    e2e_value = world * flops_step * len(e2e_ms) / (e2e_max * 1e-3) / 1e12
+    mq.check_device_status()
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms_max / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": f"{wl.fmt} codes x e4m3 scales -> fp16 MMA, fp32 accumulate",
+        "data": "synthetic (seeded splitmix64/Box-Muller draws with the workload's distributions)",
+        "config": {"workload": wl.name, "layers": [L.name() for L in wl.layers], "element_format": wl.fmt,
+                   "input_dtype": wl.dtype, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed (256 MB write) before every timed step; inputs also exceed L2",
+                   "conv_flops_per_step": flops_step},
+        "ops": ops,
+        "roofline": roof,
+        "clocks": clk,
+        "gpu_launches": step.launches_per_step * args.steps,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": step.h2d_bytes,
+                "d2h_bytes_per_step": step.d2h_bytes, "ms_per_step": e2e_max / len(e2e_ms)},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------- CPU oracle arm
+def oracle_sample_step(wl, budget_s, state):
+    """A bounded sample of the workload on the CPU oracle: quantize a slice of
+    each input tensor, then 7-loop fp64 fwd/dgrad/wgrad outputs of the first
+    layer, one by one.  Returns (conv FLOPs done, seconds)."""
+    import oracle
+    L = wl.layers[0]
+    if "ops" not in state:
+        rng = np.random.default_rng(0)
+        # a batch slice of 8 keeps the sample's tensors small; taps see the full spatial extent
+        Ls = S.scaled_layer(L, N=8)
+        X = S.draw_x(wl, 0)[:8]
+        W = S.draw_w(wl, 0)
+        dY = S.draw_dy(wl, len(wl.layers) - 1)[:8]
+        state["ops"] = (Ls, X, W, dY)
+        state["idx_f"] = rng.integers(0, int(np.prod(Ls.y_shape())), 512)
+        state["idx_d"] = rng.integers(0, int(np.prod(Ls.x_shape())), 512)
+        state["idx_w"] = rng.integers(0, int(np.prod(Ls.w_shape())), 16)
+    Ls, X, W, dY = state["ops"]
+    t0 = time.perf_counter()
+    qx = oracle.quantize(X, wl.fmt, "act", "nchw")
+    qw = oracle.quantize(W, wl.fmt, "weight", "oihw")
+    qg = oracle.quantize(dY, wl.fmt, "grad", "nchw")
+    Xd, Wd, Gd = oracle.dequantize(qx), oracle.dequantize(qw), oracle.dequantize(qg)
+    oracle.conv_fwd_at(Xd, Wd, Ls, state["idx_f"])
+    oracle.conv_dgrad_at(Wd, Gd, Ls, state["idx_d"])
+    oracle.conv_wgrad_at(Gd, Xd, Ls, state["idx_w"])
+    dt = time.perf_counter() - t0
+    per_out = 2 * Ls.Cin * Ls.k * Ls.k
+    flops = (len(state["idx_f"]) + len(state["idx_d"])) * per_out + len(state["idx_w"]) * 2 * Ls.N * Ls.Ho * Ls.Wo
+    return flops, dt, {"quantized_elements": X.size + W.size + dY.size}
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    state = {}
+    flops = secs = 0.0
+    reps = 0
+    while secs < budget_s and reps < 1000:
+        f, dt, info = oracle_sample_step(wl, budget_s, state)
+        flops += f
+        secs += dt
+        reps += 1
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    Ls = state["ops"][0]
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": (f"{reps} reps of: quantize X[:8], W, dY[:8] of {Ls.name()} ({info['quantized_elements']} "
+                       f"elements) + 512 fwd, 512 dgrad and 16 wgrad outputs by the fp64 7-loop oracle"),
+            "seconds": secs}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    wl = S.WORKLOADS[WORKLOADS[args.workload]]
+    state = {}
+    for _ in range(args.warmup):
+        oracle_sample_step(wl, 0, state)
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f, dt, info = oracle_sample_step(wl, 0, state)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    Ls = state["ops"][0]
+    sample = (f"per step: quantize X[:8], W, dY[:8] of {Ls.name()} + 512 fwd, 512 dgrad and 16 wgrad outputs "
+              f"by the fp64 7-loop oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": sample, "value": value},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["mqconv", "reference"], default="mqconv")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stack4-nvfp4")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl != "reference":
+        print("note: warm-up raised to 3 steps", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
