@@ -45,35 +45,38 @@ constexpr int A_STAGE = 16 * KCH * 128;   // 128 rows x 64 K x fp16
 
 // ------------------------------------------------------------ block decode
 // Row `r` (eight consecutive in-block elements 8r .. 8r+7) of a packed block
-// -> eight fp16 values code * scale, as 16 bytes.  `s2` is the block scale in
-// both halves of an f16x2 (already multiplied by the operand pre-scale).
-template <int F> __device__ __forceinline__ uint4 decode_row(const uint8_t *blk, int r, uint32_t s2);
-
+// is fetched raw (load_raw) and turned into eight fp16 values code * scale
+// (decode_raw, 16 bytes).  `s2` holds the block scale in both halves of an
+// f16x2 (already multiplied by the operand pre-scale).
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
   __half2 x = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
   return *reinterpret_cast<uint32_t *>(&x);
 }
 
-template <> __device__ __forceinline__ uint4 decode_row<4>(const uint8_t *blk, int r, uint32_t s2) {
-  const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(blk) + r);
-  return make_uint4(hmul2u(dec2<4>(w), s2), hmul2u(dec2<4>(w >> 8), s2), hmul2u(dec2<4>(w >> 16), s2),
-                    hmul2u(dec2<4>(w >> 24), s2));
-}
-template <> __device__ __forceinline__ uint4 decode_row<6>(const uint8_t *blk, int r, uint32_t s2) {
+template <int F> __device__ __forceinline__ uint2 load_raw(const uint8_t *blk, int r) {
+  if (F == 4) return make_uint2(__ldg(reinterpret_cast<const uint32_t *>(blk) + r), 0u);
+  if (F == 8) return __ldg(reinterpret_cast<const uint2 *>(blk) + r);
   const uint16_t *h = reinterpret_cast<const uint16_t *>(blk + 6 * r);
-  const uint64_t v = (uint64_t)__ldg(h) | ((uint64_t)__ldg(h + 1) << 16) | ((uint64_t)__ldg(h + 2) << 32);
-  uint32_t q[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t lo = (uint32_t)(v >> (12 * k)) & 0x3Fu, hi = (uint32_t)(v >> (12 * k + 6)) & 0x3Fu;
-    q[k] = hmul2u(dec2<6>(lo | (hi << 8)), s2);
-  }
-  return make_uint4(q[0], q[1], q[2], q[3]);
+  return make_uint2((uint32_t)__ldg(h) | ((uint32_t)__ldg(h + 1) << 16), (uint32_t)__ldg(h + 2));
 }
-template <> __device__ __forceinline__ uint4 decode_row<8>(const uint8_t *blk, int r, uint32_t s2) {
-  const uint2 v = __ldg(reinterpret_cast<const uint2 *>(blk) + r);
-  return make_uint4(hmul2u(dec2<8>(v.x), s2), hmul2u(dec2<8>(v.x >> 16), s2), hmul2u(dec2<8>(v.y), s2),
-                    hmul2u(dec2<8>(v.y >> 16), s2));
+
+template <int F> __device__ __forceinline__ uint4 decode_raw(uint2 w, uint32_t s2) {
+  if (F == 4) {
+    return make_uint4(hmul2u(dec2<4>(w.x), s2), hmul2u(dec2<4>(w.x >> 8), s2), hmul2u(dec2<4>(w.x >> 16), s2),
+                      hmul2u(dec2<4>(w.x >> 24), s2));
+  } else if (F == 8) {
+    return make_uint4(hmul2u(dec2<8>(w.x), s2), hmul2u(dec2<8>(w.x >> 16), s2), hmul2u(dec2<8>(w.y), s2),
+                      hmul2u(dec2<8>(w.y >> 16), s2));
+  } else {
+    const uint64_t v = (uint64_t)w.x | ((uint64_t)w.y << 32);   // 8 x 6-bit codes, element j at bits 6j
+    uint32_t q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t lo = (uint32_t)(v >> (12 * k)) & 0x3Fu, hi = (uint32_t)(v >> (12 * k + 6)) & 0x3Fu;
+      q[k] = hmul2u(dec2<6>(lo | (hi << 8)), s2);
+    }
+    return make_uint4(q[0], q[1], q[2], q[3]);
+  }
 }
 
 // fp16 pair holding the E4M3 block scale (times 1/4 for E4M3-coded operands,
@@ -87,6 +90,7 @@ template <int F> __device__ __forceinline__ uint32_t scale_pair(uint8_t sc) {
 // ----------------------------------------------------------------- tiles
 struct Phase {
   int phh, phw, Hp, Wp, kh0, kw0, nth, ntw;
+  int q0, r0;   // ho = a - u + q0, wo = b - v + r0 for in-phase position (a, b) and tap (u, v)
 };
 
 __device__ __forceinline__ Phase get_phase(const ConvParams &p, int ph) {
@@ -100,6 +104,8 @@ __device__ __forceinline__ Phase get_phase(const ConvParams &p, int ph) {
   q.kw0 = (q.phw + p.pad) % s;
   q.nth = q.kh0 < p.Kh ? (p.Kh - q.kh0 + s - 1) / s : 0;
   q.ntw = q.kw0 < p.Kw ? (p.Kw - q.kw0 + s - 1) / s : 0;
+  q.q0 = (q.phh + p.pad) / s;
+  q.r0 = (q.phw + p.pad) / s;
   return q;
 }
 
@@ -143,67 +149,111 @@ __device__ __forceinline__ Tile get_tile(const ConvParams &p, int t) {
   return T;
 }
 
-// Locate the packed block feeding core matrix (row group g, k-group kg) of
-// operand A, or (column group g, k-group kg) of operand B.  Returns the block
-// index or -1 for an all-zero core matrix (padding, out-of-range, ragged tail).
+// ------------------------------------------------------- address tables
+// The block feeding core matrix (row group g, k-group k) of operand A, or
+// (column group g, k-group k) of operand B, depends on one entry of three
+// small tables that the producers rebuild for every chunk: A row groups (16),
+// B column groups (BN/8 <= 32) and the chunk's k-groups (KCH).  Combining an
+// entry pair is a few integer multiply-adds; v < 0 marks "no block" (padding,
+// ragged tail, invalid stride phase): the core matrix is zero.
+struct Ent {
+  int x, y, z, w, v;
+};
+struct Tables {
+  Ent rg[16];
+  Ent cg[32];
+  Ent kg[KCH];
+};
+
 template <int OP>
-__device__ __forceinline__ int64_t a_block(const ConvParams &p, const Tile &T, int g, int kg) {
-  if (OP == OP_FWD) {
-    const int rg = T.m * 16 + g;
-    if (rg >= p.Ho * p.Wo * p.NG || kg >= p.kg_total) return -1;
-    const int pos = rg / p.NG, ng = rg - pos * p.NG;
-    const int ho = pos / p.Wo, wo = pos - ho * p.Wo;
-    const int tap = kg / p.CIG, cg = kg - tap * p.CIG;
-    const int kh = tap / p.Kw, kw = tap - kh * p.Kw;
-    const int hi = ho * p.stride + kh - p.pad, wi = wo * p.stride + kw - p.pad;
-    if (hi < 0 || hi >= p.H || wi < 0 || wi >= p.W) return -1;
-    return ((int64_t)(hi * p.W + wi) * p.NG + ng) * p.CIG + cg;
-  } else if (OP == OP_DGRAD) {
-    const int rg = T.m * 16 + g;
-    if (rg >= T.ph.Hp * T.ph.Wp * p.NG || kg >= T.ph.nth * T.ph.ntw * p.COG) return -1;
-    const int pos = rg / p.NG, ng = rg - pos * p.NG;
-    const int a = pos / T.ph.Wp, b = pos - a * T.ph.Wp;
-    const int tap = kg / p.COG, cog = kg - tap * p.COG;
-    const int u = tap / T.ph.ntw, v = tap - u * T.ph.ntw;
-    const int kh = T.ph.kh0 + p.stride * u, kw = T.ph.kw0 + p.stride * v;
-    const int th = T.ph.phh + p.stride * a + p.pad - kh, tw = T.ph.phw + p.stride * b + p.pad - kw;
-    if (th < 0 || tw < 0) return -1;
-    const int ho = th / p.stride, wo = tw / p.stride;
-    if (ho >= p.Ho || wo >= p.Wo) return -1;
-    return ((int64_t)(ho * p.Wo + wo) * p.NG + ng) * p.COG + cog;
-  } else {
-    const int cog = T.m * 16 + g;
-    const int k = T.kg0 + kg;
-    if (cog >= p.COG || k >= T.kg1) return -1;
-    return (int64_t)k * p.COG + cog;   // k = position * NG + ng
+__device__ __forceinline__ void fill_tables(const ConvParams &p, const Tile &T, int c, Tables &tb, int tid) {
+  Ent e = {0, 0, 0, 0, -1};
+  if (tid < 16) {
+    const int g = tid;
+    if (OP == OP_FWD) {
+      const int rg = T.m * 16 + g;
+      if (rg < p.Ho * p.Wo * p.NG) {
+        const int pos = rg / p.NG, ng = rg - pos * p.NG, ho = pos / p.Wo, wo = pos - ho * p.Wo;
+        e = {ho * p.stride - p.pad, wo * p.stride - p.pad, ng, 0, 0};
+      }
+    } else if (OP == OP_DGRAD) {
+      const int rg = T.m * 16 + g;
+      if (rg < T.ph.Hp * T.ph.Wp * p.NG) {
+        const int pp = rg / p.NG, ng = rg - pp * p.NG, a = pp / T.ph.Wp, b = pp - a * T.ph.Wp;
+        e = {a, b, ng, 0, 0};
+      }
+    } else {
+      const int cog = T.m * 16 + g;
+      if (cog < p.COG) e = {cog, 0, 0, 0, 0};
+    }
+    tb.rg[g] = e;
+  } else if (tid < 48) {
+    const int g = tid - 16;
+    if (g < p.BN / 8) {
+      const int col = T.n * (p.BN / 8) + g;
+      if (OP == OP_FWD) {
+        if (col < p.COG) e = {col, 0, 0, 0, 0};
+      } else if (OP == OP_DGRAD) {
+        if (col < p.CIG) e = {col, 0, 0, 0, 0};
+      } else if (col < p.Kh * p.Kw * p.CIG) {
+        const int tap = col / p.CIG, cig = col - tap * p.CIG, kh = tap / p.Kw, kw = tap - kh * p.Kw;
+        e = {kh, kw, cig, 0, 0};
+      }
+      tb.cg[g] = e;
+    }
+  } else if (tid < 48 + KCH) {
+    const int k = tid - 48;
+    if (OP == OP_FWD) {
+      const int kg = c * KCH + k;
+      if (kg < p.kg_total) {
+        const int tap = kg / p.CIG, cg = kg - tap * p.CIG, kh = tap / p.Kw, kw = tap - kh * p.Kw;
+        e = {kh, kw, cg, 0, 0};
+      }
+    } else if (OP == OP_DGRAD) {
+      const int kg = c * KCH + k;
+      if (kg < T.ph.nth * T.ph.ntw * p.COG) {
+        const int tap = kg / p.COG, cog = kg - tap * p.COG, u = tap / T.ph.ntw, v = tap - u * T.ph.ntw;
+        e = {u, v, cog, 0, 0};
+      }
+    } else {
+      const int ka = T.kg0 + c * KCH + k;
+      if (ka < T.kg1) {
+        const int pos = ka / p.NG, ng = ka - pos * p.NG, ho = pos / p.Wo, wo = pos - ho * p.Wo;
+        e = {ho * p.stride - p.pad, wo * p.stride - p.pad, ng, ka, 0};
+      }
+    }
+    tb.kg[k] = e;
   }
 }
 
 template <int OP>
-__device__ __forceinline__ int64_t b_block(const ConvParams &p, const Tile &T, int g, int kg) {
+__device__ __forceinline__ int64_t a_blk(const ConvParams &p, const Tile &T, const Ent &r, const Ent &k) {
+  if ((r.v | k.v) < 0) return -1;
   if (OP == OP_FWD) {
-    const int cog = T.n * (p.BN / 8) + g;
-    if (cog >= p.COG || kg >= p.kg_total) return -1;
-    const int tap = kg / p.CIG, cg = kg - tap * p.CIG;
-    return ((int64_t)tap * p.COG + cog) * p.CIG + cg;
+    const int hi = r.x + k.x, wi = r.y + k.y;
+    if ((unsigned)hi >= (unsigned)p.H || (unsigned)wi >= (unsigned)p.W) return -1;
+    return ((int64_t)(hi * p.W + wi) * p.NG + r.z) * p.CIG + k.z;
   } else if (OP == OP_DGRAD) {
-    const int cig = T.n * (p.BN / 8) + g;
-    if (cig >= p.CIG || kg >= T.ph.nth * T.ph.ntw * p.COG) return -1;
-    const int tap = kg / p.COG, cog = kg - tap * p.COG;
-    const int u = tap / T.ph.ntw, v = tap - u * T.ph.ntw;
-    const int kh = T.ph.kh0 + p.stride * u, kw = T.ph.kw0 + p.stride * v;
-    return ((int64_t)(kh * p.Kw + kw) * p.COG + cog) * p.CIG + cig;
+    const int ho = r.x - k.x + T.ph.q0, wo = r.y - k.y + T.ph.r0;
+    if ((unsigned)ho >= (unsigned)p.Ho || (unsigned)wo >= (unsigned)p.Wo) return -1;
+    return ((int64_t)(ho * p.Wo + wo) * p.NG + r.z) * p.COG + k.z;
   } else {
-    const int cgl = T.n * (p.BN / 8) + g;
-    const int k = T.kg0 + kg;
-    if (cgl >= p.Kh * p.Kw * p.CIG || k >= T.kg1) return -1;
-    const int tap = cgl / p.CIG, cig = cgl - tap * p.CIG;
-    const int kh = tap / p.Kw, kw = tap - kh * p.Kw;
-    const int pos = k / p.NG, ng = k - pos * p.NG;
-    const int ho = pos / p.Wo, wo = pos - ho * p.Wo;
-    const int hi = ho * p.stride + kh - p.pad, wi = wo * p.stride + kw - p.pad;
-    if (hi < 0 || hi >= p.H || wi < 0 || wi >= p.W) return -1;
-    return ((int64_t)(hi * p.W + wi) * p.NG + ng) * p.CIG + cig;
+    return (int64_t)k.w * p.COG + r.x;    // k.w = position * NG + ng
+  }
+}
+
+template <int OP>
+__device__ __forceinline__ int64_t b_blk(const ConvParams &p, const Tile &T, const Ent &c, const Ent &k) {
+  if ((c.v | k.v) < 0) return -1;
+  if (OP == OP_FWD) {
+    return ((int64_t)(k.x * p.Kw + k.y) * p.COG + c.x) * p.CIG + k.z;
+  } else if (OP == OP_DGRAD) {
+    const int kh = T.ph.kh0 + p.stride * k.x, kw = T.ph.kw0 + p.stride * k.y;
+    return ((int64_t)(kh * p.Kw + kw) * p.COG + k.z) * p.CIG + c.x;
+  } else {
+    const int hi = k.x + c.x, wi = k.y + c.y;
+    if ((unsigned)hi >= (unsigned)p.H || (unsigned)wi >= (unsigned)p.W) return -1;
+    return ((int64_t)(hi * p.W + wi) * p.NG + k.z) * p.CIG + c.z;
   }
 }
 
@@ -284,6 +334,8 @@ __device__ __forceinline__ void requant_chunk(const ConvParams &p, const float (
 
 // --------------------------------------------------------------- kernel
 struct SmemCtl {
+  Tables tab[2];
+  volatile int prod_ok[2];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t acc_full[2];
@@ -342,32 +394,64 @@ __global__ void __launch_bounds__(CONV_THREADS, 1) conv_kernel(const ConvParams 
 
   if (warp < PROD_WARPS) {
     // ------------------------------------------------------ producers
+    // Every thread first issues all loads of its (up to MAXJ) core-matrix
+    // rows for the stage, then decodes and stores them: the global latency of
+    // one stage overlaps instead of serialising row by row.  Stage layout:
+    // core matrix (group g, k-group k) at (g * KCH + k) * 128 bytes.
+    constexpr int MAXJ = 4 + 8;                       // 4 A rows + up to 8 B rows per thread
     const int ptid = threadIdx.x;
-    const int a_tasks = 16 * KCH * 8, tasks = a_tasks + (p.BN / 8) * KCH * 8;
+    const int btasks = p.BN * 8;
     int it = 0;
-    for (int t = blockIdx.x; t < num_tiles && !ctl->abort_flag; t += gridDim.x) {
+    bool run = true;
+    for (int t = blockIdx.x; t < num_tiles && run; t += gridDim.x) {
       const Tile T = get_tile(p, t);
       for (int c = 0; c < T.nchunks; ++c, ++it) {
         const int s = it % STAGES;
-        if (!wait_or_abort(&ctl->empty[s], ((it / STAGES) & 1) ^ 1, p, ctl)) break;
+        Tables &tb = ctl->tab[it & 1];
+        if (ptid == 0) ctl->prod_ok[it & 1] = wait_or_abort(&ctl->empty[s], ((it / STAGES) & 1) ^ 1, p, ctl) ? 1 : 0;
+        fill_tables<OP>(p, T, c, tb, ptid);
+        asm volatile("bar.sync 1, %0;" ::"n"(PROD_WARPS * 32) : "memory");
+        if (!ctl->prod_ok[it & 1]) { run = false; break; }
         uint8_t *sa = a_ring + s * A_STAGE, *sb = b_ring + s * b_stage;
-        for (int i = ptid; i < tasks; i += PROD_WARPS * 32) {
-          const int cm = i >> 3, r = i & 7;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          uint8_t *dst;
-          if (i < a_tasks) {
-            const int k = cm >> 4, g = cm & 15;
-            const int64_t blk = a_block<OP>(p, T, g, c * KCH + k);
-            if (blk >= 0) v = decode_row<FA>(p.a.codes + blk * Fmt<FA>::BLOCK_BYTES, r, scale_pair<FA>(__ldg(p.a.scales + blk)));
-            dst = sa + cm * 128 + r * 16;
-          } else {
-            const int cmb = cm - 16 * KCH, gb = p.BN / 8;
-            const int k = cmb / gb, g = cmb - k * gb;
-            const int64_t blk = b_block<OP>(p, T, g, c * KCH + k);
-            if (blk >= 0) v = decode_row<FB>(p.b.codes + blk * Fmt<FB>::BLOCK_BYTES, r, scale_pair<FB>(__ldg(p.b.scales + blk)));
-            dst = sb + cmb * 128 + r * 16;
+        uint2 raw[MAXJ];
+        uint32_t scb[MAXJ];
+        bool ok[MAXJ];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = ptid + PROD_WARPS * 32 * j, cm = i >> 3, r = i & 7;
+          const int64_t blk = a_blk<OP>(p, T, tb.rg[cm >> 3], tb.kg[cm & 7]);
+          ok[j] = blk >= 0;
+          if (ok[j]) {
+            raw[j] = load_raw<FA>(p.a.codes + blk * Fmt<FA>::BLOCK_BYTES, r);
+            scb[j] = __ldg(p.a.scales + blk);
           }
-          *reinterpret_cast<uint4 *>(dst) = v;
+        }
+#pragma unroll
+        for (int j = 4; j < MAXJ; ++j) {
+          const int i = ptid + PROD_WARPS * 32 * (j - 4), cm = i >> 3, r = i & 7;
+          ok[j] = false;
+          if (i < btasks) {
+            const int64_t blk = b_blk<OP>(p, T, tb.cg[cm >> 3], tb.kg[cm & 7]);
+            ok[j] = blk >= 0;
+            if (ok[j]) {
+              raw[j] = load_raw<FB>(p.b.codes + blk * Fmt<FB>::BLOCK_BYTES, r);
+              scb[j] = __ldg(p.b.scales + blk);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = ptid + PROD_WARPS * 32 * j;
+          const uint4 v = ok[j] ? decode_raw<FA>(raw[j], scale_pair<FA>((uint8_t)scb[j])) : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4 *>(sa + i * 16) = v;
+        }
+#pragma unroll
+        for (int j = 4; j < MAXJ; ++j) {
+          const int i = ptid + PROD_WARPS * 32 * (j - 4);
+          if (i < btasks) {
+            const uint4 v = ok[j] ? decode_raw<FB>(raw[j], scale_pair<FB>((uint8_t)scb[j])) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(sb + i * 16) = v;
+          }
         }
         fence_async_smem();
         mbar_arrive(&ctl->full[s]);
@@ -379,7 +463,7 @@ __global__ void __launch_bounds__(CONV_THREADS, 1) conv_kernel(const ConvParams 
       constexpr bool a_mn = (OP == OP_WGRAD);
       constexpr bool b_mn = (OP != OP_FWD);
       const uint32_t idesc = idesc_f16(128, p.BN, a_mn, b_mn);
-      const uint32_t a_lbo = 16 * 128, b_lbo = (p.BN / 8) * 128;
+      constexpr uint32_t lbo = 128, sbo = KCH * 128;   // core matrix (g, k) at (g * KCH + k) * 128
       int it = 0, tc = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tc) {
@@ -395,8 +479,8 @@ __global__ void __launch_bounds__(CONV_THREADS, 1) conv_kernel(const ConvParams 
           const uint32_t sa = smem_u32(a_ring + s * A_STAGE), sb = smem_u32(b_ring + s * b_stage);
 #pragma unroll
           for (int kk = 0; kk < KCH / 2; ++kk) {
-            const uint64_t da = sdesc(sa + kk * 2 * a_lbo, a_lbo, 128);
-            const uint64_t db = sdesc(sb + kk * 2 * b_lbo, b_lbo, 128);
+            const uint64_t da = sdesc(sa + kk * 2 * lbo, lbo, sbo);
+            const uint64_t db = sdesc(sb + kk * 2 * lbo, lbo, sbo);
             umma_f16(d, da, db, idesc, (c > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&ctl->empty[s]);
