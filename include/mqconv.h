@@ -167,6 +167,35 @@ size_t mqconv_wgrad_workspace_bytes(const mq_conv_desc *desc);
 mq_status mqconv_wgrad(const mq_conv_desc *desc, const mq_packed *dyq, const mq_packed *xq, float *dw,
                        void *workspace, size_t ws_bytes, mq_stream stream);
 
+/*
+ * Weight gradient that allocates nothing (this entry point has no counterpart
+ * in the paper; it exists for callers of this library).
+ *
+ * Same result as mqconv_wgrad, up to the fp32 summation order of the split-K
+ * partial sums, but without the workspace argument.  It is meant for callers
+ * that cannot hand the library extra device memory: runtimes that own a fixed
+ * device-memory budget and pass in only the inputs and outputs, allocators
+ * that must not be bypassed or fragmented by side allocations, and code that
+ * cannot accept the implicit device synchronisation a cudaMalloc/cudaFree may
+ * bring.  The partial sums live in a built-in device array of
+ * MQCONV_WGRAD_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library
+ * reserves until the process exits; no cudaMalloc, cudaFree or other
+ * allocating routine is called.
+ *   dyq, xq, dw   as for mqconv_wgrad.
+ *   Returns MQ_ERR_WORKSPACE, without launching, when one set of partial sums
+ *   (Cout * Kh * Kw * Cin fp32) does not fit in the built-in array; when
+ *   several sets are needed the reduction is split into fewer, longer chunks
+ *   to fit.
+ *   The first call on a device looks up the array's device address with that
+ *   device current (cudaGetSymbolAddress); make that first call before any
+ *   stream capture.  Every call overwrites the partial sums it reads, so no
+ *   clearing is needed, but all calls share the one array: calls whose work
+ *   overlaps on the GPU (e.g. on two streams at once) race and give wrong dW.
+ */
+#define MQCONV_WGRAD_NOALLOC_SCRATCH_BYTES (16u << 20)
+mq_status mqconv_wgrad_noalloc(const mq_conv_desc *desc, const mq_packed *dyq, const mq_packed *xq, float *dw,
+                               mq_stream stream);
+
 /* Synchronize `stream`, copy the device status word (an OR of mq_status bit
  * flags 1 << MQ_ERR_*) to *host_status, and clear it. */
 mq_status mqconv_device_status(mq_stream stream, int32_t *host_status);

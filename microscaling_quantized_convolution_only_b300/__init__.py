@@ -71,7 +71,10 @@ def lib() -> ctypes.CDLL:
         L.mqconv_wgrad.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P, P,
                                    ctypes.c_size_t, P]
         L.mqconv_device_status.argtypes = [P, ctypes.POINTER(i32)]
-        for f in ("mqconv_quantize_cbf", "mqconv_fwd", "mqconv_dgrad", "mqconv_wgrad", "mqconv_device_status"):
+        L.mqconv_wgrad_noalloc.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P,
+                                           P]
+        for f in ("mqconv_quantize_cbf", "mqconv_fwd", "mqconv_dgrad", "mqconv_wgrad", "mqconv_device_status",
+                  "mqconv_wgrad_noalloc"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -179,6 +182,14 @@ def wgrad(layer, dyq: Packed, xq: Packed, dw: torch.Tensor, workspace: torch.Ten
     rc = lib().mqconv_wgrad(ctypes.byref(d), ctypes.byref(g), ctypes.byref(x), _ptr(dw), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "mqconv_wgrad")
+
+
+def wgrad_noalloc(layer, dyq: Packed, xq: Packed, dw: torch.Tensor, stream=None) -> None:
+    """mqconv_wgrad_noalloc: dW like wgrad(), with no workspace and no device
+    allocation anywhere (the partial sums use the library's built-in scratch)."""
+    d, g, x = desc(layer), dyq.c(), xq.c()
+    rc = lib().mqconv_wgrad_noalloc(ctypes.byref(d), ctypes.byref(g), ctypes.byref(x), _ptr(dw), _stream(stream))
+    _check(rc, "mqconv_wgrad_noalloc")
 
 
 def device_status(stream=None) -> int:

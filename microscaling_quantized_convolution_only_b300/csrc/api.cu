@@ -111,6 +111,36 @@ size_t wgrad_ws_bytes(const mq_conv_desc *d) {
 
 }  // namespace
 
+// ------------------------------------------------ wgrad without allocation
+// Fixed device scratch for mqconv_wgrad_noalloc: it holds the split-K partial
+// sums that mqconv_wgrad keeps in a caller-supplied workspace.  Every device
+// that loads this library reserves it until the process exits.  Host code must
+// not pass the symbol itself to a kernel (on the host it names a stand-in, not
+// device memory); its device address is looked up per device below.
+static __device__ __align__(256) float g_wgrad_scratch[MQCONV_WGRAD_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+
+float *g_scratch_addr[kMaxDevices];
+std::mutex g_scratch_mu;
+
+// Device address of g_wgrad_scratch on the current device, looked up on the
+// first call per device (with that device current).
+mq_status scratch_addr(float **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_wgrad_scratch) != cudaSuccess || !ptr) return MQ_ERR_CUDA;
+    g_scratch_addr[dev] = static_cast<float *>(ptr);
+  }
+  *out = g_scratch_addr[dev];
+  return MQ_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int32_t mqconv_abi_version(void) { return MQCONV_ABI_VERSION; }
@@ -275,6 +305,42 @@ mq_status mqconv_wgrad(const mq_conv_desc *desc, const mq_packed *dyq, const mq_
   p.pre_mult = pre_mult(dyq->fmt, xq->fmt);
   p.out = static_cast<float *>(workspace);
   mq::conv_plan(p);
+  if (mq::launch_conv(p, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
+  if (mq::launch_wgrad_reduce(p, dw, s) != cudaSuccess) return MQ_ERR_CUDA;
+  return MQ_OK;
+}
+
+mq_status mqconv_wgrad_noalloc(const mq_conv_desc *desc, const mq_packed *dyq, const mq_packed *xq, float *dw,
+                               mq_stream stream) {
+  mq_status st = check_desc(desc);
+  if (st != MQ_OK) return st;
+  const int64_t Ho = out_dim(desc->H, desc->Kh, desc->stride, desc->pad);
+  const int64_t Wo = out_dim(desc->W, desc->Kw, desc->stride, desc->pad);
+  if ((st = check_packed(dyq, MQ_ROLE_GRAD, desc->N, desc->Cout, Ho, Wo)) != MQ_OK) return st;
+  if ((st = check_packed(xq, MQ_ROLE_ACT, desc->N, desc->Cin, desc->H, desc->W)) != MQ_OK) return st;
+  if (!dw) return MQ_ERR_INVALID_ARG;
+  if (!aligned16(dw)) return MQ_ERR_ALIGNMENT;
+  DevInfo *di = nullptr;
+  if ((st = dev_info(&di)) != MQ_OK) return st;
+  mq::ConvParams p = base_params(desc, mq::OP_WGRAD, di->status);
+  p.a = operand(dyq);
+  p.b = operand(xq);
+  p.pre_mult = pre_mult(dyq->fmt, xq->fmt);
+  mq::conv_plan(p);
+  // fit the split-K partial sums into the fixed scratch: fewer, longer splits
+  const size_t per_split = (size_t)p.Cout * (size_t)p.ncols * sizeof(float);
+  const size_t max_splits = MQCONV_WGRAD_NOALLOC_SCRATCH_BYTES / per_split;
+  if (max_splits == 0) return MQ_ERR_WORKSPACE;
+  if ((size_t)p.k_splits > max_splits) {
+    int per = (int)((p.kg_total + (int64_t)max_splits - 1) / (int64_t)max_splits);
+    per = (per + 7) / 8 * 8;
+    p.kg_per_split = per;
+    p.k_splits = (p.kg_total + per - 1) / per;
+  }
+  float *scratch = nullptr;
+  if ((st = scratch_addr(&scratch)) != MQ_OK) return st;
+  p.out = scratch;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (mq::launch_conv(p, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
   if (mq::launch_wgrad_reduce(p, dw, s) != cudaSuccess) return MQ_ERR_CUDA;
   return MQ_OK;
