@@ -8,7 +8,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmqconv.so")
-SOURCES = ["api.cu", "quantize.cu", "conv.cu"]
+SOURCES = ["api.cu", "quantize.cu", "conv.cu", "conv_halo.cu"]
 HEADERS = ["common.cuh", "kernels.h", os.path.join("..", "..", "include", "mqconv.h")]
 
 NVCC_FLAGS = [

@@ -103,6 +103,15 @@ mq::Operand operand(const mq_packed *t) {
 
 float pre_mult(int fa, int fb) { return (fa == MQ_FMT_E4M3 ? 4.0f : 1.0f) * (fb == MQ_FMT_E4M3 ? 4.0f : 1.0f); }
 
+// Forward or data gradient: the halo-reuse kernel when the layer fits it
+// (stride 1), the generic implicit-im2col kernel otherwise.
+mq_status run_conv(mq::ConvParams &p, int num_sms, cudaStream_t s) {
+  mq::HaloConv h;
+  if (mq::halo_plan(p, h)) return mq::halo_launch(p, h, num_sms, s) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+  mq::conv_plan(p);
+  return mq::launch_conv(p, num_sms, s) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+}
+
 size_t wgrad_ws_bytes(const mq_conv_desc *d) {
   mq::ConvParams p = base_params(d, mq::OP_WGRAD, nullptr);
   mq::conv_plan(p);
@@ -252,9 +261,7 @@ mq_status mqconv_fwd(const mq_conv_desc *desc, const mq_packed *xq, const mq_pac
     p.rq.fmt = rq->fmt;
     if (rq->amax_out && cudaMemsetAsync(rq->amax_out, 0, sizeof(float), s) != cudaSuccess) return MQ_ERR_CUDA;
   }
-  mq::conv_plan(p);
-  if (mq::launch_conv(p, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
-  return MQ_OK;
+  return run_conv(p, di->num_sms, s);
 }
 
 mq_status mqconv_dgrad(const mq_conv_desc *desc, const mq_packed *wq, const mq_packed *dyq, float *dx,
@@ -274,9 +281,7 @@ mq_status mqconv_dgrad(const mq_conv_desc *desc, const mq_packed *wq, const mq_p
   p.b = operand(wq);
   p.pre_mult = pre_mult(dyq->fmt, wq->fmt);
   p.out = dx;
-  mq::conv_plan(p);
-  if (mq::launch_conv(p, di->num_sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MQ_ERR_CUDA;
-  return MQ_OK;
+  return run_conv(p, di->num_sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t mqconv_wgrad_workspace_bytes(const mq_conv_desc *desc) {

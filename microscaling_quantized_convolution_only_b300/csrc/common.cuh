@@ -208,3 +208,72 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 }  // namespace mq
+
+namespace mq {
+
+// ------------------------------------------------------------------- TMA
+// arrive once on `bar` and add `bytes` to the transaction count it waits for
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// tiled tensor loads (global -> this CTA's shared memory); completion is
+// signalled on `bar` as transaction bytes.  Out-of-range boxes read zeros.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_t *bar, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+}  // namespace mq
+
+namespace mq {
+
+// ------------------------------------------------------------ block decode
+// Row `r` (eight consecutive in-block elements 8r .. 8r+7) of a packed block
+// is fetched raw (load_raw) and turned into eight fp16 values code * scale
+// (decode_raw, 16 bytes).  `s2` holds the block scale in both halves of an
+// f16x2 (already multiplied by the operand pre-scale).
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+  __half2 x = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+  return *reinterpret_cast<uint32_t *>(&x);
+}
+
+template <int F> __device__ __forceinline__ uint4 decode_raw(uint2 w, uint32_t s2) {
+  if (F == 4) {
+    return make_uint4(hmul2u(dec2<4>(w.x), s2), hmul2u(dec2<4>(w.x >> 8), s2), hmul2u(dec2<4>(w.x >> 16), s2),
+                      hmul2u(dec2<4>(w.x >> 24), s2));
+  } else if (F == 8) {
+    return make_uint4(hmul2u(dec2<8>(w.x), s2), hmul2u(dec2<8>(w.x >> 16), s2), hmul2u(dec2<8>(w.y), s2),
+                      hmul2u(dec2<8>(w.y >> 16), s2));
+  } else {
+    const uint64_t v = (uint64_t)w.x | ((uint64_t)w.y << 32);   // 8 x 6-bit codes, element j at bits 6j
+    uint32_t q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t lo = (uint32_t)(v >> (12 * k)) & 0x3Fu, hi = (uint32_t)(v >> (12 * k + 6)) & 0x3Fu;
+      q[k] = hmul2u(dec2<6>(lo | (hi << 8)), s2);
+    }
+    return make_uint4(q[0], q[1], q[2], q[3]);
+  }
+}
+
+// fp16 pair holding the E4M3 block scale (times 1/4 for E4M3-coded operands,
+// whose code * scale can exceed the fp16 range; the epilogue multiplies back).
+template <int F> __device__ __forceinline__ uint32_t scale_pair(uint8_t sc) {
+  uint32_t h = dec2<8>((uint32_t)sc) & 0xFFFFu;
+  if (F == 8) h = hmul2u(h, 0x3400u);   // x 0.25 (exact: a power of two, stays normal)
+  return h | (h << 16);
+}
+
+}  // namespace mq

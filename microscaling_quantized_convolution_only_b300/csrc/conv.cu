@@ -43,48 +43,12 @@ constexpr int CONV_THREADS = (PROD_WARPS + EPI_WARPS + 1) * 32;
 constexpr int STAGES = 4;
 constexpr int A_STAGE = 16 * KCH * 128;   // 128 rows x 64 K x fp16
 
-// ------------------------------------------------------------ block decode
-// Row `r` (eight consecutive in-block elements 8r .. 8r+7) of a packed block
-// is fetched raw (load_raw) and turned into eight fp16 values code * scale
-// (decode_raw, 16 bytes).  `s2` holds the block scale in both halves of an
-// f16x2 (already multiplied by the operand pre-scale).
-__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
-  __half2 x = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
-  return *reinterpret_cast<uint32_t *>(&x);
-}
-
+// packed row fetch from global memory (the decode itself is in common.cuh)
 template <int F> __device__ __forceinline__ uint2 load_raw(const uint8_t *blk, int r) {
   if (F == 4) return make_uint2(__ldg(reinterpret_cast<const uint32_t *>(blk) + r), 0u);
   if (F == 8) return __ldg(reinterpret_cast<const uint2 *>(blk) + r);
   const uint16_t *h = reinterpret_cast<const uint16_t *>(blk + 6 * r);
   return make_uint2((uint32_t)__ldg(h) | ((uint32_t)__ldg(h + 1) << 16), (uint32_t)__ldg(h + 2));
-}
-
-template <int F> __device__ __forceinline__ uint4 decode_raw(uint2 w, uint32_t s2) {
-  if (F == 4) {
-    return make_uint4(hmul2u(dec2<4>(w.x), s2), hmul2u(dec2<4>(w.x >> 8), s2), hmul2u(dec2<4>(w.x >> 16), s2),
-                      hmul2u(dec2<4>(w.x >> 24), s2));
-  } else if (F == 8) {
-    return make_uint4(hmul2u(dec2<8>(w.x), s2), hmul2u(dec2<8>(w.x >> 16), s2), hmul2u(dec2<8>(w.y), s2),
-                      hmul2u(dec2<8>(w.y >> 16), s2));
-  } else {
-    const uint64_t v = (uint64_t)w.x | ((uint64_t)w.y << 32);   // 8 x 6-bit codes, element j at bits 6j
-    uint32_t q[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t lo = (uint32_t)(v >> (12 * k)) & 0x3Fu, hi = (uint32_t)(v >> (12 * k + 6)) & 0x3Fu;
-      q[k] = hmul2u(dec2<6>(lo | (hi << 8)), s2);
-    }
-    return make_uint4(q[0], q[1], q[2], q[3]);
-  }
-}
-
-// fp16 pair holding the E4M3 block scale (times 1/4 for E4M3-coded operands,
-// whose code * scale can exceed the fp16 range; the epilogue multiplies back).
-template <int F> __device__ __forceinline__ uint32_t scale_pair(uint8_t sc) {
-  uint32_t h = dec2<8>((uint32_t)sc) & 0xFFFFu;
-  if (F == 8) h = hmul2u(h, 0x3400u);   // x 0.25 (exact: a power of two, stays normal)
-  return h | (h << 16);
 }
 
 // ----------------------------------------------------------------- tiles

@@ -1,0 +1,645 @@
+// conv_halo.cu -- stride-1 forward and data-gradient convolutions that decode
+// every packed input block once per tile and reuse it for all taps.
+//
+// MicroQonv §IV-A builds the channel-batch-first im2col X' on chip: each
+// contiguous CBF block crosses the off-chip/on-chip boundary once and is then
+// replicated locally for every receptive field that needs it.  Here the
+// replication costs nothing: a CTA
+// tile covers R output rows x P output positions x G batch groups (8 n each)
+// = R x 128 GEMM rows, and per chunk of 16 input channels the CTA stages the
+// (R + Kh - 1) x (P + Kw - 1) halo of packed input blocks (TMA, zero fill
+// outside the image), decodes it once to fp16 core matrices, and every tap
+// (u, v) of every output row s reads the same decoded halo through a
+// shared-memory matrix descriptor whose start address is shifted by
+// ((s + u) * (P + Kw - 1) + v) halo positions.  The weights of the chunk
+// (all taps, BN output channels) are staged and decoded the same way.
+//
+// The data gradient of a stride-1 layer is the same correlation run on dY
+// with the taps mirrored and the weight blocks read transposed
+// (MN-major descriptor), padding Kh - 1 - pad: dX = col2im(W^T G_Y) of
+// MicroQonv §IV-A without any col2im buffer.
+//
+// GEMM per tile: rows = (output row s, position p, batch group j, n), columns
+// = output channels (BN), K = (chunk, tap, 16 channels).  One accumulator of
+// 128 x BN fp32 per output row s lives in TMEM (R x BN <= 512 columns); the
+// epilogue of row s of one tile overlaps the MMAs of rows s+1.. and the next
+// tile, because the MMA warp waits for accumulator s only before its own
+// first MMA into it.
+//
+// Warp roles: warps 0-7 decode, warps 8-11 drain the accumulators
+// (tcgen05.ld) into fp32 HWCN outputs or requantized CBF blocks, warp 12 lane
+// 0 issues the TMA loads, warp 13 lane 0 issues tcgen05.mma.  Every wait is
+// bounded; on expiry the CTA records MQ_ERR_TIMEOUT, stops, lets its copies
+// and MMAs in flight finish and frees its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mq {
+
+namespace {
+
+constexpr int HC_DEC_WARPS = 8;
+constexpr int HC_EPI_WARP0 = 8;
+constexpr int HC_EPI_WARPS = 4;
+constexpr int HC_TMA_WARP = 12;
+constexpr int HC_MMA_WARP = 13;
+constexpr int HC_THREADS = 14 * 32;
+constexpr int HC_DEC_THREADS = HC_DEC_WARPS * 32;
+constexpr int CGC = 2;          // channel groups (8 channels each) per chunk: K = 16 per tap
+constexpr int DSTAGES = 2;      // decoded ring depth
+constexpr int MAX_PS = 4;       // packed ring depth (at most)
+constexpr int MAX_R = 8;
+
+struct HcCtl {
+  uint64_t pfull[MAX_PS], pempty[MAX_PS];
+  uint64_t dfull[DSTAGES], dempty[DSTAGES];
+  uint64_t sfull[2], sempty[2];
+  uint64_t acc_full[MAX_R], acc_empty[MAX_R];
+  uint64_t done;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+__device__ __forceinline__ bool hc_wait(uint64_t *bar, uint32_t parity, const HaloConv &p, HcCtl *ctl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (ctl->abort_flag) return false;
+      if (globaltimer_ns() - t0 > 2000000000ull) {
+        atomicOr(p.status, ST_TIMEOUT);
+        ctl->abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// raw bits of row r (8 codes) of a packed block in shared memory
+template <int F> __device__ __forceinline__ uint2 lds_row(const uint8_t *blk, int r) {
+  if (F == 4) return make_uint2(*reinterpret_cast<const uint32_t *>(blk + 4 * r), 0u);
+  if (F == 8) return *reinterpret_cast<const uint2 *>(blk + 8 * r);
+  const uint16_t *h = reinterpret_cast<const uint16_t *>(blk + 6 * r);
+  return make_uint2((uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2]);
+}
+
+struct TileCoord {
+  int g0, w0, h0, n0;   // first batch group, output column, output row, output channel
+};
+
+__device__ __forceinline__ TileCoord hc_tile(const HaloConv &p, int t) {
+  TileCoord c;
+  int r = t;
+  c.g0 = (r % p.tiles_g) * p.G;
+  r /= p.tiles_g;
+  c.w0 = (r % p.tiles_w) * p.P;
+  r /= p.tiles_w;
+  c.h0 = (r % p.tiles_h) * p.R;
+  r /= p.tiles_h;
+  c.n0 = r * p.BN;
+  return c;
+}
+
+// Requantize 16 fp32 columns of one row into two blocks of the next layer's
+// activations (see quantize.cu for the rounding).  Lanes 8q..8q+7 hold the
+// eight batch rows of one block; the block amax is their shuffle-max.
+template <int F>
+__device__ __forceinline__ void hc_requant16(const HaloConv &p, const float (&y)[16], int64_t blk_pos_ng, int n_in,
+                                             int co0, bool row_ok, float s_t, uint32_t &amax_acc) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int co = co0 + 8 * h;
+    float v[8];
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = y[8 * h + j];
+      m = max(m, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+    }
+    if (!row_ok || co >= p.NC) m = 0;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    amax_acc = max(amax_acc, m);
+    if (!row_ok || co >= p.NC) continue;
+    const uint32_t bsc = block_scale_code<F>(__uint_as_float(m), s_t);
+    const float bs = code_value<8>(bsc);
+    // codes of the eight values (exact RN of the real quotient, as the quantizer)
+    float inv_lo = 0.0f, inv_hi = 0.0f;
+    if (bs > 0.0f) {
+      const float inv = __frcp_rn(bs * s_t);
+      inv_lo = inv * (1.0f - QEPS);
+      inv_hi = inv * (1.0f + QEPS);
+    }
+    constexpr uint32_t cmask = F == 4 ? 0xFu : 0xFFu;
+    constexpr int sh = F == 4 ? 4 : 8;
+    uint64_t bits = 0;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t lo = cvt2<F>(v[2 * jj] * inv_lo, v[2 * jj + 1] * inv_lo);
+      const uint32_t hi = cvt2<F>(v[2 * jj] * inv_hi, v[2 * jj + 1] * inv_hi);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t cl = (lo >> (e * sh)) & cmask, ch = (hi >> (e * sh)) & cmask;
+        uint32_t cc = cl;
+        if (cl != ch) {
+          const float x = v[2 * jj + e];
+          cc = resolve_tie<F>(fabsf(x), bs, s_t, cl & Fmt<F>::MAG, ch & Fmt<F>::MAG) |
+               (signbit(x) ? Fmt<F>::SBIT : 0u);
+        }
+        bits |= (uint64_t)cc << ((2 * jj + e) * (F == 4 ? 4 : F == 6 ? 6 : 8));
+      }
+    }
+    const int64_t blk = blk_pos_ng + co / 8;
+    uint8_t *dst = p.rq.codes + blk * Fmt<F>::BLOCK_BYTES;
+    if (F == 4) {
+      reinterpret_cast<uint32_t *>(dst)[n_in] = (uint32_t)bits;
+    } else if (F == 6) {
+      uint16_t *d16 = reinterpret_cast<uint16_t *>(dst + 6 * n_in);
+      d16[0] = (uint16_t)bits;
+      d16[1] = (uint16_t)(bits >> 16);
+      d16[2] = (uint16_t)(bits >> 32);
+    } else {
+      reinterpret_cast<uint64_t *>(dst)[n_in] = bits;
+    }
+    if (n_in == 0) p.rq.scales[blk] = (uint8_t)bsc;
+  }
+}
+
+}  // namespace
+
+// FA: format of the input blocks (X or dY), FB: of the weights, FR: format of
+// the fused requantization of the output (0 = none).
+template <int OP, int FA, int FB, int FR>
+__global__ void __launch_bounds__(HC_THREADS, 1)
+    halo_conv_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_w,
+                     const HaloConv p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  HcCtl *ctl = reinterpret_cast<HcCtl *>(smem + p.off_ctl);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int BBA = Fmt<FA>::BLOCK_BYTES, BBB = Fmt<FB>::BLOCK_BYTES;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.PS; ++s) {
+      mbar_init(&ctl->pfull[s], 1);
+      mbar_init(&ctl->pempty[s], HC_DEC_THREADS);
+    }
+    for (int s = 0; s < DSTAGES; ++s) {
+      mbar_init(&ctl->dfull[s], HC_DEC_THREADS);
+      mbar_init(&ctl->dempty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctl->sfull[s], 32);
+      mbar_init(&ctl->sempty[s], HC_DEC_THREADS);
+    }
+    for (int s = 0; s < p.R; ++s) {
+      mbar_init(&ctl->acc_full[s], 1);
+      mbar_init(&ctl->acc_empty[s], HC_EPI_WARPS * 32);
+    }
+    mbar_init(&ctl->done, 1);
+    ctl->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == HC_MMA_WARP) tmem_alloc(&ctl->tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const int taps = p.Kh * p.Kw;
+
+  if (warp == HC_TMA_WARP) {
+    // ------------------------------------------------------- TMA producer
+    // The whole warp gathers the tile's halo block scales (zero outside the
+    // image: those blocks' codes are zero-filled by the TMA as well); lane 0
+    // then streams the packed codes of every chunk.
+    int pit = 0, k = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
+      const TileCoord tc = hc_tile(p, t);
+      const int tb = k & 1;
+      int okw = 1;
+      if (lane == 0) okw = hc_wait(&ctl->sempty[tb], ((k >> 1) & 1) ^ 1, p, ctl) ? 1 : 0;
+      if (!__shfl_sync(0xFFFFFFFFu, okw, 0)) break;
+      uint8_t *scd = smem + p.off_sc + tb * p.sc_stride;
+      const int rowb = p.G * p.CGin;                       // bytes per halo position
+      for (int i = lane; i < (int)p.sc_bytes; i += 32) {
+        const int hw = i / rowb, b = i - hw * rowb;
+        const int hr = hw / p.WP, wc = hw - hr * p.WP;
+        const int hi = tc.h0 - p.padh + hr, wi = tc.w0 - p.padw + wc;
+        uint8_t v = 0;
+        if ((unsigned)hi < (unsigned)p.Hin && (unsigned)wi < (unsigned)p.Win)
+          v = __ldg(p.in_scales + (((int64_t)hi * p.Win + wi) * p.NG + tc.g0) * p.CGin + b);
+        scd[i] = v;
+      }
+      mbar_arrive(&ctl->sfull[tb]);
+      if (lane == 0) {
+        for (int c = 0; c < p.nchunks; ++c, ++pit) {
+          const int ps = pit % p.PS;
+          if (!hc_wait(&ctl->pempty[ps], ((pit / p.PS) & 1) ^ 1, p, ctl)) { ok = false; break; }
+          mbar_expect_tx(&ctl->pfull[ps], p.pk_bytes);
+          uint8_t *dst = smem + p.off_pk + ps * p.pk_stage;
+          tma_load_4d(dst, &tm_in, &ctl->pfull[ps], c * CGC * BBA / 8, tc.g0, tc.w0 - p.padw, tc.h0 - p.padh);
+          if (OP == OP_FWD)
+            tma_load_3d(dst + p.pk_b_off, &tm_w, &ctl->pfull[ps], c * CGC * BBB / 8, tc.n0 / 8, 0);
+          else
+            tma_load_3d(dst + p.pk_b_off, &tm_w, &ctl->pfull[ps], (tc.n0 / 8) * BBB / 8, c * CGC, 0);
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      pit = __shfl_sync(0xFFFFFFFFu, pit, 0);
+    }
+    // let the copies in flight land before the CTA can exit
+    if (lane == 0) {
+      for (int i = 0; i < p.PS && i < pit; ++i) {
+        const int q = pit - 1 - i;
+        hc_wait(&ctl->pfull[q % p.PS], (q / p.PS) & 1, p, ctl);
+      }
+    }
+    __syncwarp();
+  } else if (warp < HC_DEC_WARPS) {
+    // ------------------------------------------------------------ decoders
+    const int tid = threadIdx.x;
+    int pit = 0, dit = 0, k = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
+      const TileCoord tc = hc_tile(p, t);
+      const int tb = k & 1;
+      if (!hc_wait(&ctl->sfull[tb], (k >> 1) & 1, p, ctl)) break;
+      const uint8_t *sc = smem + p.off_sc + tb * p.sc_stride;
+      for (int c = 0; c < p.nchunks; ++c, ++pit, ++dit) {
+        const int ps = pit % p.PS, ds = dit % DSTAGES;
+        if (!hc_wait(&ctl->pfull[ps], (pit / p.PS) & 1, p, ctl)) { ok = false; break; }
+        if (!hc_wait(&ctl->dempty[ds], ((dit / DSTAGES) & 1) ^ 1, p, ctl)) { ok = false; break; }
+        const uint8_t *pk = smem + p.off_pk + ps * p.pk_stage;
+        uint8_t *dec = smem + p.off_dec + ds * p.dec_stage;
+        // input halo: block (hr, wc, j, kc) at index ((hr * WP + wc) * G + j) * CGC + kc
+        const int nh = p.nh_blocks * 8;
+        for (int i = tid; i < nh; i += HC_DEC_THREADS) {
+          const int blk = i >> 3, r = i & 7;
+          const int hp = blk / CGC, kc = blk - hp * CGC;
+          const uint8_t s = sc[hp * p.CGin + c * CGC + kc];
+          const uint4 v = decode_raw<FA>(lds_row<FA>(pk + blk * BBA, r), scale_pair<FA>(s));
+          *reinterpret_cast<uint4 *>(dec + i * 16) = v;
+        }
+        // weights: fwd block (tap, nb, kc) at (tap * NB + nb) * CGC + kc;
+        //          dgrad block (tap, kc, nb) at (tap * CGC + kc) * NB + nb
+        const int nbr = p.nb_blocks * 8;
+        uint8_t *decb = dec + p.dec_b_off;
+        const uint8_t *pkb = pk + p.pk_b_off;
+        for (int i = tid; i < nbr; i += HC_DEC_THREADS) {
+          const int blk = i >> 3, r = i & 7;
+          uint8_t s = 0;
+          if (OP == OP_FWD) {
+            const int tap = blk / (p.NB * CGC), rem = blk - tap * (p.NB * CGC), nb = rem / CGC, kc = rem - nb * CGC;
+            const int cog = tc.n0 / 8 + nb;
+            if (cog < p.COG) s = __ldg(p.w_scales + ((int64_t)tap * p.COG + cog) * p.CIG + c * CGC + kc);
+          } else {
+            const int tap = blk / (p.NB * CGC), rem = blk - tap * (p.NB * CGC), kc = rem / p.NB, nb = rem - kc * p.NB;
+            const int cig = tc.n0 / 8 + nb;
+            if (cig < p.CIG) s = __ldg(p.w_scales + ((int64_t)tap * p.COG + c * CGC + kc) * p.CIG + cig);
+          }
+          const uint4 v = decode_raw<FB>(lds_row<FB>(pkb + blk * BBB, r), scale_pair<FB>(s));
+          *reinterpret_cast<uint4 *>(decb + i * 16) = v;
+        }
+        fence_async_smem();
+        mbar_arrive(&ctl->pempty[ps]);
+        mbar_arrive(&ctl->dfull[ds]);
+      }
+      if (ok) mbar_arrive(&ctl->sempty[tb]);
+    }
+  } else if (warp == HC_MMA_WARP) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(128, p.BN, false, OP == OP_DGRAD);
+      const uint32_t halo_row = (uint32_t)(p.WP * p.G * CGC * 128);   // bytes per halo row
+      const uint32_t halo_col = (uint32_t)(p.G * CGC * 128);          // bytes per halo position
+      int dit = 0, k = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
+        for (int c = 0; c < p.nchunks; ++c, ++dit) {
+          const int ds = dit % DSTAGES;
+          if (!hc_wait(&ctl->dfull[ds], (dit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + p.off_dec + ds * p.dec_stage);
+          const uint32_t b0 = a0 + p.dec_b_off;
+          for (int s = 0; s < p.R && ok; ++s) {
+            if (c == 0) {
+              if (!hc_wait(&ctl->acc_empty[s], (k & 1) ^ 1, p, ctl)) { ok = false; break; }
+              tc_fence_after();
+            }
+            const uint32_t d = tmem + s * p.acc_cols;
+            for (int u = 0; u < p.Kh; ++u) {
+              for (int v = 0; v < p.Kw; ++v) {
+                const uint64_t ad = sdesc(a0 + (s + u) * halo_row + v * halo_col, 128, CGC * 128);
+                uint64_t bd;
+                if (OP == OP_FWD) {
+                  bd = sdesc(b0 + (u * p.Kw + v) * (p.NB * CGC * 128), 128, CGC * 128);
+                } else {
+                  const int tw = (p.Kh - 1 - u) * p.Kw + (p.Kw - 1 - v);
+                  bd = sdesc(b0 + tw * (p.NB * CGC * 128), p.NB * 128, 128);
+                }
+                umma_f16(d, ad, bd, idesc, (c | u | v) ? 1u : 0u);
+              }
+            }
+            if (c == p.nchunks - 1) umma_commit(&ctl->acc_full[s]);
+          }
+          umma_commit(&ctl->dempty[ds]);
+        }
+      }
+      (void)taps;
+      umma_commit(&ctl->done);
+      hc_wait(&ctl->done, 0, p, ctl);
+    }
+    __syncwarp();
+  } else if (warp >= HC_EPI_WARP0 && warp < HC_EPI_WARP0 + HC_EPI_WARPS) {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;                       // TMEM lanes 32q .. 32q+31
+    const int row = q * 32 + lane;
+    const int g = row >> 3, n_in = row & 7, pp = g / p.G, j = g - pp * p.G;
+    const float f = (*p.sa) * (*p.sb) * p.pre_mult;
+    float rq_st = 0.0f;
+    if (FR) rq_st = __fdiv_rn(*p.rq.amax_in, Fmt<FR ? FR : 4>::DENOM);
+    uint32_t amax_acc = 0;
+    int k = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++k) {
+      const TileCoord tc = hc_tile(p, t);
+      const int wo = tc.w0 + pp, ng = tc.g0 + j, n = ng * 8 + n_in;
+      bool stop = false;
+      for (int s = 0; s < p.R; ++s) {
+        if (!hc_wait(&ctl->acc_full[s], k & 1, p, ctl)) { stop = true; break; }
+        tc_fence_after();
+        const int ho = tc.h0 + s;
+        const bool valid = ho < p.Hout && wo < p.Wout;
+        const int64_t pos = (int64_t)ho * p.Wout + wo;
+        const int64_t obase = pos * p.NC * (int64_t)p.N + n;
+        const int64_t rq_blk = (pos * p.NG + ng) * p.NCG;
+        const uint32_t tb = tmem + s * p.acc_cols + ((uint32_t)(q * 32) << 16);
+        for (int c0 = 0; c0 < p.BN; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tb + c0, r);
+          tmem_wait_ld();
+          float y[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) y[jj] = __uint_as_float(r[jj]) * f;
+          const int co0 = tc.n0 + c0;
+          if (p.out && valid) {
+            float *o = p.out + obase + (int64_t)co0 * p.N;
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              if (co0 + jj < p.NC) o[(int64_t)jj * p.N] = y[jj];
+          }
+          if (FR) hc_requant16<FR ? FR : 4>(p, y, rq_blk, n_in, co0, valid, rq_st, amax_acc);
+        }
+        tc_fence_before();
+        mbar_arrive(&ctl->acc_empty[s]);
+      }
+      if (stop) break;
+    }
+    if (FR) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) amax_acc = max(amax_acc, __shfl_xor_sync(0xFFFFFFFFu, amax_acc, o));
+      if (lane == 0 && amax_acc && p.rq.amax_out_bits) atomicMax(p.rq.amax_out_bits, amax_acc);
+      if (blockIdx.x == 0 && row == 0) *p.rq.s_t_out = rq_st;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == HC_MMA_WARP) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------ host
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Row-major tensor of `rank` dims (dims[0] innermost, in elements of
+// `esize` bytes), box `box`, no swizzle, zero fill out of range.
+bool make_map(CUtensorMap *m, const void *base, int esize, int rank, const uint64_t *dims, const uint32_t *box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bd[5], es[5];
+  uint64_t stride = (uint64_t)esize;
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bd[i] = box[i];
+    es[i] = 1;
+    if (i > 0) gs[i - 1] = stride;
+    stride *= dims[i];
+  }
+  const CUtensorMapDataType dt = esize == 8 ? CU_TENSOR_MAP_DATA_TYPE_UINT64
+                                 : esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void *>(base), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr size_t SMEM_LIMIT = 227 * 1024;
+
+size_t halo_smem(HaloConv &h, int bba, int bbb) {
+  const int taps = h.Kh * h.Kw;
+  h.WP = h.P + h.Kw - 1;
+  h.RH = h.R + h.Kh - 1;
+  h.nh_blocks = h.RH * h.WP * h.G * CGC;
+  h.nb_blocks = taps * h.NB * CGC;
+  h.dec_b_off = (uint32_t)h.nh_blocks * 128;
+  h.dec_stage = (uint32_t)(h.nh_blocks + h.nb_blocks) * 128;
+  h.pk_b_off = (uint32_t)((h.nh_blocks * bba + 127) / 128 * 128);
+  h.pk_bytes = (uint32_t)(h.nh_blocks * bba + h.nb_blocks * bbb);
+  h.pk_stage = (uint32_t)((h.pk_b_off + h.nb_blocks * bbb + 127) / 128 * 128);
+  h.sc_bytes = (uint32_t)(h.RH * h.WP * h.G * h.CGin);
+  h.sc_stride = (h.sc_bytes + 127) / 128 * 128;
+  const size_t fixed = 1024 + (size_t)DSTAGES * h.dec_stage + 2 * h.sc_stride + sizeof(HcCtl) + 128;
+  if (fixed + 2 * (size_t)h.pk_stage > SMEM_LIMIT) return 0;
+  h.PS = (int)std::min<size_t>(MAX_PS, (SMEM_LIMIT - fixed) / h.pk_stage);
+  h.off_dec = 0;
+  h.off_pk = DSTAGES * h.dec_stage;
+  h.off_sc = h.off_pk + h.PS * h.pk_stage;
+  h.off_ctl = h.off_sc + 2 * h.sc_stride;
+  return 1024 + (size_t)h.off_ctl + sizeof(HcCtl);
+}
+
+int pow2_at_least32(int x) {
+  int v = 32;
+  while (v < x) v <<= 1;
+  return v;
+}
+
+}  // namespace
+
+// Plans the halo kernel for a stride-1 forward or data-gradient convolution;
+// returns false when the layer does not fit its constraints (the caller then
+// uses the generic kernel).
+bool halo_plan(const ConvParams &cp, HaloConv &h) {
+  std::memset(&h, 0, sizeof(h));
+  if (cp.stride != 1 || (cp.op != OP_FWD && cp.op != OP_DGRAD)) return false;
+  h.op = cp.op;
+  h.N = cp.N;
+  h.NG = cp.NG;
+  h.Kh = cp.Kh;
+  h.Kw = cp.Kw;
+  h.COG = cp.COG;
+  h.CIG = cp.CIG;
+  if (cp.op == OP_FWD) {
+    h.Hin = cp.H; h.Win = cp.W; h.CGin = cp.CIG;
+    h.Hout = cp.Ho; h.Wout = cp.Wo; h.NC = cp.Cout;
+    h.padh = cp.pad; h.padw = cp.pad;
+  } else {
+    if (cp.pad > cp.Kh - 1 || cp.pad > cp.Kw - 1) return false;
+    h.Hin = cp.Ho; h.Win = cp.Wo; h.CGin = cp.COG;
+    h.Hout = cp.H; h.Wout = cp.W; h.NC = cp.Cin;
+    h.padh = cp.Kh - 1 - cp.pad; h.padw = cp.Kw - 1 - cp.pad;
+  }
+  h.NCG = h.NC / 8;
+  if (h.CGin % CGC) return false;
+  h.nchunks = h.CGin / CGC;
+  // positions x batch groups = 16 row groups (M = 128); least padding waste
+  int best = -1;
+  double best_waste = 1e30;
+  for (int P = 16; P >= 1; P >>= 1) {
+    const int G = 16 / P;
+    if (G > h.NG || h.NG % G) continue;
+    const double waste = (double)((h.Wout + P - 1) / P * P) / h.Wout;
+    if (waste < best_waste - 1e-9) {
+      best_waste = waste;
+      best = P;
+    }
+  }
+  if (best < 0) return false;
+  h.P = best;
+  h.G = 16 / best;
+  const int bba = block_bytes(cp.a.fmt), bbb = block_bytes(cp.b.fmt);
+  h.BN = std::min(256, (h.NC + 15) / 16 * 16);
+  for (;;) {
+    h.NB = h.BN / 8;
+    h.acc_cols = pow2_at_least32(h.BN);
+    h.R = std::min(std::min(MAX_R, 512 / h.acc_cols), std::min(4, h.Hout));
+    size_t sm = 0;
+    while (h.R >= 1 && (sm = halo_smem(h, bba, bbb)) == 0) --h.R;
+    if (h.R >= 1 && sm) {
+      h.smem = sm;
+      break;
+    }
+    if (h.BN <= 16) return false;
+    h.BN = std::max(16, h.BN / 2 / 16 * 16);
+  }
+  h.tiles_g = h.NG / h.G;
+  h.tiles_w = (h.Wout + h.P - 1) / h.P;
+  h.tiles_h = (h.Hout + h.R - 1) / h.R;
+  h.tiles_n = (h.NC + h.BN - 1) / h.BN;
+  const int64_t nt = (int64_t)h.tiles_g * h.tiles_w * h.tiles_h * h.tiles_n;
+  if (nt <= 0 || nt > INT32_MAX) return false;
+  h.num_tiles = (int)nt;
+  return true;
+}
+
+namespace {
+
+template <int OP, int FA, int FB, int FR>
+cudaError_t hc_launch(const CUtensorMap &a, const CUtensorMap &b, const HaloConv &h, int grid,
+                      cudaStream_t st) {
+  auto k = halo_conv_kernel<OP, FA, FB, FR>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, HC_THREADS, h.smem, st>>>(a, b, h);
+  return cudaGetLastError();
+}
+
+template <int OP, int FA, int FR>
+cudaError_t hc_dispatch_b(int fb, const CUtensorMap &a, const CUtensorMap &b, const HaloConv &h, int grid,
+                          cudaStream_t st) {
+  switch (fb) {
+    case 4: return hc_launch<OP, FA, 4, FR>(a, b, h, grid, st);
+    case 6: return hc_launch<OP, FA, 6, FR>(a, b, h, grid, st);
+    default: return hc_launch<OP, FA, 8, FR>(a, b, h, grid, st);
+  }
+}
+
+template <int OP, int FR>
+cudaError_t hc_dispatch(int fa, int fb, const CUtensorMap &a, const CUtensorMap &b, const HaloConv &h, int grid,
+                        cudaStream_t st) {
+  switch (fa) {
+    case 4: return hc_dispatch_b<OP, 4, FR>(fb, a, b, h, grid, st);
+    case 6: return hc_dispatch_b<OP, 6, FR>(fb, a, b, h, grid, st);
+    default: return hc_dispatch_b<OP, 8, FR>(fb, a, b, h, grid, st);
+  }
+}
+
+}  // namespace
+
+cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStream_t st) {
+  const int bba = block_bytes(cp.a.fmt), bbb = block_bytes(cp.b.fmt);
+  h.w_scales = cp.b.scales;
+  h.in_scales = cp.a.scales;
+  h.sa = cp.a.s_t;
+  h.sb = cp.b.s_t;
+  h.pre_mult = cp.pre_mult;
+  h.out = cp.out;
+  h.rq = cp.rq;
+  h.status = cp.status;
+  // input codes [Hin][Win][NG][CGin * BBA] as 8-byte units; box: one chunk's
+  // channel groups x G batch groups x WP positions x RH rows
+  CUtensorMap ma, mb;
+  {
+    const uint64_t d[4] = {(uint64_t)h.CGin * bba / 8, (uint64_t)h.NG, (uint64_t)h.Win, (uint64_t)h.Hin};
+    const uint32_t bx[4] = {(uint32_t)(CGC * bba / 8), (uint32_t)h.G, (uint32_t)h.WP, (uint32_t)h.RH};
+    if (!make_map(&ma, cp.a.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
+  }
+  {
+    // weights [taps][COG][CIG * BBB]
+    const uint64_t d[3] = {(uint64_t)h.CIG * bbb / 8, (uint64_t)h.COG, (uint64_t)(h.Kh * h.Kw)};
+    uint32_t bx[3];
+    if (cp.op == OP_FWD) {
+      bx[0] = (uint32_t)(CGC * bbb / 8); bx[1] = (uint32_t)h.NB; bx[2] = (uint32_t)(h.Kh * h.Kw);
+    } else {
+      bx[0] = (uint32_t)(h.NB * bbb / 8); bx[1] = (uint32_t)CGC; bx[2] = (uint32_t)(h.Kh * h.Kw);
+    }
+    if (!make_map(&mb, cp.b.codes, 8, 3, d, bx)) return cudaErrorInvalidValue;
+  }
+  const int grid = std::min(h.num_tiles, num_sms);
+  const int fa = cp.a.fmt, fb = cp.b.fmt;
+  if (cp.op == OP_FWD) {
+    if (cp.rq.codes) {
+      switch (cp.rq.fmt) {
+        case 4: return hc_dispatch<OP_FWD, 4>(fa, fb, ma, mb, h, grid, st);
+        case 6: return hc_dispatch<OP_FWD, 6>(fa, fb, ma, mb, h, grid, st);
+        default: return hc_dispatch<OP_FWD, 8>(fa, fb, ma, mb, h, grid, st);
+      }
+    }
+    return hc_dispatch<OP_FWD, 0>(fa, fb, ma, mb, h, grid, st);
+  }
+  if (cp.rq.codes) {
+    switch (cp.rq.fmt) {
+      case 4: return hc_dispatch<OP_DGRAD, 4>(fa, fb, ma, mb, h, grid, st);
+      case 6: return hc_dispatch<OP_DGRAD, 6>(fa, fb, ma, mb, h, grid, st);
+      default: return hc_dispatch<OP_DGRAD, 8>(fa, fb, ma, mb, h, grid, st);
+    }
+  }
+  return hc_dispatch<OP_DGRAD, 0>(fa, fb, ma, mb, h, grid, st);
+}
+
+}  // namespace mq

@@ -57,6 +57,38 @@ struct ConvParams {
   uint32_t *status;
 };
 
+// Stride-1 forward / data-gradient convolution with per-tile halo reuse
+// (conv_halo.cu).  Filled by halo_plan() from a ConvParams.
+struct HaloConv {
+  int op;
+  int N, NG;
+  int Hin, Win, CGin;            // correlation input (fwd: X; dgrad: dY) and its channel groups (K)
+  int Hout, Wout, NC, NCG;       // output dims and channels (fwd: Ho, Wo, Cout; dgrad: H, W, Cin)
+  int Kh, Kw, padh, padw;        // taps and padding of the correlation (dgrad: K - 1 - pad)
+  int P, G, R, WP, RH;           // tile: positions, batch groups, output rows; halo width / height
+  int BN, NB, acc_cols;          // output channels per tile, their groups, TMEM columns per row
+  int nchunks;                   // CGin / 2
+  int tiles_g, tiles_w, tiles_h, tiles_n, num_tiles;
+  int PS;                        // packed ring depth
+  const uint8_t *w_scales, *in_scales;
+  int COG, CIG;                  // weight block groups: W is [Kh*Kw][COG][CIG]
+  const float *sa, *sb;
+  float pre_mult;
+  float *out;                    // fp32 HWCN, nullable with rq
+  Requant rq;
+  uint32_t *status;
+  // shared-memory carve-up (bytes from the 1 KB-aligned base)
+  uint32_t off_dec, dec_stage, dec_b_off;
+  uint32_t off_pk, pk_stage, pk_b_off, pk_bytes;
+  uint32_t off_sc, sc_bytes, sc_stride;
+  uint32_t off_ctl;
+  int nh_blocks, nb_blocks;
+  size_t smem;
+};
+
+bool halo_plan(const ConvParams &cp, HaloConv &h);
+cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStream_t s);
+
 cudaError_t launch_amax(const void *src, int dtype, int64_t n, uint32_t *amax_bits, int num_sms, cudaStream_t s);
 cudaError_t launch_quantize(const void *src, int dtype, int layout, int fmt, const QuantParams &p, cudaStream_t s);
 
