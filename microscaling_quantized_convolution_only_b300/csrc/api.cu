@@ -112,10 +112,50 @@ mq_status run_conv(mq::ConvParams &p, int num_sms, cudaStream_t s) {
   return mq::launch_conv(p, num_sms, s) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
 }
 
+// Split-K partial sums of one plan.
+size_t partial_bytes(int splits, const mq::ConvParams &p) {
+  return (size_t)splits * (size_t)p.Cout * (size_t)(p.Kh * p.Kw * p.Cin) * sizeof(float);
+}
+
+// Workspace of the weight gradient: enough for every plan the call may pick
+// whatever the element formats (the halo kernel's tiling depends on them).
 size_t wgrad_ws_bytes(const mq_conv_desc *d) {
   mq::ConvParams p = base_params(d, mq::OP_WGRAD, nullptr);
   mq::conv_plan(p);
-  return (size_t)p.k_splits * (size_t)p.Cout * (size_t)p.ncols * sizeof(float);
+  size_t need = partial_bytes(p.k_splits, p);
+  for (int f : {MQ_FMT_E2M1, MQ_FMT_E2M3, MQ_FMT_E4M3}) {
+    mq::ConvParams q = base_params(d, mq::OP_WGRAD, nullptr);
+    q.a.fmt = q.b.fmt = f;
+    mq::HaloWgrad h;
+    if (mq::halo_wgrad_plan(q, h, 0)) need = std::max(need, partial_bytes(h.splits, q));
+  }
+  return need;
+}
+
+// Weight gradient into the split-K buffer `partials`, then the fixed-order
+// reduction into dW.  max_splits bounds the split count (0: none).
+mq_status run_wgrad(mq::ConvParams &p, float *partials, size_t bytes, int max_splits, float *dw, int num_sms,
+                    cudaStream_t s) {
+  p.out = partials;
+  mq::HaloWgrad h;
+  if (mq::halo_wgrad_plan(p, h, max_splits)) {
+    if (partial_bytes(h.splits, p) > bytes) return MQ_ERR_WORKSPACE;
+    if (mq::halo_wgrad_launch(p, h, num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
+    p.k_splits = h.splits;
+    p.ncols = h.ncols;
+  } else {
+    mq::conv_plan(p);
+    if (max_splits > 0 && p.k_splits > max_splits) {
+      int per = (p.kg_total + max_splits - 1) / max_splits;
+      per = (per + 7) / 8 * 8;
+      p.kg_per_split = per;
+      p.k_splits = (p.kg_total + per - 1) / per;
+    }
+    if (partial_bytes(p.k_splits, p) > bytes) return MQ_ERR_WORKSPACE;
+    if (mq::launch_conv(p, num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
+  }
+  if (mq::launch_wgrad_reduce(p, dw, s) != cudaSuccess) return MQ_ERR_CUDA;
+  return MQ_OK;
 }
 
 }  // namespace
@@ -308,11 +348,7 @@ mq_status mqconv_wgrad(const mq_conv_desc *desc, const mq_packed *dyq, const mq_
   p.a = operand(dyq);
   p.b = operand(xq);
   p.pre_mult = pre_mult(dyq->fmt, xq->fmt);
-  p.out = static_cast<float *>(workspace);
-  mq::conv_plan(p);
-  if (mq::launch_conv(p, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
-  if (mq::launch_wgrad_reduce(p, dw, s) != cudaSuccess) return MQ_ERR_CUDA;
-  return MQ_OK;
+  return run_wgrad(p, static_cast<float *>(workspace), ws_bytes, 0, dw, di->num_sms, s);
 }
 
 mq_status mqconv_wgrad_noalloc(const mq_conv_desc *desc, const mq_packed *dyq, const mq_packed *xq, float *dw,
@@ -331,24 +367,14 @@ mq_status mqconv_wgrad_noalloc(const mq_conv_desc *desc, const mq_packed *dyq, c
   p.a = operand(dyq);
   p.b = operand(xq);
   p.pre_mult = pre_mult(dyq->fmt, xq->fmt);
-  mq::conv_plan(p);
   // fit the split-K partial sums into the fixed scratch: fewer, longer splits
-  const size_t per_split = (size_t)p.Cout * (size_t)p.ncols * sizeof(float);
+  const size_t per_split = partial_bytes(1, p);
   const size_t max_splits = MQCONV_WGRAD_NOALLOC_SCRATCH_BYTES / per_split;
   if (max_splits == 0) return MQ_ERR_WORKSPACE;
-  if ((size_t)p.k_splits > max_splits) {
-    int per = (int)((p.kg_total + (int64_t)max_splits - 1) / (int64_t)max_splits);
-    per = (per + 7) / 8 * 8;
-    p.kg_per_split = per;
-    p.k_splits = (p.kg_total + per - 1) / per;
-  }
   float *scratch = nullptr;
   if ((st = scratch_addr(&scratch)) != MQ_OK) return st;
-  p.out = scratch;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (mq::launch_conv(p, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
-  if (mq::launch_wgrad_reduce(p, dw, s) != cudaSuccess) return MQ_ERR_CUDA;
-  return MQ_OK;
+  return run_wgrad(p, scratch, MQCONV_WGRAD_NOALLOC_SCRATCH_BYTES, (int)std::min<size_t>(max_splits, 1 << 20), dw,
+                   di->num_sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mq_status mqconv_device_status(mq_stream stream, int32_t *host_status) {

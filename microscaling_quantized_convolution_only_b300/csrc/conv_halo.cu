@@ -417,6 +417,251 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
   if (warp == HC_MMA_WARP) tmem_dealloc(tmem, 512);
 }
 
+
+// ---------------------------------------------------------------- wgrad
+// G_W[co][kh][kw][ci] = sum over (ho, wo, n) of dY[ho][wo][co][n] *
+// X[ho + kh - pad][wo + kw - pad][ci][n]  (MicroQonv §IV-A: G_W = G_Y X'^T).
+// A CTA tile fixes kh, a block of 128 output channels and BNc input channels
+// and walks a range of chunks; a chunk is one output row ho, P positions and
+// G batch groups (K = 8 P G).  Per chunk it stages the dY blocks (P x G x 16
+// channel groups) and the one-row X halo (P + Kw - 1 positions) and decodes
+// both once; tap kw reads the halo through a descriptor shifted by kw
+// positions.  Accumulator kw (128 x BNc fp32) sits at TMEM column kw * acc.
+// Both operands are MN-major: a block row is 8 channels of one batch element.
+struct WgCtl {
+  uint64_t pfull[MAX_PS], pempty[MAX_PS];
+  uint64_t dfull[DSTAGES], dempty[DSTAGES];
+  uint64_t acc_full, acc_empty;
+  uint64_t done;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+struct WgTile {
+  int kh, c0, m0, split, q0, q1;   // kernel row, first input / output channel, split, chunk range
+};
+
+__device__ __forceinline__ WgTile wg_tile(const HaloWgrad &p, int t) {
+  WgTile w;
+  int r = t;
+  w.kh = r % p.Kh;
+  r /= p.Kh;
+  w.c0 = (r % p.c_tiles) * p.BNc;
+  r /= p.c_tiles;
+  w.m0 = (r % p.m_tiles) * 128;
+  w.split = r / p.m_tiles;
+  w.q0 = w.split * p.chunks_per_split;
+  w.q1 = min(p.total_chunks, w.q0 + p.chunks_per_split);
+  return w;
+}
+
+__device__ __forceinline__ bool wg_wait(uint64_t *bar, uint32_t parity, const HaloWgrad &p, WgCtl *ctl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (ctl->abort_flag) return false;
+      if (globaltimer_ns() - t0 > 2000000000ull) {
+        atomicOr(p.status, ST_TIMEOUT);
+        ctl->abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <int FA, int FB>
+__global__ void __launch_bounds__(HC_THREADS, 1)
+    halo_wgrad_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const HaloWgrad p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  WgCtl *ctl = reinterpret_cast<WgCtl *>(smem + p.off_ctl);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int BBA = Fmt<FA>::BLOCK_BYTES, BBB = Fmt<FB>::BLOCK_BYTES;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.PS; ++s) {
+      mbar_init(&ctl->pfull[s], 32);
+      mbar_init(&ctl->pempty[s], HC_DEC_THREADS);
+    }
+    for (int s = 0; s < DSTAGES; ++s) {
+      mbar_init(&ctl->dfull[s], HC_DEC_THREADS);
+      mbar_init(&ctl->dempty[s], 1);
+    }
+    mbar_init(&ctl->acc_full, 1);
+    mbar_init(&ctl->acc_empty, HC_EPI_WARPS * 32);
+    mbar_init(&ctl->done, 1);
+    ctl->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == HC_MMA_WARP) tmem_alloc(&ctl->tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == HC_TMA_WARP) {
+    // ----------------------------------------------------------- producer
+    // all lanes gather the chunk's block scales (zero where the block is out
+    // of range), lane 0 issues the two code boxes; 32 arrivals + the bytes
+    // complete a stage.
+    int pit = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      const WgTile T = wg_tile(p, t);
+      for (int q = T.q0; q < T.q1; ++q, ++pit) {
+        const int ps = pit % p.PS;
+        int okw = 1;
+        if (lane == 0) okw = wg_wait(&ctl->pempty[ps], ((pit / p.PS) & 1) ^ 1, p, ctl) ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, okw, 0)) { ok = false; break; }
+        const int gb = q % p.tiles_g, rest = q / p.tiles_g;
+        const int g0 = gb * p.G, wo0 = (rest % p.tiles_w) * p.P, ho = rest / p.tiles_w;
+        const int hi = ho + T.kh - p.pad;
+        uint8_t *stage = smem + p.off_pk + ps * p.pk_stage;
+        uint8_t *sc = stage + p.pk_sc_off;
+        for (int i = lane; i < p.na_blocks; i += 32) {      // (p, j, m)
+          const int m = i & 15, pj = i >> 4, pp = pj / p.G, j = pj - pp * p.G;
+          const int wo = wo0 + pp, cog = T.m0 / 8 + m;
+          uint8_t v = 0;
+          if (wo < p.Wo && cog < p.COG)
+            v = __ldg(p.a_scales + (((int64_t)ho * p.Wo + wo) * p.NG + g0 + j) * p.COG + cog);
+          sc[i] = v;
+        }
+        for (int i = lane; i < p.nb_blocks; i += 32) {      // (wc, j, cb)
+          const int cb = i % p.CB, wj = i / p.CB, wc = wj / p.G, j = wj - wc * p.G;
+          const int wi = wo0 - p.pad + wc, cig = T.c0 / 8 + cb;
+          uint8_t v = 0;
+          if ((unsigned)hi < (unsigned)p.H && (unsigned)wi < (unsigned)p.W && cig < p.CIG)
+            v = __ldg(p.b_scales + (((int64_t)hi * p.W + wi) * p.NG + g0 + j) * p.CIG + cig);
+          sc[p.na_blocks + i] = v;
+        }
+        if (lane == 0) {
+          mbar_expect_tx(&ctl->pfull[ps], p.pk_bytes);
+          tma_load_4d(stage, &tm_a, &ctl->pfull[ps], (T.m0 / 8) * BBA / 8, g0, wo0, ho);
+          tma_load_4d(stage + p.pk_b_off, &tm_b, &ctl->pfull[ps], (T.c0 / 8) * BBB / 8, g0, wo0 - p.pad, hi);
+        } else {
+          mbar_arrive(&ctl->pfull[ps]);
+        }
+      }
+    }
+    if (lane == 0) {
+      for (int i = 0; i < p.PS && i < pit; ++i) {
+        const int q = pit - 1 - i;
+        wg_wait(&ctl->pfull[q % p.PS], (q / p.PS) & 1, p, ctl);
+      }
+    }
+    __syncwarp();
+  } else if (warp < HC_DEC_WARPS) {
+    // ------------------------------------------------------------ decoders
+    const int tid = threadIdx.x;
+    int pit = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      const WgTile T = wg_tile(p, t);
+      for (int q = T.q0; q < T.q1; ++q, ++pit) {
+        const int ps = pit % p.PS, ds = pit % DSTAGES;
+        if (!wg_wait(&ctl->pfull[ps], (pit / p.PS) & 1, p, ctl)) { ok = false; break; }
+        if (!wg_wait(&ctl->dempty[ds], ((pit / DSTAGES) & 1) ^ 1, p, ctl)) { ok = false; break; }
+        const uint8_t *pk = smem + p.off_pk + ps * p.pk_stage;
+        const uint8_t *sc = pk + p.pk_sc_off;
+        uint8_t *dec = smem + p.off_dec + ds * p.dec_stage;
+        const int na = p.na_blocks * 8;
+        for (int i = tid; i < na; i += HC_DEC_THREADS) {
+          const int blk = i >> 3, r = i & 7;
+          const uint4 v = decode_raw<FA>(lds_row<FA>(pk + blk * BBA, r), scale_pair<FA>(sc[blk]));
+          *reinterpret_cast<uint4 *>(dec + i * 16) = v;
+        }
+        const int nb = p.nb_blocks * 8;
+        const uint8_t *pkb = pk + p.pk_b_off;
+        uint8_t *decb = dec + p.dec_b_off;
+        for (int i = tid; i < nb; i += HC_DEC_THREADS) {
+          const int blk = i >> 3, r = i & 7;
+          const uint4 v = decode_raw<FB>(lds_row<FB>(pkb + blk * BBB, r), scale_pair<FB>(sc[p.na_blocks + blk]));
+          *reinterpret_cast<uint4 *>(decb + i * 16) = v;
+        }
+        fence_async_smem();
+        mbar_arrive(&ctl->pempty[ps]);
+        mbar_arrive(&ctl->dfull[ds]);
+      }
+    }
+  } else if (warp == HC_MMA_WARP) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(128, p.BNc, true, true);
+      const uint32_t a_lbo = 16 * 128, b_lbo = (uint32_t)p.CB * 128;
+      int pit = 0, k = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
+        const WgTile T = wg_tile(p, t);
+        if (!wg_wait(&ctl->acc_empty, (k & 1) ^ 1, p, ctl)) break;
+        tc_fence_after();
+        for (int q = T.q0; q < T.q1; ++q, ++pit) {
+          const int ds = pit % DSTAGES;
+          if (!wg_wait(&ctl->dfull[ds], (pit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + p.off_dec + ds * p.dec_stage);
+          const uint32_t b0 = a0 + p.dec_b_off;
+          for (int kw = 0; kw < p.Kw; ++kw) {
+            const uint32_t d = tmem + kw * p.acc_cols;
+            for (int kk = 0; kk < p.KG / 2; ++kk) {
+              const uint64_t ad = sdesc(a0 + kk * 2 * a_lbo, a_lbo, 128);
+              const uint64_t bd = sdesc(b0 + (kw * p.G * p.CB + kk * 2 * p.CB) * 128, b_lbo, 128);
+              umma_f16(d, ad, bd, idesc, (q > T.q0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(&ctl->dempty[ds]);
+        }
+        if (!ok) break;
+        umma_commit(&ctl->acc_full);
+      }
+      umma_commit(&ctl->done);
+      wg_wait(&ctl->done, 0, p, ctl);
+    }
+    __syncwarp();
+  } else if (warp >= HC_EPI_WARP0 && warp < HC_EPI_WARP0 + HC_EPI_WARPS) {
+    // ------------------------------------------------------------- epilogue
+    const int qd = warp & 3;
+    const int row = qd * 32 + lane;
+    int k = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++k) {
+      const WgTile T = wg_tile(p, t);
+      if (!wg_wait(&ctl->acc_full, k & 1, p, ctl)) break;
+      tc_fence_after();
+      const int co = T.m0 + row;
+      float *orow = p.out + ((int64_t)T.split * p.Cout + co) * p.ncols + (int64_t)T.kh * p.Kw * p.Cin + T.c0;
+      for (int kw = 0; kw < p.Kw; ++kw) {
+        const uint32_t tb = tmem + kw * p.acc_cols + ((uint32_t)(qd * 32) << 16);
+        for (int c = 0; c < p.BNc; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(tb + c, r);
+          tmem_wait_ld();
+          if (co < p.Cout) {
+            float *o = orow + kw * p.Cin + c;
+            if (T.c0 + c + 16 <= p.Cin) {
+#pragma unroll
+              for (int jj = 0; jj < 16; jj += 4)
+                *reinterpret_cast<float4 *>(o + jj) = make_float4(__uint_as_float(r[jj]), __uint_as_float(r[jj + 1]),
+                                                                  __uint_as_float(r[jj + 2]), __uint_as_float(r[jj + 3]));
+            } else {
+              for (int jj = 0; jj < 16; ++jj)
+                if (T.c0 + c + jj < p.Cin) o[jj] = __uint_as_float(r[jj]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&ctl->acc_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == HC_MMA_WARP) tmem_dealloc(tmem, 512);
+}
+
 // ------------------------------------------------------------------ host
 namespace {
 
@@ -640,6 +885,128 @@ cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStre
     }
   }
   return hc_dispatch<OP_DGRAD, 0>(fa, fb, ma, mb, h, grid, st);
+}
+
+
+namespace {
+
+size_t wgrad_smem(HaloWgrad &h, int bba, int bbb) {
+  h.WP = h.P + h.Kw - 1;
+  h.na_blocks = h.KG * 16;
+  h.nb_blocks = h.WP * h.G * h.CB;
+  h.dec_b_off = (uint32_t)h.na_blocks * 128;
+  h.dec_stage = (uint32_t)(h.na_blocks + h.nb_blocks) * 128;
+  h.pk_b_off = (uint32_t)((h.na_blocks * bba + 127) / 128 * 128);
+  h.pk_sc_off = (uint32_t)((h.pk_b_off + h.nb_blocks * bbb + 127) / 128 * 128);
+  h.pk_bytes = (uint32_t)(h.na_blocks * bba + h.nb_blocks * bbb);
+  h.pk_stage = (uint32_t)((h.pk_sc_off + h.na_blocks + h.nb_blocks + 127) / 128 * 128);
+  const size_t fixed = 1024 + (size_t)DSTAGES * h.dec_stage + sizeof(WgCtl) + 128;
+  if (fixed + 2 * (size_t)h.pk_stage > SMEM_LIMIT) return 0;
+  h.PS = (int)std::min<size_t>(MAX_PS, (SMEM_LIMIT - fixed) / h.pk_stage);
+  h.off_dec = 0;
+  h.off_pk = DSTAGES * h.dec_stage;
+  h.off_ctl = h.off_pk + h.PS * h.pk_stage;
+  return 1024 + (size_t)h.off_ctl + sizeof(WgCtl);
+}
+
+constexpr int WG_TARGET_CTAS = 148;   // split-K sized for one wave on a 148-SM B300
+
+}  // namespace
+
+bool halo_wgrad_plan(const ConvParams &cp, HaloWgrad &h, int max_splits) {
+  std::memset(&h, 0, sizeof(h));
+  if (cp.op != OP_WGRAD || cp.stride != 1) return false;
+  h.N = cp.N; h.NG = cp.NG; h.H = cp.H; h.W = cp.W; h.Ho = cp.Ho; h.Wo = cp.Wo;
+  h.Cin = cp.Cin; h.Cout = cp.Cout; h.CIG = cp.CIG; h.COG = cp.COG;
+  h.Kh = cp.Kh; h.Kw = cp.Kw; h.pad = cp.pad;
+  h.ncols = cp.Kh * cp.Kw * cp.Cin;
+  if (h.Kw > 16 || h.Kh > 64) return false;
+  // chunk: P positions x G batch groups, 16 k-groups, least padding waste
+  int best = -1;
+  double best_waste = 1e30;
+  for (int P = 16; P >= 1; P >>= 1) {
+    const int G = 16 / P;
+    if (G > h.NG || h.NG % G) continue;
+    const double waste = (double)((h.Wo + P - 1) / P * P) / h.Wo;
+    if (waste < best_waste - 1e-9) {
+      best_waste = waste;
+      best = P;
+    }
+  }
+  if (best < 0) return false;
+  h.P = best;
+  h.G = 16 / best;
+  h.KG = 16;
+  const int bba = block_bytes(cp.a.fmt), bbb = block_bytes(cp.b.fmt);
+  h.BNc = std::min(128, (h.Cin + 15) / 16 * 16);
+  for (;;) {
+    h.CB = (h.BNc + 7) / 8;
+    h.acc_cols = pow2_at_least32(h.BNc);
+    const bool fits_tmem = h.Kw * h.acc_cols <= 512;
+    if (fits_tmem && (h.smem = wgrad_smem(h, bba, bbb)) != 0) break;
+    if (h.BNc <= 16) return false;
+    h.BNc = std::max(16, h.BNc / 2 / 16 * 16);
+  }
+  if (h.BNc % 16) return false;
+  h.m_tiles = (h.Cout + 127) / 128;
+  h.c_tiles = (h.Cin + h.BNc - 1) / h.BNc;
+  h.tiles_w = (h.Wo + h.P - 1) / h.P;
+  h.tiles_g = h.NG / h.G;
+  const int64_t q = (int64_t)h.Ho * h.tiles_w * h.tiles_g;
+  if (q <= 0 || q > INT32_MAX) return false;
+  h.total_chunks = (int)q;
+  const int groups = h.m_tiles * h.c_tiles * h.Kh;
+  int s = std::max(1, WG_TARGET_CTAS / groups);
+  s = std::min(s, h.total_chunks);
+  if (max_splits > 0) s = std::min(s, max_splits);
+  h.chunks_per_split = (h.total_chunks + s - 1) / s;
+  h.splits = (h.total_chunks + h.chunks_per_split - 1) / h.chunks_per_split;   // every split non-empty
+  const int64_t nt = (int64_t)groups * h.splits;
+  if (nt > INT32_MAX) return false;
+  h.num_tiles = (int)nt;
+  return true;
+}
+
+cudaError_t halo_wgrad_launch(const ConvParams &cp, HaloWgrad &h, int num_sms, cudaStream_t st) {
+  const int bba = block_bytes(cp.a.fmt), bbb = block_bytes(cp.b.fmt);
+  h.a_scales = cp.a.scales;
+  h.b_scales = cp.b.scales;
+  h.out = cp.out;
+  h.status = cp.status;
+  CUtensorMap ma, mb;
+  {
+    // dY codes [Ho][Wo][NG][COG * BBA]; box: 16 channel groups x G x P x 1 row
+    const uint64_t d[4] = {(uint64_t)h.COG * bba / 8, (uint64_t)h.NG, (uint64_t)h.Wo, (uint64_t)h.Ho};
+    const uint32_t bx[4] = {(uint32_t)(16 * bba / 8), (uint32_t)h.G, (uint32_t)h.P, 1u};
+    if (!make_map(&ma, cp.a.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
+  }
+  {
+    // X codes [H][W][NG][CIG * BBB]; box: CB channel groups x G x WP x 1 row
+    const uint64_t d[4] = {(uint64_t)h.CIG * bbb / 8, (uint64_t)h.NG, (uint64_t)h.W, (uint64_t)h.H};
+    const uint32_t bx[4] = {(uint32_t)(h.CB * bbb / 8), (uint32_t)h.G, (uint32_t)h.WP, 1u};
+    if (!make_map(&mb, cp.b.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
+  }
+  const int grid = std::min(h.num_tiles, num_sms);
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, HC_THREADS, h.smem, st>>>(ma, mb, h);
+    return cudaGetLastError();
+  };
+  const int fa = cp.a.fmt, fb = cp.b.fmt;
+  if (fa == 4) {
+    if (fb == 4) return go(halo_wgrad_kernel<4, 4>);
+    if (fb == 6) return go(halo_wgrad_kernel<4, 6>);
+    return go(halo_wgrad_kernel<4, 8>);
+  }
+  if (fa == 6) {
+    if (fb == 4) return go(halo_wgrad_kernel<6, 4>);
+    if (fb == 6) return go(halo_wgrad_kernel<6, 6>);
+    return go(halo_wgrad_kernel<6, 8>);
+  }
+  if (fb == 4) return go(halo_wgrad_kernel<8, 4>);
+  if (fb == 6) return go(halo_wgrad_kernel<8, 6>);
+  return go(halo_wgrad_kernel<8, 8>);
 }
 
 }  // namespace mq

@@ -86,7 +86,33 @@ struct HaloConv {
   size_t smem;
 };
 
+// Stride-1 weight gradient with per-chunk halo reuse (conv_halo.cu).  Each
+// CTA tile accumulates one kernel row (kh) x Kw taps x BNc input channels x
+// 128 output channels over a range of (output row, positions, batch groups)
+// chunks and writes one split-K partial.
+struct HaloWgrad {
+  int N, NG, H, W, Ho, Wo, Cin, Cout, CIG, COG, Kh, Kw, pad;
+  int P, G, KG, WP;              // chunk: P positions x G batch groups = KG k-groups (K = 8 KG)
+  int BNc, CB, acc_cols;         // input channels per tile, their groups, TMEM columns per tap
+  int m_tiles, c_tiles, splits, chunks_per_split, total_chunks;
+  int tiles_w, tiles_g;
+  int num_tiles;
+  int PS;
+  const uint8_t *a_scales, *b_scales;   // dY, X
+  float *out;                    // partial sums [split][Cout][Kh * Kw * Cin]
+  int ncols;
+  uint32_t *status;
+  uint32_t off_dec, dec_stage, dec_b_off;
+  uint32_t off_pk, pk_stage, pk_b_off, pk_sc_off, pk_bytes;
+  uint32_t off_ctl;
+  int na_blocks, nb_blocks;
+  size_t smem;
+};
+
 bool halo_plan(const ConvParams &cp, HaloConv &h);
+// max_splits <= 0: no limit
+bool halo_wgrad_plan(const ConvParams &cp, HaloWgrad &h, int max_splits);
+cudaError_t halo_wgrad_launch(const ConvParams &cp, HaloWgrad &h, int num_sms, cudaStream_t s);
 cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStream_t s);
 
 cudaError_t launch_amax(const void *src, int dtype, int64_t n, uint32_t *amax_bits, int num_sms, cudaStream_t s);
