@@ -335,6 +335,17 @@ class LayersStep:
                 "dw": [d["dw"].cpu().pin_memory() for d in self.layers]}
 
 
+def workload(args):
+    import dataclasses
+    wl = S.WORKLOADS[WORKLOADS[args.workload]]
+    if args.batch:
+        if args.batch % 8:
+            raise SystemExit("--batch must be a multiple of 8")
+        wl = dataclasses.replace(wl, name=f"{wl.name}-N{args.batch}",
+                                 layers=[S.scaled_layer(L, N=args.batch) for L in wl.layers])
+    return wl
+
+
 def make_step(wl, device):
     return StackStep(wl, device) if wl.chained else LayersStep(wl, device)
 
@@ -373,7 +384,7 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
-    wl = S.WORKLOADS[WORKLOADS[args.workload]]
+    wl = workload(args)
     step = make_step(wl, device)
     peaks = load_peaks()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)   # > 126 MB L2
@@ -585,6 +596,9 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stack4-nvfp4")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch N (multiple of 8) for small profiling captures; "
+                         "the default runs the workload as specified")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl != "reference":
         print("note: warm-up raised to 3 steps", file=sys.stderr)

@@ -50,7 +50,8 @@ mq_status check_packed(const mq_packed *t, int32_t role, int64_t d0, int64_t d1,
   if (!t || !t->codes || !t->scales || !t->s_t) return MQ_ERR_INVALID_ARG;
   if (!fmt_ok(t->fmt) || t->role != role) return MQ_ERR_INVALID_ARG;
   if (t->dims[0] != d0 || t->dims[1] != d1 || t->dims[2] != d2 || t->dims[3] != d3) return MQ_ERR_INVALID_ARG;
-  if (!aligned16(t->codes) || (reinterpret_cast<uintptr_t>(t->s_t) & 3u)) return MQ_ERR_ALIGNMENT;
+  if (!aligned16(t->codes) || !aligned16(t->scales) || (reinterpret_cast<uintptr_t>(t->s_t) & 3u))
+    return MQ_ERR_ALIGNMENT;
   return MQ_OK;
 }
 

@@ -113,6 +113,20 @@ template <int FMT> __device__ __forceinline__ uint32_t block_scale_code(float am
   return resolve_tie<8>(amax_b, Fmt<FMT>::EMAX, s_t, c_lo, c_hi);
 }
 
+// Same decision as block_scale_code, with the quotient formed from a
+// precomputed inv_den = rcp(maxB_ef * s_t): the bracket [q(1-eps), q(1+eps)]
+// still contains the exact quotient (a few fp32 roundings, each 2^-24, are
+// far inside eps = 2^-20) and the tie test stays exact.
+template <int FMT>
+__device__ __forceinline__ uint32_t block_scale_code_r(float amax_b, float s_t, float inv_den) {
+  if (!(s_t > 0.0f)) return 0u;
+  const float q = amax_b * inv_den;
+  uint32_t c_lo = cvt2<8>(q * (1.0f - QEPS), 0.0f) & 0xFFu;
+  uint32_t c_hi = cvt2<8>(q * (1.0f + QEPS), 0.0f) & 0xFFu;
+  if (c_lo == c_hi) return c_lo;
+  return resolve_tie<8>(amax_b, Fmt<FMT>::EMAX, s_t, c_lo, c_hi);
+}
+
 // ------------------------------------------------------------- misc device
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -274,6 +288,73 @@ template <int F> __device__ __forceinline__ uint32_t scale_pair(uint8_t sc) {
   uint32_t h = dec2<8>((uint32_t)sc) & 0xFFFFu;
   if (F == 8) h = hmul2u(h, 0x3400u);   // x 0.25 (exact: a power of two, stays normal)
   return h | (h << 16);
+}
+
+}  // namespace mq
+
+namespace mq {
+
+// -------------------------------------------------------------- cp.async
+// Asynchronous global -> shared copy of BYTES (4, 8 or 16) bytes; when
+// `valid` is false nothing is read and the destination is zero-filled.
+template <int BYTES>
+__device__ __forceinline__ void cp_async_zfill(void *dst, const void *src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(smem_u32(dst)), "l"(src), "n"(BYTES),
+               "r"(valid ? BYTES : 0)
+               : "memory");
+}
+// arrive on `bar` once every cp.async this thread issued so far has landed
+// (counts as one of the barrier's expected arrivals)
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// add `bytes` to the transaction count of the current phase without arriving
+__device__ __forceinline__ void mbar_add_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Copy `nruns` byte runs into shared memory: run r has `len(r)` valid bytes
+// (a multiple of GRAN) starting at `src(r)` (GRAN-aligned; null: no valid
+// bytes) and occupies `fill` bytes at dst + r * stride, the bytes past
+// len(r) zero-filled.  Lane-strided over a warp.  GRAN >= 4 issues cp.async
+// copies (complete them with cp_async_arrive); GRAN 1 or 2 copies
+// synchronously (complete with an ordinary arrive).
+template <int GRAN, class SrcF, class LenF>
+__device__ __forceinline__ void copy_runs(uint8_t *dst, int nruns, int stride, int fill, SrcF src, LenF len,
+                                          const uint8_t *safe, int lane) {
+  const int per = fill / GRAN;
+  for (int i = lane; i < nruns * per; i += 32) {
+    const int r = i / per, part = i - r * per;
+    const uint8_t *s = src(r);
+    const bool ok = s != nullptr && part * GRAN < len(r);
+    uint8_t *d = dst + r * stride + part * GRAN;
+    if constexpr (GRAN >= 4) {
+      cp_async_zfill<GRAN>(d, ok ? s + part * GRAN : safe, ok);
+    } else {
+      uint8_t v[GRAN];
+#pragma unroll
+      for (int b = 0; b < GRAN; ++b) v[b] = ok ? __ldg(s + part * GRAN + b) : (uint8_t)0;
+#pragma unroll
+      for (int b = 0; b < GRAN; ++b) d[b] = v[b];
+    }
+  }
+}
+
+// copy_runs with the granule chosen at run time (1, 2, 4, 8 or 16).  A
+// stage filled this way completes with two arrivals per lane:
+// cp_async_arrive (the asynchronous copies) and mbar_arrive (release of the
+// synchronous ones).
+// `safe`: any valid global address, given to zero-filling copies that read nothing.
+template <class SrcF, class LenF>
+__device__ __forceinline__ void copy_runs_rt(int gran, uint8_t *dst, int nruns, int stride, int fill, SrcF src,
+                                             LenF len, const uint8_t *safe, int lane) {
+  switch (gran) {
+    case 16: copy_runs<16>(dst, nruns, stride, fill, src, len, safe, lane); break;
+    case 8: copy_runs<8>(dst, nruns, stride, fill, src, len, safe, lane); break;
+    case 4: copy_runs<4>(dst, nruns, stride, fill, src, len, safe, lane); break;
+    case 2: copy_runs<2>(dst, nruns, stride, fill, src, len, safe, lane); break;
+    default: copy_runs<1>(dst, nruns, stride, fill, src, len, safe, lane); break;
+  }
 }
 
 }  // namespace mq

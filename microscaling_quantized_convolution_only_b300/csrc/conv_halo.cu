@@ -26,9 +26,11 @@
 // tile, because the MMA warp waits for accumulator s only before its own
 // first MMA into it.
 //
-// Warp roles: warps 0-7 decode, warps 8-11 drain the accumulators
-// (tcgen05.ld) into fp32 HWCN outputs or requantized CBF blocks, warp 12 lane
-// 0 issues the TMA loads, warp 13 lane 0 issues tcgen05.mma.  Every wait is
+// Warp roles: warps 0-7 decode, warps 8-15 drain the accumulators
+// (tcgen05.ld; warps w and w+4 share TMEM lane quadrant w % 4 and take
+// alternate 16-column chunks) into fp32 HWCN outputs or requantized CBF
+// blocks, warp 16 copies block scales and issues the TMA loads (lane 0),
+// warp 17 lane 0 issues tcgen05.mma.  Every wait is
 // bounded; on expiry the CTA records MQ_ERR_TIMEOUT, stops, lets its copies
 // and MMAs in flight finish and frees its TMEM.
 #include <cuda.h>
@@ -36,6 +38,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <numeric>
 #include <mutex>
 
 #include "common.cuh"
@@ -47,10 +50,10 @@ namespace {
 
 constexpr int HC_DEC_WARPS = 8;
 constexpr int HC_EPI_WARP0 = 8;
-constexpr int HC_EPI_WARPS = 4;
-constexpr int HC_TMA_WARP = 12;
-constexpr int HC_MMA_WARP = 13;
-constexpr int HC_THREADS = 14 * 32;
+constexpr int HC_EPI_WARPS = 8;   // two per TMEM lane quadrant, alternating 16-column chunks
+constexpr int HC_TMA_WARP = 16;
+constexpr int HC_MMA_WARP = 17;
+constexpr int HC_THREADS = 18 * 32;
 constexpr int HC_DEC_THREADS = HC_DEC_WARPS * 32;
 constexpr int CGC = 2;          // channel groups (8 channels each) per chunk: K = 16 per tap
 constexpr int DSTAGES = 2;      // decoded ring depth
@@ -113,7 +116,7 @@ __device__ __forceinline__ TileCoord hc_tile(const HaloConv &p, int t) {
 // eight batch rows of one block; the block amax is their shuffle-max.
 template <int F>
 __device__ __forceinline__ void hc_requant16(const HaloConv &p, const float (&y)[16], int64_t blk_pos_ng, int n_in,
-                                             int co0, bool row_ok, float s_t, uint32_t &amax_acc) {
+                                             int co0, bool row_ok, float s_t, float inv_den, uint32_t &amax_acc) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int co = co0 + 8 * h;
@@ -129,7 +132,7 @@ __device__ __forceinline__ void hc_requant16(const HaloConv &p, const float (&y)
     for (int o = 1; o < 8; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     amax_acc = max(amax_acc, m);
     if (!row_ok || co >= p.NC) continue;
-    const uint32_t bsc = block_scale_code<F>(__uint_as_float(m), s_t);
+    const uint32_t bsc = block_scale_code_r<F>(__uint_as_float(m), s_t, inv_den);
     const float bs = code_value<8>(bsc);
     // codes of the eight values (exact RN of the real quotient, as the quantizer)
     float inv_lo = 0.0f, inv_hi = 0.0f;
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
       mbar_init(&ctl->dempty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&ctl->sfull[s], 32);
+      mbar_init(&ctl->sfull[s], 64);
       mbar_init(&ctl->sempty[s], HC_DEC_THREADS);
     }
     for (int s = 0; s < p.R; ++s) {
@@ -217,9 +220,10 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
 
   if (warp == HC_TMA_WARP) {
     // ------------------------------------------------------- TMA producer
-    // The whole warp gathers the tile's halo block scales (zero outside the
-    // image: those blocks' codes are zero-filled by the TMA as well); lane 0
-    // then streams the packed codes of every chunk.
+    // Per tile the whole warp copies the halo block scales (zero outside the
+    // image, where the TMA zero-fills the codes too) and the weight block
+    // scales asynchronously into the tile's scale buffer (64 arrivals: two
+    // per lane); lane 0 then streams the packed codes of every chunk.
     int pit = 0, k = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
@@ -229,17 +233,36 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
       if (lane == 0) okw = hc_wait(&ctl->sempty[tb], ((k >> 1) & 1) ^ 1, p, ctl) ? 1 : 0;
       if (!__shfl_sync(0xFFFFFFFFu, okw, 0)) break;
       uint8_t *scd = smem + p.off_sc + tb * p.sc_stride;
-      const int rowb = p.G * p.CGin;                       // bytes per halo position
-      for (int i = lane; i < (int)p.sc_bytes; i += 32) {
-        const int hw = i / rowb, b = i - hw * rowb;
-        const int hr = hw / p.WP, wc = hw - hr * p.WP;
-        const int hi = tc.h0 - p.padh + hr, wi = tc.w0 - p.padw + wc;
-        uint8_t v = 0;
-        if ((unsigned)hi < (unsigned)p.Hin && (unsigned)wi < (unsigned)p.Win)
-          v = __ldg(p.in_scales + (((int64_t)hi * p.Win + wi) * p.NG + tc.g0) * p.CGin + b);
-        scd[i] = v;
+      {
+        // halo block scales: one run of G * CGin bytes per halo position
+        const int run = p.G * p.CGin;
+        copy_runs_rt(
+            p.gran_h, scd, p.RH * p.WP, run, run,
+            [&](int r) -> const uint8_t * {
+              const int hr = r / p.WP, wc = r - hr * p.WP;
+              const int hi = tc.h0 - p.padh + hr, wi = tc.w0 - p.padw + wc;
+              if ((unsigned)hi >= (unsigned)p.Hin || (unsigned)wi >= (unsigned)p.Win) return nullptr;
+              return p.in_scales + (((int64_t)hi * p.Win + wi) * p.NG + tc.g0) * p.CGin;
+            },
+            [&](int) { return run; }, p.in_scales, lane);
+        // weight block scales of the tile's output channels
+        const int nb0 = tc.n0 / 8;
+        if (OP == OP_FWD) {
+          const int nbv = min(p.NB, p.COG - nb0), fill = p.NB * p.CIG;
+          copy_runs_rt(
+              p.gran_w, scd + p.scw_off, p.Kh * p.Kw, fill, fill,
+              [&](int tap) -> const uint8_t * { return p.w_scales + ((int64_t)tap * p.COG + nb0) * p.CIG; },
+              [&](int) { return nbv * p.CIG; }, p.w_scales, lane);
+        } else {
+          const int nbv = min(p.NB, p.CIG - nb0);
+          copy_runs_rt(
+              p.gran_w, scd + p.scw_off, p.Kh * p.Kw * p.COG, p.NB, p.NB,
+              [&](int r) -> const uint8_t * { return p.w_scales + (int64_t)r * p.CIG + nb0; },
+              [&](int) { return nbv; }, p.w_scales, lane);
+        }
+        cp_async_arrive(&ctl->sfull[tb]);
+        mbar_arrive(&ctl->sfull[tb]);
       }
-      mbar_arrive(&ctl->sfull[tb]);
       if (lane == 0) {
         for (int c = 0; c < p.nchunks; ++c, ++pit) {
           const int ps = pit % p.PS;
@@ -294,18 +317,18 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
         const int nbr = p.nb_blocks * 8;
         uint8_t *decb = dec + p.dec_b_off;
         const uint8_t *pkb = pk + p.pk_b_off;
+        const uint8_t *scw = sc + p.scw_off;
         for (int i = tid; i < nbr; i += HC_DEC_THREADS) {
           const int blk = i >> 3, r = i & 7;
-          uint8_t s = 0;
-          if (OP == OP_FWD) {
-            const int tap = blk / (p.NB * CGC), rem = blk - tap * (p.NB * CGC), nb = rem / CGC, kc = rem - nb * CGC;
-            const int cog = tc.n0 / 8 + nb;
-            if (cog < p.COG) s = __ldg(p.w_scales + ((int64_t)tap * p.COG + cog) * p.CIG + c * CGC + kc);
-          } else {
-            const int tap = blk / (p.NB * CGC), rem = blk - tap * (p.NB * CGC), kc = rem / p.NB, nb = rem - kc * p.NB;
-            const int cig = tc.n0 / 8 + nb;
-            if (cig < p.CIG) s = __ldg(p.w_scales + ((int64_t)tap * p.COG + c * CGC + kc) * p.CIG + cig);
+          int si;
+          if (OP == OP_FWD) {   // block (tap, nb, kc); scales [tap][nb][cig]
+            const int tn = blk / CGC, kc = blk - tn * CGC;
+            si = tn * p.CIG + c * CGC + kc;
+          } else {              // block (tap, kc, nb); scales [tap][cog][nb]
+            const int tk = blk / p.NB, nb = blk - tk * p.NB, tap = tk / CGC, kc = tk - tap * CGC;
+            si = (tap * p.COG + c * CGC + kc) * p.NB + nb;
           }
+          const uint8_t s = scw[si];
           const uint4 v = decode_raw<FB>(lds_row<FB>(pkb + blk * BBB, r), scale_pair<FB>(s));
           *reinterpret_cast<uint4 *>(decb + i * 16) = v;
         }
@@ -362,11 +385,16 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
   } else if (warp >= HC_EPI_WARP0 && warp < HC_EPI_WARP0 + HC_EPI_WARPS) {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;                       // TMEM lanes 32q .. 32q+31
+    const int half = (warp - HC_EPI_WARP0) >> 2;  // 16-column chunks half, half + 2, ...
     const int row = q * 32 + lane;
     const int g = row >> 3, n_in = row & 7, pp = g / p.G, j = g - pp * p.G;
     const float f = (*p.sa) * (*p.sb) * p.pre_mult;
     float rq_st = 0.0f;
-    if (FR) rq_st = __fdiv_rn(*p.rq.amax_in, Fmt<FR ? FR : 4>::DENOM);
+    float rq_inv = 0.0f;
+    if (FR) {
+      rq_st = __fdiv_rn(*p.rq.amax_in, Fmt<FR ? FR : 4>::DENOM);
+      rq_inv = __frcp_rn(Fmt<FR ? FR : 4>::EMAX * rq_st);
+    }
     uint32_t amax_acc = 0;
     int k = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++k) {
@@ -382,7 +410,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
         const int64_t obase = pos * p.NC * (int64_t)p.N + n;
         const int64_t rq_blk = (pos * p.NG + ng) * p.NCG;
         const uint32_t tb = tmem + s * p.acc_cols + ((uint32_t)(q * 32) << 16);
-        for (int c0 = 0; c0 < p.BN; c0 += 16) {
+        for (int c0 = 16 * half; c0 < p.BN; c0 += 32) {
           uint32_t r[16];
           tmem_ld16(tb + c0, r);
           tmem_wait_ld();
@@ -396,7 +424,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
             for (int jj = 0; jj < 16; ++jj)
               if (co0 + jj < p.NC) o[(int64_t)jj * p.N] = y[jj];
           }
-          if (FR) hc_requant16<FR ? FR : 4>(p, y, rq_blk, n_in, co0, valid, rq_st, amax_acc);
+          if (FR) hc_requant16<FR ? FR : 4>(p, y, rq_blk, n_in, co0, valid, rq_st, rq_inv, amax_acc);
         }
         tc_fence_before();
         mbar_arrive(&ctl->acc_empty[s]);
@@ -407,7 +435,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
 #pragma unroll
       for (int o = 16; o; o >>= 1) amax_acc = max(amax_acc, __shfl_xor_sync(0xFFFFFFFFu, amax_acc, o));
       if (lane == 0 && amax_acc && p.rq.amax_out_bits) atomicMax(p.rq.amax_out_bits, amax_acc);
-      if (blockIdx.x == 0 && row == 0) *p.rq.s_t_out = rq_st;
+      if (blockIdx.x == 0 && row == 0 && half == 0) *p.rq.s_t_out = rq_st;
     }
   }
 
@@ -483,7 +511,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.PS; ++s) {
-      mbar_init(&ctl->pfull[s], 32);
+      mbar_init(&ctl->pfull[s], 64);
       mbar_init(&ctl->pempty[s], HC_DEC_THREADS);
     }
     for (int s = 0; s < DSTAGES; ++s) {
@@ -504,9 +532,9 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
 
   if (warp == HC_TMA_WARP) {
     // ----------------------------------------------------------- producer
-    // all lanes gather the chunk's block scales (zero where the block is out
-    // of range), lane 0 issues the two code boxes; 32 arrivals + the bytes
-    // complete a stage.
+    // lane 0 issues the two code boxes, all lanes copy the chunk's block
+    // scales asynchronously (zero where the block is out of range); 64
+    // arrivals (two per lane) + the box bytes complete a stage.
     int pit = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
@@ -521,29 +549,33 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
         const int hi = ho + T.kh - p.pad;
         uint8_t *stage = smem + p.off_pk + ps * p.pk_stage;
         uint8_t *sc = stage + p.pk_sc_off;
-        for (int i = lane; i < p.na_blocks; i += 32) {      // (p, j, m)
-          const int m = i & 15, pj = i >> 4, pp = pj / p.G, j = pj - pp * p.G;
-          const int wo = wo0 + pp, cog = T.m0 / 8 + m;
-          uint8_t v = 0;
-          if (wo < p.Wo && cog < p.COG)
-            v = __ldg(p.a_scales + (((int64_t)ho * p.Wo + wo) * p.NG + g0 + j) * p.COG + cog);
-          sc[i] = v;
-        }
-        for (int i = lane; i < p.nb_blocks; i += 32) {      // (wc, j, cb)
-          const int cb = i % p.CB, wj = i / p.CB, wc = wj / p.G, j = wj - wc * p.G;
-          const int wi = wo0 - p.pad + wc, cig = T.c0 / 8 + cb;
-          uint8_t v = 0;
-          if ((unsigned)hi < (unsigned)p.H && (unsigned)wi < (unsigned)p.W && cig < p.CIG)
-            v = __ldg(p.b_scales + (((int64_t)hi * p.W + wi) * p.NG + g0 + j) * p.CIG + cig);
-          sc[p.na_blocks + i] = v;
-        }
         if (lane == 0) {
-          mbar_expect_tx(&ctl->pfull[ps], p.pk_bytes);
+          mbar_add_tx(&ctl->pfull[ps], p.pk_bytes);
           tma_load_4d(stage, &tm_a, &ctl->pfull[ps], (T.m0 / 8) * BBA / 8, g0, wo0, ho);
           tma_load_4d(stage + p.pk_b_off, &tm_b, &ctl->pfull[ps], (T.c0 / 8) * BBB / 8, g0, wo0 - p.pad, hi);
-        } else {
-          mbar_arrive(&ctl->pfull[ps]);
         }
+        // dY block scales: run (p, j) = 16 output-channel groups
+        const int mbv = min(16, p.COG - T.m0 / 8);
+        copy_runs_rt(
+            p.gran_a, sc, p.KG, 16, 16,
+            [&](int r) -> const uint8_t * {
+              const int pp = r / p.G, j = r - pp * p.G, wo = wo0 + pp;
+              if (wo >= p.Wo) return nullptr;
+              return p.a_scales + (((int64_t)ho * p.Wo + wo) * p.NG + g0 + j) * p.COG + T.m0 / 8;
+            },
+            [&](int) { return mbv; }, p.a_scales, lane);
+        // X halo block scales: run (wc, j) = CB input-channel groups
+        const int cbv = min(p.CB, p.CIG - T.c0 / 8);
+        copy_runs_rt(
+            p.gran_b, sc + p.na_blocks, p.WP * p.G, p.CB, p.CB,
+            [&](int r) -> const uint8_t * {
+              const int wc = r / p.G, j = r - wc * p.G, wi = wo0 - p.pad + wc;
+              if ((unsigned)hi >= (unsigned)p.H || (unsigned)wi >= (unsigned)p.W) return nullptr;
+              return p.b_scales + (((int64_t)hi * p.W + wi) * p.NG + g0 + j) * p.CIG + T.c0 / 8;
+            },
+            [&](int) { return cbv; }, p.b_scales, lane);
+        cp_async_arrive(&ctl->pfull[ps]);
+        mbar_arrive(&ctl->pfull[ps]);
       }
     }
     if (lane == 0) {
@@ -623,6 +655,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
   } else if (warp >= HC_EPI_WARP0 && warp < HC_EPI_WARP0 + HC_EPI_WARPS) {
     // ------------------------------------------------------------- epilogue
     const int qd = warp & 3;
+    const int half = (warp - HC_EPI_WARP0) >> 2;
     const int row = qd * 32 + lane;
     int k = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++k) {
@@ -633,7 +666,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
       float *orow = p.out + ((int64_t)T.split * p.Cout + co) * p.ncols + (int64_t)T.kh * p.Kw * p.Cin + T.c0;
       for (int kw = 0; kw < p.Kw; ++kw) {
         const uint32_t tb = tmem + kw * p.acc_cols + ((uint32_t)(qd * 32) << 16);
-        for (int c = 0; c < p.BNc; c += 16) {
+        for (int c = 16 * half; c < p.BNc; c += 32) {
           uint32_t r[16];
           tmem_ld16(tb + c, r);
           tmem_wait_ld();
@@ -717,7 +750,9 @@ size_t halo_smem(HaloConv &h, int bba, int bbb) {
   h.pk_bytes = (uint32_t)(h.nh_blocks * bba + h.nb_blocks * bbb);
   h.pk_stage = (uint32_t)((h.pk_b_off + h.nb_blocks * bbb + 127) / 128 * 128);
   h.sc_bytes = (uint32_t)(h.RH * h.WP * h.G * h.CGin);
-  h.sc_stride = (h.sc_bytes + 127) / 128 * 128;
+  h.scw_off = (h.sc_bytes + 15) / 16 * 16;
+  const uint32_t scw = h.op == OP_FWD ? (uint32_t)(taps * h.NB * h.CIG) : (uint32_t)(taps * h.COG * h.NB);
+  h.sc_stride = (h.scw_off + scw + 127) / 128 * 128;
   const size_t fixed = 1024 + (size_t)DSTAGES * h.dec_stage + 2 * h.sc_stride + sizeof(HcCtl) + 128;
   if (fixed + 2 * (size_t)h.pk_stage > SMEM_LIMIT) return 0;
   h.PS = (int)std::min<size_t>(MAX_PS, (SMEM_LIMIT - fixed) / h.pk_stage);
@@ -726,6 +761,13 @@ size_t halo_smem(HaloConv &h, int bba, int bbb) {
   h.off_sc = h.off_pk + h.PS * h.pk_stage;
   h.off_ctl = h.off_sc + 2 * h.sc_stride;
   return 1024 + (size_t)h.off_ctl + sizeof(HcCtl);
+}
+
+// largest power of two dividing x, at most 16 (the cp.async granule)
+int pow2_part(int x) {
+  int g = 1;
+  while (g < 16 && x % (2 * g) == 0) g *= 2;
+  return g;
 }
 
 int pow2_at_least32(int x) {
@@ -792,6 +834,8 @@ bool halo_plan(const ConvParams &cp, HaloConv &h) {
     if (h.BN <= 16) return false;
     h.BN = std::max(16, h.BN / 2 / 16 * 16);
   }
+  h.gran_h = pow2_part(h.G * h.CGin);
+  h.gran_w = h.op == OP_FWD ? pow2_part(h.CIG * std::gcd(h.COG, h.NB)) : pow2_part(std::gcd(h.CIG, h.NB));
   h.tiles_g = h.NG / h.G;
   h.tiles_w = (h.Wout + h.P - 1) / h.P;
   h.tiles_h = (h.Hout + h.R - 1) / h.R;
@@ -948,6 +992,8 @@ bool halo_wgrad_plan(const ConvParams &cp, HaloWgrad &h, int max_splits) {
     h.BNc = std::max(16, h.BNc / 2 / 16 * 16);
   }
   if (h.BNc % 16) return false;
+  h.gran_a = pow2_part(std::gcd(h.COG, 16));
+  h.gran_b = pow2_part(std::gcd(h.CIG, h.CB));
   h.m_tiles = (h.Cout + 127) / 128;
   h.c_tiles = (h.Cin + h.BNc - 1) / h.BNc;
   h.tiles_w = (h.Wo + h.P - 1) / h.P;

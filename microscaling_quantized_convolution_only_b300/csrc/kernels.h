@@ -80,9 +80,10 @@ struct HaloConv {
   // shared-memory carve-up (bytes from the 1 KB-aligned base)
   uint32_t off_dec, dec_stage, dec_b_off;
   uint32_t off_pk, pk_stage, pk_b_off, pk_bytes;
-  uint32_t off_sc, sc_bytes, sc_stride;
+  uint32_t off_sc, sc_bytes, sc_stride, scw_off;   // per-tile scales: halo runs, then weight runs
   uint32_t off_ctl;
   int nh_blocks, nb_blocks;
+  int gran_h, gran_w;            // cp.async granules of the scale runs
   size_t smem;
 };
 
@@ -106,6 +107,7 @@ struct HaloWgrad {
   uint32_t off_pk, pk_stage, pk_b_off, pk_sc_off, pk_bytes;
   uint32_t off_ctl;
   int na_blocks, nb_blocks;
+  int gran_a, gran_b;
   size_t smem;
 };
 
