@@ -8,7 +8,8 @@ Default workload: the chained 4-layer stack (N=256, 56x56, C 128->128, 3x3,
 stride 1, pad 1, bf16 inputs, NVFP4): quantize X0 and W0..W3, forward through
 the four layers with the fused epilogue requantizing Y_l into X_{l+1} (its
 T_scale from the previous step's amax, Hindsight-style), quantize dY3, then
-wgrad + dgrad of layers 3..0 with each dX_l (fp32) requantized into dY_{l-1}.
+wgrad + dgrad of layers 3..0, the dgrad epilogue requantizing dX_l straight
+into dY_{l-1} the same way (layer 0 writes fp32 dX).
 
 value = algorithmic conv TFLOP/s of the whole step (quantization included in
 the step time); per-op throughputs, the quantizer's GB/s and the roofline of
@@ -188,6 +189,8 @@ class StackStep:
         self.amax = torch.zeros(16, dtype=torch.float32, device=device)        # exact-mode amax outputs
         self.y_stat = torch.ones(nl, dtype=torch.float32, device=device)       # hindsight statistics of Y_l
         self.y_amax = torch.zeros(nl, dtype=torch.float32, device=device)
+        self.dx_stat = torch.ones(nl, dtype=torch.float32, device=device)      # ... and of dX_l (l > 0)
+        self.dx_amax = torch.zeros(nl, dtype=torch.float32, device=device)
         self.nl = nl
         # accounting
         n_el = int(np.prod(L.x_shape()))
@@ -196,15 +199,17 @@ class StackStep:
         in_b = 2 if wl.dtype == "bf16" else 4
         self.qbytes = {   # algorithmic bytes: one read of the input + the packed output
             "quant_bf16": 2 * (n_el * in_b + packed_bytes(fmt, n_el)) + nl * (w_el * in_b + packed_bytes(fmt, w_el)),
-            "quant_f32": (nl - 1) * (n_el * 4 + packed_bytes(fmt, n_el)),
         }
         self.conv_bytes = {
             "fwd": (nl - 1) * (2 * packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el)) +
                    (packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el) + 4 * n_el),
-            "dgrad": nl * (packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el) + 4 * n_el),
+            "dgrad": (nl - 1) * (2 * packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el)) +
+                     (packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el) + 4 * n_el),
             "wgrad": nl * (2 * packed_bytes(fmt, n_el) + 4 * w_el),
         }
-        self.launches_per_step = (2 + 2 * nl) + nl + 2 + 2 * nl + nl + 2 * (nl - 1)
+        # amax + quantize of X0 and each W, fwd per layer, amax + quantize of dY,
+        # wgrad + split-K reduction and dgrad per layer
+        self.launches_per_step = (2 + 2 * nl) + nl + 2 + 2 * nl + nl
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in [self.h_x0, self.h_dy] + self.h_w)
         self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.dw)
 
@@ -237,14 +242,15 @@ class StackStep:
             mq.wgrad(L, self.gq[l], self.xq[l], self.dw[l], self.ws)
             tm.end()
             tm.begin("dgrad")
-            mq.dgrad(L, self.wq[l], self.gq[l], self.dx)
+            if l > 0:   # fused requantization of dX_l into dY_{l-1}
+                mq.dgrad(L, self.wq[l], self.gq[l], None, rq_out=self.gq[l - 1], rq_amax_in=self.dx_stat[l:l + 1],
+                         rq_amax_out=self.dx_amax[l:l + 1])
+            else:
+                mq.dgrad(L, self.wq[l], self.gq[l], self.dx)
             tm.end()
-            if l > 0:
-                tm.begin("quant")
-                mq.quantize_cbf(self.dx, "hwcn", self.gq[l - 1], amax_out=self.amax[9 + l:10 + l])
-                tm.end()
         # hindsight: next step's statistics are this step's measured amax
         self.y_stat.copy_(self.y_amax)
+        self.dx_stat.copy_(self.dx_amax)
 
     def upload(self, pinned):
         """e2e: host -> device copies of the step's inputs."""

@@ -25,9 +25,9 @@
  * Packed tensor layout (mq_packed)
  *   Activations (role ACT) and gradients (role GRAD) with dims (N, C, H, W):
  *     blocks ordered [H][W][N/8][C/8]; inside a block element i = 8*n + c
- *     (channel fastest) -- "each spatial location (h, w) contains a contiguous
- *     block of all channels across all batch elements", values consecutive
- *     along C_in (MicroQonv §IV-A, Fig. 3).
+ *     (channel fastest).  So every spatial position holds one contiguous run
+ *     covering all its channels and all batch elements, the channel-batch-first
+ *     storage of MicroQonv §IV-A, Fig. 3.
  *   Weights (role WEIGHT) with dims (Cout, Cin, Kh, Kw):
  *     blocks ordered [Kh][Kw][Cout/8][Cin/8]; element i = 8*co + ci (§IV-B:
  *     weights quantized along C_in and C_out).
@@ -143,8 +143,8 @@ mq_status mqconv_fwd(const mq_conv_desc *desc, const mq_packed *xq, const mq_pac
 
 /*
  * Data gradient: G_X = col2im(W_f^T * G_Y) computed directly as the adjoint
- * convolution ("convolving the output gradient with transposed kernels",
- * paperlayer summary §II-A "Backward Pass"; MicroQonv §IV-A:
+ * convolution, i.e. G_Y correlated with the spatially flipped, channel-
+ * transposed kernels (paperlayer summary §II-A "Backward Pass"; MicroQonv §IV-A:
  * G_X'_{Cin,N} = W^T_{fCout,Cin} . G_Y_{fCout,N}).
  *   wq   packed weights, role WEIGHT, dims (Cout, Cin, Kh, Kw).
  *   dyq  packed output gradient, role GRAD, dims (N, Cout, Ho, Wo).
@@ -152,6 +152,21 @@ mq_status mqconv_fwd(const mq_conv_desc *desc, const mq_packed *xq, const mq_pac
  */
 mq_status mqconv_dgrad(const mq_conv_desc *desc, const mq_packed *wq, const mq_packed *dyq, float *dx,
                        mq_stream stream);
+
+/*
+ * Data gradient with the fused requantizing epilogue: dX goes from the
+ * accumulators straight into packed blocks of role GRAD, dims (N, Cin, H, W)
+ * -- the output gradient G_Y of the layer below, quantized once (MicroQonv
+ * §IV-B: gradients in (N, C) square blocks) -- without an fp32 round trip
+ * through device memory.  As for the forward epilogue (mq_requant), T_scale
+ * comes from the caller's statistic rq->amax_in (e.g. the previous step's
+ * amax of dX) and the true amax is written to rq->amax_out.
+ *   wq, dyq  as for mqconv_dgrad.
+ *   dx       device fp32 [H][W][Cin][N], or NULL (only the packed result).
+ *   rq       required; rq->out has role MQ_ROLE_GRAD.
+ */
+mq_status mqconv_dgrad_requant(const mq_conv_desc *desc, const mq_packed *wq, const mq_packed *dyq, float *dx,
+                               const mq_requant *rq, mq_stream stream);
 
 /*
  * Weight gradient: G_W = G_Y * X'^T (MicroQonv §IV-A: G_W_{fCout,Cin} =

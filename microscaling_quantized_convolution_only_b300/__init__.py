@@ -4,8 +4,9 @@ Argument marshalling only: every step of quantization and convolution runs in
 the library's CUDA kernels.  PyTorch supplies device memory and streams.  There
 is no fallback: if libmqconv.so is missing or a call fails, this module raises.
 
-Entry points mirror the C names: quantize_cbf, fwd, dgrad, wgrad,
-wgrad_workspace_bytes, packed_code_bytes, packed_scale_bytes, device_status.
+Entry points mirror the C names: quantize_cbf, fwd, dgrad (and, with rq_out,
+dgrad_requant), wgrad, wgrad_noalloc, wgrad_workspace_bytes,
+packed_code_bytes, packed_scale_bytes, device_status.
 """
 from __future__ import annotations
 
@@ -66,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.mqconv_fwd.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P,
                                  ctypes.POINTER(_Requant), P]
         L.mqconv_dgrad.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P, P]
+        L.mqconv_dgrad_requant.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed),
+                                           P, ctypes.POINTER(_Requant), P]
         L.mqconv_wgrad_workspace_bytes.argtypes = [ctypes.POINTER(_Desc)]
         L.mqconv_wgrad_workspace_bytes.restype = ctypes.c_size_t
         L.mqconv_wgrad.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P, P,
@@ -73,8 +76,8 @@ def lib() -> ctypes.CDLL:
         L.mqconv_device_status.argtypes = [P, ctypes.POINTER(i32)]
         L.mqconv_wgrad_noalloc.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P,
                                            P]
-        for f in ("mqconv_quantize_cbf", "mqconv_fwd", "mqconv_dgrad", "mqconv_wgrad", "mqconv_device_status",
-                  "mqconv_wgrad_noalloc"):
+        for f in ("mqconv_quantize_cbf", "mqconv_fwd", "mqconv_dgrad", "mqconv_dgrad_requant", "mqconv_wgrad",
+                  "mqconv_device_status", "mqconv_wgrad_noalloc"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -164,11 +167,20 @@ def fwd(layer, xq: Packed, wq: Packed, y: Optional[torch.Tensor], rq_out: Option
     _check(rc, "mqconv_fwd")
 
 
-def dgrad(layer, wq: Packed, dyq: Packed, dx: torch.Tensor, stream=None) -> None:
-    """mqconv_dgrad: dX (fp32, [H][W][Cin][N])."""
+def dgrad(layer, wq: Packed, dyq: Packed, dx: Optional[torch.Tensor], rq_out: Optional[Packed] = None,
+          rq_amax_in: Optional[torch.Tensor] = None, rq_amax_out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """mqconv_dgrad: dX (fp32, [H][W][Cin][N]); with rq_out, mqconv_dgrad_requant: dX (optional) and its
+    fused requantization into rq_out (role grad, dims (N, Cin, H, W))."""
     d, w, g = desc(layer), wq.c(), dyq.c()
-    rc = lib().mqconv_dgrad(ctypes.byref(d), ctypes.byref(w), ctypes.byref(g), _ptr(dx), _stream(stream))
-    _check(rc, "mqconv_dgrad")
+    if rq_out is None:
+        rc = lib().mqconv_dgrad(ctypes.byref(d), ctypes.byref(w), ctypes.byref(g), _ptr(dx), _stream(stream))
+        _check(rc, "mqconv_dgrad")
+        return
+    out_c = rq_out.c()
+    rq = _Requant(FMT[rq_out.fmt], _ptr(rq_amax_in), ctypes.pointer(out_c), _ptr(rq_amax_out))
+    rc = lib().mqconv_dgrad_requant(ctypes.byref(d), ctypes.byref(w), ctypes.byref(g), _ptr(dx), ctypes.byref(rq),
+                                    _stream(stream))
+    _check(rc, "mqconv_dgrad_requant")
 
 
 def wgrad_workspace_bytes(layer) -> int:

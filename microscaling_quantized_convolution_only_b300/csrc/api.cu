@@ -189,6 +189,52 @@ mq_status scratch_addr(float **out) {
   return MQ_OK;
 }
 
+// Forward (a = Xq) or data gradient (a = dYq) with optional fused
+// requantization of the fp32 result into packed blocks.
+mq_status conv_fwd_or_dgrad(int op, const mq_conv_desc *desc, const mq_packed *a, const mq_packed *wq, float *out,
+                            const mq_requant *rq, mq_stream stream) {
+  mq_status st = check_desc(desc);
+  if (st != MQ_OK) return st;
+  const int64_t Ho = out_dim(desc->H, desc->Kh, desc->stride, desc->pad);
+  const int64_t Wo = out_dim(desc->W, desc->Kw, desc->stride, desc->pad);
+  const bool fwd = op == mq::OP_FWD;
+  if (fwd) {
+    if ((st = check_packed(a, MQ_ROLE_ACT, desc->N, desc->Cin, desc->H, desc->W)) != MQ_OK) return st;
+  } else {
+    if ((st = check_packed(a, MQ_ROLE_GRAD, desc->N, desc->Cout, Ho, Wo)) != MQ_OK) return st;
+  }
+  if ((st = check_packed(wq, MQ_ROLE_WEIGHT, desc->Cout, desc->Cin, desc->Kh, desc->Kw)) != MQ_OK) return st;
+  if (!out && !rq) return MQ_ERR_INVALID_ARG;
+  if (out && !aligned16(out)) return MQ_ERR_ALIGNMENT;
+  if (rq) {
+    if (!rq->amax_in || !fmt_ok(rq->fmt) || !rq->out || rq->out->fmt != rq->fmt) return MQ_ERR_INVALID_ARG;
+    st = fwd ? check_packed(rq->out, MQ_ROLE_ACT, desc->N, desc->Cout, Ho, Wo)
+             : check_packed(rq->out, MQ_ROLE_GRAD, desc->N, desc->Cin, desc->H, desc->W);
+    if (st != MQ_OK) return st;
+    if ((reinterpret_cast<uintptr_t>(rq->amax_in) & 3u) ||
+        (rq->amax_out && (reinterpret_cast<uintptr_t>(rq->amax_out) & 3u)))
+      return MQ_ERR_ALIGNMENT;
+  }
+  DevInfo *di = nullptr;
+  if ((st = dev_info(&di)) != MQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mq::ConvParams p = base_params(desc, op, di->status);
+  p.a = operand(a);
+  p.b = operand(wq);
+  p.pre_mult = pre_mult(a->fmt, wq->fmt);
+  p.out = out;
+  if (rq) {
+    p.rq.codes = static_cast<uint8_t *>(rq->out->codes);
+    p.rq.scales = rq->out->scales;
+    p.rq.s_t_out = rq->out->s_t;
+    p.rq.amax_in = rq->amax_in;
+    p.rq.amax_out_bits = reinterpret_cast<uint32_t *>(rq->amax_out);
+    p.rq.fmt = rq->fmt;
+    if (rq->amax_out && cudaMemsetAsync(rq->amax_out, 0, sizeof(float), s) != cudaSuccess) return MQ_ERR_CUDA;
+  }
+  return run_conv(p, di->num_sms, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -271,58 +317,19 @@ mq_status mqconv_quantize_cbf(const void *src, int32_t dtype, int32_t layout, co
 
 mq_status mqconv_fwd(const mq_conv_desc *desc, const mq_packed *xq, const mq_packed *wq, float *y,
                      const mq_requant *rq, mq_stream stream) {
-  mq_status st = check_desc(desc);
-  if (st != MQ_OK) return st;
-  const int64_t Ho = out_dim(desc->H, desc->Kh, desc->stride, desc->pad);
-  const int64_t Wo = out_dim(desc->W, desc->Kw, desc->stride, desc->pad);
-  if ((st = check_packed(xq, MQ_ROLE_ACT, desc->N, desc->Cin, desc->H, desc->W)) != MQ_OK) return st;
-  if ((st = check_packed(wq, MQ_ROLE_WEIGHT, desc->Cout, desc->Cin, desc->Kh, desc->Kw)) != MQ_OK) return st;
-  if (!y && !rq) return MQ_ERR_INVALID_ARG;
-  if (y && !aligned16(y)) return MQ_ERR_ALIGNMENT;
-  if (rq) {
-    if (!rq->amax_in || !fmt_ok(rq->fmt) || !rq->out || rq->out->fmt != rq->fmt) return MQ_ERR_INVALID_ARG;
-    if ((st = check_packed(rq->out, MQ_ROLE_ACT, desc->N, desc->Cout, Ho, Wo)) != MQ_OK) return st;
-    if ((reinterpret_cast<uintptr_t>(rq->amax_in) & 3u) || (rq->amax_out && (reinterpret_cast<uintptr_t>(rq->amax_out) & 3u)))
-      return MQ_ERR_ALIGNMENT;
-  }
-  DevInfo *di = nullptr;
-  if ((st = dev_info(&di)) != MQ_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  mq::ConvParams p = base_params(desc, mq::OP_FWD, di->status);
-  p.a = operand(xq);
-  p.b = operand(wq);
-  p.pre_mult = pre_mult(xq->fmt, wq->fmt);
-  p.out = y;
-  if (rq) {
-    p.rq.codes = static_cast<uint8_t *>(rq->out->codes);
-    p.rq.scales = rq->out->scales;
-    p.rq.s_t_out = rq->out->s_t;
-    p.rq.amax_in = rq->amax_in;
-    p.rq.amax_out_bits = reinterpret_cast<uint32_t *>(rq->amax_out);
-    p.rq.fmt = rq->fmt;
-    if (rq->amax_out && cudaMemsetAsync(rq->amax_out, 0, sizeof(float), s) != cudaSuccess) return MQ_ERR_CUDA;
-  }
-  return run_conv(p, di->num_sms, s);
+  return conv_fwd_or_dgrad(mq::OP_FWD, desc, xq, wq, y, rq, stream);
 }
 
 mq_status mqconv_dgrad(const mq_conv_desc *desc, const mq_packed *wq, const mq_packed *dyq, float *dx,
                        mq_stream stream) {
-  mq_status st = check_desc(desc);
-  if (st != MQ_OK) return st;
-  const int64_t Ho = out_dim(desc->H, desc->Kh, desc->stride, desc->pad);
-  const int64_t Wo = out_dim(desc->W, desc->Kw, desc->stride, desc->pad);
-  if ((st = check_packed(wq, MQ_ROLE_WEIGHT, desc->Cout, desc->Cin, desc->Kh, desc->Kw)) != MQ_OK) return st;
-  if ((st = check_packed(dyq, MQ_ROLE_GRAD, desc->N, desc->Cout, Ho, Wo)) != MQ_OK) return st;
   if (!dx) return MQ_ERR_INVALID_ARG;
-  if (!aligned16(dx)) return MQ_ERR_ALIGNMENT;
-  DevInfo *di = nullptr;
-  if ((st = dev_info(&di)) != MQ_OK) return st;
-  mq::ConvParams p = base_params(desc, mq::OP_DGRAD, di->status);
-  p.a = operand(dyq);
-  p.b = operand(wq);
-  p.pre_mult = pre_mult(dyq->fmt, wq->fmt);
-  p.out = dx;
-  return run_conv(p, di->num_sms, reinterpret_cast<cudaStream_t>(stream));
+  return conv_fwd_or_dgrad(mq::OP_DGRAD, desc, dyq, wq, dx, nullptr, stream);
+}
+
+mq_status mqconv_dgrad_requant(const mq_conv_desc *desc, const mq_packed *wq, const mq_packed *dyq, float *dx,
+                               const mq_requant *rq, mq_stream stream) {
+  if (!rq) return MQ_ERR_INVALID_ARG;
+  return conv_fwd_or_dgrad(mq::OP_DGRAD, desc, dyq, wq, dx, rq, stream);
 }
 
 size_t mqconv_wgrad_workspace_bytes(const mq_conv_desc *desc) {

@@ -155,6 +155,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `sleep_ns` inside the
+// instruction; it wakes as soon as the phase completes.  Long hints keep
+// waiting warps from re-polling shared memory.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t sleep_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(sleep_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; gives up after
 // `limit_ns` of wall time, sets ST_TIMEOUT in *status and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status,
@@ -354,6 +367,56 @@ __device__ __forceinline__ void copy_runs_rt(int gran, uint8_t *dst, int nruns, 
     case 4: copy_runs<4>(dst, nruns, stride, fill, src, len, safe, lane); break;
     case 2: copy_runs<2>(dst, nruns, stride, fill, src, len, safe, lane); break;
     default: copy_runs<1>(dst, nruns, stride, fill, src, len, safe, lane); break;
+  }
+}
+
+}  // namespace mq
+
+namespace mq {
+
+// Codes of eight fp32 values (one block row) for block scale value bs and
+// T_scale s_t: exact RN of the real quotient x / (bs * s_t) with the bracket
+// and fma-sign tie test of resolve_tie.  Returns the packed row: element j at
+// bits 4j (E2M1), 6j (E2M3) or 8j (E4M3).
+template <int F> __device__ __forceinline__ uint64_t encode_row8(const float (&v)[8], float bs, float s_t) {
+  float inv_lo = 0.0f, inv_hi = 0.0f;
+  if (bs > 0.0f) {
+    const float inv = __frcp_rn(bs * s_t);
+    inv_lo = inv * (1.0f - QEPS);
+    inv_hi = inv * (1.0f + QEPS);
+  }
+  constexpr uint32_t cmask = F == 4 ? 0xFu : 0xFFu;
+  constexpr int sh = F == 4 ? 4 : 8;
+  uint64_t bits = 0;
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const uint32_t lo = cvt2<F>(v[2 * jj] * inv_lo, v[2 * jj + 1] * inv_lo);
+    const uint32_t hi = cvt2<F>(v[2 * jj] * inv_hi, v[2 * jj + 1] * inv_hi);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t cl = (lo >> (e * sh)) & cmask, ch = (hi >> (e * sh)) & cmask;
+      uint32_t cc = cl;
+      if (cl != ch) {
+        const float x = v[2 * jj + e];
+        cc = resolve_tie<F>(fabsf(x), bs, s_t, cl & Fmt<F>::MAG, ch & Fmt<F>::MAG) | (signbit(x) ? Fmt<F>::SBIT : 0u);
+      }
+      bits |= (uint64_t)cc << ((2 * jj + e) * (F == 4 ? 4 : F == 6 ? 6 : 8));
+    }
+  }
+  return bits;
+}
+
+// store one packed row (8 codes) at byte offset 4r / 6r / 8r of its block
+template <int F> __device__ __forceinline__ void store_row8(uint8_t *blk, int r, uint64_t bits) {
+  if (F == 4) {
+    reinterpret_cast<uint32_t *>(blk)[r] = (uint32_t)bits;
+  } else if (F == 6) {
+    uint16_t *d16 = reinterpret_cast<uint16_t *>(blk + 6 * r);
+    d16[0] = (uint16_t)bits;
+    d16[1] = (uint16_t)(bits >> 16);
+    d16[2] = (uint16_t)(bits >> 32);
+  } else {
+    reinterpret_cast<uint64_t *>(blk)[r] = bits;
   }
 }
 

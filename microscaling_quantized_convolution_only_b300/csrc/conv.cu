@@ -222,46 +222,14 @@ __device__ __forceinline__ int64_t b_blk(const ConvParams &p, const Tile &T, con
 }
 
 // ------------------------------------------------------- requant epilogue
-// Eight fp32 values of one block row -> eight codes (exact RN, see quantize.cu).
-template <int F>
-__device__ __forceinline__ uint64_t encode_row8(const float (&y)[8], float bs, float s_t) {
-  float inv_lo = 0.0f, inv_hi = 0.0f;
-  if (bs > 0.0f) {
-    const float inv = __frcp_rn(bs * s_t);
-    inv_lo = inv * (1.0f - QEPS);
-    inv_hi = inv * (1.0f + QEPS);
-  }
-  constexpr uint32_t cmask = F == 4 ? 0xFu : 0xFFu;
-  constexpr int sh = F == 4 ? 4 : 8;
-  uint32_t c[8];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t lo = cvt2<F>(y[2 * j] * inv_lo, y[2 * j + 1] * inv_lo);
-    const uint32_t hi = cvt2<F>(y[2 * j] * inv_hi, y[2 * j + 1] * inv_hi);
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const uint32_t cl = (lo >> (e * sh)) & cmask, ch = (hi >> (e * sh)) & cmask;
-      c[2 * j + e] = cl;
-      if (cl != ch) {
-        const float v = y[2 * j + e];
-        c[2 * j + e] = resolve_tie<F>(fabsf(v), bs, s_t, cl & Fmt<F>::MAG, ch & Fmt<F>::MAG) |
-                       (signbit(v) ? Fmt<F>::SBIT : 0u);
-      }
-    }
-  }
-  uint64_t r = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) r |= (uint64_t)c[j] << (j * (F == 4 ? 4 : F == 6 ? 6 : 8));
-  return r;
-}
-
 // Requantize one 16-column chunk of a row (thread = one (position, n) row of
-// the tile) into two blocks of the next layer's activations.  Lanes 8q..8q+7
-// of a warp hold the eight batch rows of one block: the block amax is their
-// shuffle-max.
+// the tile) into two blocks of the packed output (the next layer's
+// activations for the forward pass, the lower layer's output gradient for the
+// data gradient; nc channels, ncg = nc / 8 groups).  Lanes 8q..8q+7 of a warp
+// hold the eight batch rows of one block: the block amax is their shuffle-max.
 template <int F>
 __device__ __forceinline__ void requant_chunk(const ConvParams &p, const float (&y)[16], int pos, int ng, int n_in,
-                                              int co0, bool row_ok, float s_t, uint32_t &amax_acc) {
+                                              int co0, bool row_ok, float s_t, int nc, int ncg, uint32_t &amax_acc) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int co = co0 + 8 * h;
@@ -276,11 +244,11 @@ __device__ __forceinline__ void requant_chunk(const ConvParams &p, const float (
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     amax_acc = max(amax_acc, m);
-    if (!row_ok || co >= p.Cout) continue;
+    if (!row_ok || co >= nc) continue;
     const uint32_t bsc = block_scale_code<F>(__uint_as_float(m), s_t);
     const float bs = code_value<8>(bsc);
     const uint64_t bits = encode_row8<F>(v, bs, s_t);
-    const int64_t blk = ((int64_t)pos * p.NG + ng) * p.COG + co / 8;   // next layer: C = Cout
+    const int64_t blk = ((int64_t)pos * p.NG + ng) * ncg + co / 8;
     uint8_t *dst = p.rq.codes + blk * Fmt<F>::BLOCK_BYTES;
     if (F == 4) {
       reinterpret_cast<uint32_t *>(dst)[n_in] = (uint32_t)bits;
@@ -491,7 +459,8 @@ __global__ void __launch_bounds__(CONV_THREADS, 1) conv_kernel(const ConvParams 
           ng = rg - pp * p.NG;
           const int a = pp / T.ph.Wp, b = pp - a * T.ph.Wp;
           const int hi = T.ph.phh + p.stride * a, wi = T.ph.phw + p.stride * b;
-          obase = ((int64_t)(hi * p.W + wi) * p.Cin) * p.N + ng * 8 + n_in;
+          pos = hi * p.W + wi;
+          obase = ((int64_t)pos * p.Cin) * p.N + ng * 8 + n_in;
         }
       } else {
         const int co = T.m * 128 + row;
@@ -529,13 +498,16 @@ __global__ void __launch_bounds__(CONV_THREADS, 1) conv_kernel(const ConvParams 
             for (int j = 0; j < 16; ++j)
               if (col0 + c0 + j < ncol_valid) p.out[obase + (int64_t)(col0 + c0 + j) * p.N] = y[j];
           }
-          if (FR && OP == OP_FWD) requant_chunk<FR ? FR : 4>(p, y, pos, ng, n_in, col0 + c0, obase >= 0, rq_st, amax_acc);
+          if (FR) {
+            const int nc = OP == OP_FWD ? p.Cout : p.Cin;
+            requant_chunk<FR ? FR : 4>(p, y, pos, ng, n_in, col0 + c0, obase >= 0, rq_st, nc, nc / 8, amax_acc);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&ctl->acc_empty[buf]);
     }
-    if (FR && OP == OP_FWD) {
+    if (FR && OP != OP_WGRAD) {
 #pragma unroll
       for (int o = 16; o; o >>= 1) amax_acc = max(amax_acc, __shfl_xor_sync(0xFFFFFFFFu, amax_acc, o));
       if (lane == 0 && amax_acc && p.rq.amax_out_bits) atomicMax(p.rq.amax_out_bits, amax_acc);
@@ -658,7 +630,16 @@ cudaError_t launch_conv(const ConvParams &p, int num_sms, cudaStream_t s) {
     }
     return dispatch_a<OP_FWD, 0>(p, grid, smem, s);
   }
-  if (p.op == OP_DGRAD) return dispatch_a<OP_DGRAD, 0>(p, grid, smem, s);
+  if (p.op == OP_DGRAD) {
+    if (p.rq.codes) {
+      switch (p.rq.fmt) {
+        case 4: return dispatch_a<OP_DGRAD, 4>(p, grid, smem, s);
+        case 6: return dispatch_a<OP_DGRAD, 6>(p, grid, smem, s);
+        default: return dispatch_a<OP_DGRAD, 8>(p, grid, smem, s);
+      }
+    }
+    return dispatch_a<OP_DGRAD, 0>(p, grid, smem, s);
+  }
   return dispatch_a<OP_WGRAD, 0>(p, grid, smem, s);
 }
 

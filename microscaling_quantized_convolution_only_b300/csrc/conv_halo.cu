@@ -21,10 +21,9 @@
 //
 // GEMM per tile: rows = (output row s, position p, batch group j, n), columns
 // = output channels (BN), K = (chunk, tap, 16 channels).  One accumulator of
-// 128 x BN fp32 per output row s lives in TMEM (R x BN <= 512 columns); the
-// epilogue of row s of one tile overlaps the MMAs of rows s+1.. and the next
-// tile, because the MMA warp waits for accumulator s only before its own
-// first MMA into it.
+// 128 x BN fp32 per output row s lives in TMEM, in two sets (2 R BN <= 512
+// columns) used by alternate tiles, so the epilogue of one tile overlaps the
+// MMAs of the next.
 //
 // Warp roles: warps 0-7 decode, warps 8-15 drain the accumulators
 // (tcgen05.ld; warps w and w+4 share TMEM lane quadrant w % 4 and take
@@ -74,8 +73,8 @@ __device__ __forceinline__ bool hc_wait(uint64_t *bar, uint32_t parity, const Ha
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if ((it & 7u) == 7u) {
       if (ctl->abort_flag) return false;
       if (globaltimer_ns() - t0 > 2000000000ull) {
         atomicOr(p.status, ST_TIMEOUT);
@@ -193,19 +192,19 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.PS; ++s) {
       mbar_init(&ctl->pfull[s], 1);
-      mbar_init(&ctl->pempty[s], HC_DEC_THREADS);
+      mbar_init(&ctl->pempty[s], HC_DEC_WARPS);
     }
     for (int s = 0; s < DSTAGES; ++s) {
-      mbar_init(&ctl->dfull[s], HC_DEC_THREADS);
+      mbar_init(&ctl->dfull[s], HC_DEC_WARPS);
       mbar_init(&ctl->dempty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl->sfull[s], 64);
-      mbar_init(&ctl->sempty[s], HC_DEC_THREADS);
+      mbar_init(&ctl->sempty[s], HC_DEC_WARPS);
     }
-    for (int s = 0; s < p.R; ++s) {
+    for (int s = 0; s < p.R * p.nbuf; ++s) {
       mbar_init(&ctl->acc_full[s], 1);
-      mbar_init(&ctl->acc_empty[s], HC_EPI_WARPS * 32);
+      mbar_init(&ctl->acc_empty[s], HC_EPI_WARPS);
     }
     mbar_init(&ctl->done, 1);
     ctl->abort_flag = 0;
@@ -333,17 +332,32 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
           *reinterpret_cast<uint4 *>(decb + i * 16) = v;
         }
         fence_async_smem();
-        mbar_arrive(&ctl->pempty[ps]);
-        mbar_arrive(&ctl->dfull[ds]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&ctl->pempty[ps]);
+          mbar_arrive(&ctl->dfull[ds]);
+        }
       }
-      if (ok) mbar_arrive(&ctl->sempty[tb]);
+      if (ok) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->sempty[tb]);
+      }
     }
   } else if (warp == HC_MMA_WARP) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, p.BN, false, OP == OP_DGRAD);
-      const uint32_t halo_row = (uint32_t)(p.WP * p.G * CGC * 128);   // bytes per halo row
-      const uint32_t halo_col = (uint32_t)(p.G * CGC * 128);          // bytes per halo position
+      // Descriptors are built once and stepped: the start-address field is
+      // bits 0-13 of (address >> 4), so moving an operand by `bytes` adds
+      // bytes >> 4 to the descriptor (addresses stay below 256 KB).
+      const uint64_t d_row = (uint64_t)((p.WP * p.G * CGC * 128) >> 4);   // one halo row
+      const uint64_t d_col = (uint64_t)((p.G * CGC * 128) >> 4);          // one halo position
+      const uint64_t d_tap = (uint64_t)((p.NB * CGC * 128) >> 4);         // one weight tap
+      const uint64_t d_stage = (uint64_t)(p.dec_stage >> 4);
+      const uint64_t a_base = sdesc(smem_u32(smem + p.off_dec), 128, CGC * 128);
+      const uint64_t b_base = OP == OP_FWD ? sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), 128, CGC * 128)
+                                           : sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), p.NB * 128, 128);
+      const int taps = p.Kh * p.Kw;
       int dit = 0, k = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
@@ -351,33 +365,32 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
           const int ds = dit % DSTAGES;
           if (!hc_wait(&ctl->dfull[ds], (dit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + p.off_dec + ds * p.dec_stage);
-          const uint32_t b0 = a0 + p.dec_b_off;
+          const uint64_t a_stage = a_base + ds * d_stage;
+          // dgrad walks the weight taps mirrored: W tap (Kh-1-u, Kw-1-v) = taps-1-(u*Kw+v)
+          const uint64_t b_first = b_base + ds * d_stage + (OP == OP_FWD ? 0 : (uint64_t)(taps - 1) * d_tap);
+          const int buf = k % p.nbuf, use = k / p.nbuf;
           for (int s = 0; s < p.R && ok; ++s) {
+            const int slot = buf * p.R + s;
             if (c == 0) {
-              if (!hc_wait(&ctl->acc_empty[s], (k & 1) ^ 1, p, ctl)) { ok = false; break; }
+              if (!hc_wait(&ctl->acc_empty[slot], (use & 1) ^ 1, p, ctl)) { ok = false; break; }
               tc_fence_after();
             }
-            const uint32_t d = tmem + s * p.acc_cols;
-            for (int u = 0; u < p.Kh; ++u) {
-              for (int v = 0; v < p.Kw; ++v) {
-                const uint64_t ad = sdesc(a0 + (s + u) * halo_row + v * halo_col, 128, CGC * 128);
-                uint64_t bd;
-                if (OP == OP_FWD) {
-                  bd = sdesc(b0 + (u * p.Kw + v) * (p.NB * CGC * 128), 128, CGC * 128);
-                } else {
-                  const int tw = (p.Kh - 1 - u) * p.Kw + (p.Kw - 1 - v);
-                  bd = sdesc(b0 + tw * (p.NB * CGC * 128), p.NB * 128, 128);
-                }
-                umma_f16(d, ad, bd, idesc, (c | u | v) ? 1u : 0u);
+            const uint32_t d = tmem + slot * p.acc_cols;
+            uint64_t a_u = a_stage + s * d_row, bd = b_first;
+            uint32_t acc = c > 0 ? 1u : 0u;
+            for (int u = 0; u < p.Kh; ++u, a_u += d_row) {
+              uint64_t ad = a_u;
+              for (int v = 0; v < p.Kw; ++v, ad += d_col) {
+                umma_f16(d, ad, bd, idesc, acc);
+                acc = 1u;
+                if (OP == OP_FWD) bd += d_tap; else bd -= d_tap;
               }
             }
-            if (c == p.nchunks - 1) umma_commit(&ctl->acc_full[s]);
+            if (c == p.nchunks - 1) umma_commit(&ctl->acc_full[slot]);
           }
           umma_commit(&ctl->dempty[ds]);
         }
       }
-      (void)taps;
       umma_commit(&ctl->done);
       hc_wait(&ctl->done, 0, p, ctl);
     }
@@ -401,15 +414,17 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
       const TileCoord tc = hc_tile(p, t);
       const int wo = tc.w0 + pp, ng = tc.g0 + j, n = ng * 8 + n_in;
       bool stop = false;
+      const int buf = k % p.nbuf, use = k / p.nbuf;
       for (int s = 0; s < p.R; ++s) {
-        if (!hc_wait(&ctl->acc_full[s], k & 1, p, ctl)) { stop = true; break; }
+        const int slot = buf * p.R + s;
+        if (!hc_wait(&ctl->acc_full[slot], use & 1, p, ctl)) { stop = true; break; }
         tc_fence_after();
         const int ho = tc.h0 + s;
         const bool valid = ho < p.Hout && wo < p.Wout;
         const int64_t pos = (int64_t)ho * p.Wout + wo;
         const int64_t obase = pos * p.NC * (int64_t)p.N + n;
         const int64_t rq_blk = (pos * p.NG + ng) * p.NCG;
-        const uint32_t tb = tmem + s * p.acc_cols + ((uint32_t)(q * 32) << 16);
+        const uint32_t tb = tmem + slot * p.acc_cols + ((uint32_t)(q * 32) << 16);
         for (int c0 = 16 * half; c0 < p.BN; c0 += 32) {
           uint32_t r[16];
           tmem_ld16(tb + c0, r);
@@ -427,7 +442,8 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
           if (FR) hc_requant16<FR ? FR : 4>(p, y, rq_blk, n_in, co0, valid, rq_st, rq_inv, amax_acc);
         }
         tc_fence_before();
-        mbar_arrive(&ctl->acc_empty[s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->acc_empty[slot]);
       }
       if (stop) break;
     }
@@ -487,8 +503,8 @@ __device__ __forceinline__ bool wg_wait(uint64_t *bar, uint32_t parity, const Ha
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if ((it & 7u) == 7u) {
       if (ctl->abort_flag) return false;
       if (globaltimer_ns() - t0 > 2000000000ull) {
         atomicOr(p.status, ST_TIMEOUT);
@@ -512,14 +528,14 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.PS; ++s) {
       mbar_init(&ctl->pfull[s], 64);
-      mbar_init(&ctl->pempty[s], HC_DEC_THREADS);
+      mbar_init(&ctl->pempty[s], HC_DEC_WARPS);
     }
     for (int s = 0; s < DSTAGES; ++s) {
-      mbar_init(&ctl->dfull[s], HC_DEC_THREADS);
+      mbar_init(&ctl->dfull[s], HC_DEC_WARPS);
       mbar_init(&ctl->dempty[s], 1);
     }
     mbar_init(&ctl->acc_full, 1);
-    mbar_init(&ctl->acc_empty, HC_EPI_WARPS * 32);
+    mbar_init(&ctl->acc_empty, HC_EPI_WARPS);
     mbar_init(&ctl->done, 1);
     ctl->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -614,8 +630,11 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
           *reinterpret_cast<uint4 *>(decb + i * 16) = v;
         }
         fence_async_smem();
-        mbar_arrive(&ctl->pempty[ps]);
-        mbar_arrive(&ctl->dfull[ds]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&ctl->pempty[ps]);
+          mbar_arrive(&ctl->dfull[ds]);
+        }
       }
     }
   } else if (warp == HC_MMA_WARP) {
@@ -623,6 +642,12 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, p.BNc, true, true);
       const uint32_t a_lbo = 16 * 128, b_lbo = (uint32_t)p.CB * 128;
+      // descriptors built once and stepped by (bytes >> 4), see the halo kernel
+      const uint64_t a_base = sdesc(smem_u32(smem + p.off_dec), a_lbo, 128);
+      const uint64_t b_base = sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), b_lbo, 128);
+      const uint64_t d_stage = (uint64_t)(p.dec_stage >> 4);
+      const uint64_t a_kk = (uint64_t)((2 * a_lbo) >> 4), b_kk = (uint64_t)((2 * b_lbo) >> 4);
+      const uint64_t b_kw = (uint64_t)((p.G * p.CB * 128) >> 4);
       int pit = 0, k = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
@@ -633,14 +658,16 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
           const int ds = pit % DSTAGES;
           if (!wg_wait(&ctl->dfull[ds], (pit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + p.off_dec + ds * p.dec_stage);
-          const uint32_t b0 = a0 + p.dec_b_off;
-          for (int kw = 0; kw < p.Kw; ++kw) {
+          const uint64_t a_stage = a_base + ds * d_stage;
+          uint64_t b_w = b_base + ds * d_stage;
+          const uint32_t acc0 = q > T.q0 ? 1u : 0u;
+          for (int kw = 0; kw < p.Kw; ++kw, b_w += b_kw) {
             const uint32_t d = tmem + kw * p.acc_cols;
-            for (int kk = 0; kk < p.KG / 2; ++kk) {
-              const uint64_t ad = sdesc(a0 + kk * 2 * a_lbo, a_lbo, 128);
-              const uint64_t bd = sdesc(b0 + (kw * p.G * p.CB + kk * 2 * p.CB) * 128, b_lbo, 128);
-              umma_f16(d, ad, bd, idesc, (q > T.q0 || kk > 0) ? 1u : 0u);
+            uint64_t ad = a_stage, bd = b_w;
+            uint32_t acc = acc0;
+            for (int kk = 0; kk < p.KG / 2; ++kk, ad += a_kk, bd += b_kk) {
+              umma_f16(d, ad, bd, idesc, acc);
+              acc = 1u;
             }
           }
           umma_commit(&ctl->dempty[ds]);
@@ -685,7 +712,8 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&ctl->acc_empty);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->acc_empty);
     }
   }
 
@@ -824,7 +852,9 @@ bool halo_plan(const ConvParams &cp, HaloConv &h) {
   for (;;) {
     h.NB = h.BN / 8;
     h.acc_cols = pow2_at_least32(h.BN);
-    h.R = std::min(std::min(MAX_R, 512 / h.acc_cols), std::min(4, h.Hout));
+    // two accumulator sets, so one tile's epilogue overlaps the next tile's MMAs
+    h.nbuf = 2 * h.acc_cols <= 512 ? 2 : 1;
+    h.R = std::min(std::min(MAX_R / h.nbuf, 512 / (h.nbuf * h.acc_cols)), std::min(4, h.Hout));
     size_t sm = 0;
     while (h.R >= 1 && (sm = halo_smem(h, bba, bbb)) == 0) --h.R;
     if (h.R >= 1 && sm) {

@@ -66,6 +66,7 @@ struct HaloConv {
   int Hout, Wout, NC, NCG;       // output dims and channels (fwd: Ho, Wo, Cout; dgrad: H, W, Cin)
   int Kh, Kw, padh, padw;        // taps and padding of the correlation (dgrad: K - 1 - pad)
   int P, G, R, WP, RH;           // tile: positions, batch groups, output rows; halo width / height
+  int nbuf;                      // accumulator sets (tiles in flight between MMA and epilogue)
   int BN, NB, acc_cols;          // output channels per tile, their groups, TMEM columns per row
   int nchunks;                   // CGin / 2
   int tiles_g, tiles_w, tiles_h, tiles_n, num_tiles;

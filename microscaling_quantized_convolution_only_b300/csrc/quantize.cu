@@ -19,6 +19,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <algorithm>
+
 namespace mq {
 
 __device__ __forceinline__ float load_elem(const float *p) { return __ldg(p); }
@@ -242,14 +244,101 @@ __global__ void __launch_bounds__(256) quantize_kernel(const T *__restrict__ src
   }
 }
 
+
+// ------------------------------------------------------ NCHW / OIHW path
+// Dense NCHW (or OIHW: a = Cout, b = Cin, hw = tap) input is contiguous along
+// hw; the packed output is contiguous along the b-groups of one (hw, a-group).
+// A CTA of 8 warps takes one a-group, 8 b-groups (one per warp) and 32
+// positions (one per lane): each thread quantizes one block from 64 loads that
+// are coalesced across the warp (consecutive positions), parks the packed
+// block in shared memory, and the CTA writes each position's 8 blocks out as
+// one contiguous run.
+constexpr int QN_HW = 32, QN_GB = 8;
+
+template <int FMT, typename T>
+__global__ void __launch_bounds__(256) quantize_nchw_kernel(const T *__restrict__ src, QuantParams p) {
+  constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
+  constexpr int OPITCH = QN_GB * BB + 16;                    // staged bytes per position (+16: banks)
+  __shared__ __align__(16) uint8_t obuf[QN_HW * OPITCH];
+  __shared__ uint8_t sbuf[QN_HW * QN_GB];
+  const int GA = (int)(p.d0 / 8), GB = (int)(p.d1 / 8);
+  const int64_t HW = p.d2 * p.d3;
+  const int64_t hw_tiles = (HW + QN_HW - 1) / QN_HW;
+  const int gb_tiles = (GB + QN_GB - 1) / QN_GB;
+  int64_t r = blockIdx.x;
+  const int64_t hw0 = (r % hw_tiles) * QN_HW;
+  r /= hw_tiles;
+  const int gb0 = (int)(r % gb_tiles) * QN_GB;
+  const int ga = (int)(r / gb_tiles);
+  const int ngb = min(QN_GB, GB - gb0);
+  const int nhw = (int)(HW - hw0 < (int64_t)QN_HW ? HW - hw0 : (int64_t)QN_HW);
+  const int wl = threadIdx.x >> 5, hl = threadIdx.x & 31;
+
+  const float amax_src = __uint_as_float(*p.amax_src_bits);
+  const float s_t = __fdiv_rn(amax_src, Fmt<FMT>::DENOM);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *p.s_t_out = s_t;
+    if (!(amax_src <= 3.4028234663852886e38f)) atomicOr(p.status, ST_NONFINITE);
+  }
+
+  uint32_t my_amax = 0;
+  if (wl < ngb && hl < nhw) {
+    const T *base = src + ((int64_t)(ga * 8) * p.d1 + (gb0 + wl) * 8) * HW + hw0 + hl;
+    // pass 1: block amax; pass 2 re-reads the rows (now cache hits) and
+    // encodes them eight at a time, which keeps the register count low
+    uint32_t mb = 0;
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      mb = max(mb, __float_as_uint(load_elem(base + ((i >> 3) * p.d1 + (i & 7)) * HW)) & 0x7FFFFFFFu);
+    my_amax = mb;
+    if (mb >= 0x7F800000u) atomicOr(p.status, ST_NONFINITE);
+    const uint32_t bs_code = block_scale_code<FMT>(__uint_as_float(mb), s_t);
+    const float bs = code_value<8>(bs_code);
+    uint8_t *ob = obuf + hl * OPITCH + wl * BB;
+#pragma unroll 2
+    for (int a = 0; a < 8; ++a) {
+      float x[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) x[b] = load_elem(base + (a * p.d1 + b) * HW);
+      store_row8<FMT>(ob, a, encode_row8<FMT>(x, bs, s_t));
+    }
+    sbuf[hl * QN_GB + wl] = (uint8_t)bs_code;
+  }
+  __syncthreads();
+  {
+    const int units = ngb * BB / 16;
+    for (int w = threadIdx.x; w < nhw * units; w += 256) {
+      const int h = w / units, u = w - h * units;
+      const int64_t blk0 = ((hw0 + h) * GA + ga) * (int64_t)GB + gb0;
+      reinterpret_cast<uint4 *>(p.codes + blk0 * BB)[u] = reinterpret_cast<const uint4 *>(obuf + h * OPITCH)[u];
+    }
+    for (int w = threadIdx.x; w < nhw * ngb; w += 256) {
+      const int h = w / ngb, b = w - h * ngb;
+      p.scales[((hw0 + h) * GA + ga) * (int64_t)GB + gb0 + b] = sbuf[h * QN_GB + b];
+    }
+  }
+  if (p.amax_meas_bits) {
+    uint32_t m = my_amax;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0 && m) atomicMax(p.amax_meas_bits, m);
+  }
+}
+
 // ----------------------------------------------------------------- launch
 template <int FMT, typename T>
 static cudaError_t launch_q(const void *src, int layout, const QuantParams &p, cudaStream_t s) {
   const int64_t nblk = (p.d0 / 8) * (p.d1 / 8) * p.d2 * p.d3;
-  const unsigned grid = (unsigned)((nblk + 255) / 256);
   const T *x = static_cast<const T *>(src);
-  if (layout == 1) quantize_kernel<FMT, T, 1><<<grid, 256, 0, s>>>(x, p);
-  else quantize_kernel<FMT, T, 0><<<grid, 256, 0, s>>>(x, p);
+  if (layout == 1) {
+    const unsigned grid = (unsigned)((nblk + 255) / 256);
+    quantize_kernel<FMT, T, 1><<<grid, 256, 0, s>>>(x, p);
+    return cudaGetLastError();
+  }
+  // NCHW / OIHW: 32 positions x 8 b-groups per CTA, contiguous output runs
+  const int64_t HW = p.d2 * p.d3;
+  const int64_t grid = (p.d0 / 8) * ((p.d1 / 8 + QN_GB - 1) / QN_GB) * ((HW + QN_HW - 1) / QN_HW);
+  quantize_nchw_kernel<FMT, T><<<(unsigned)grid, 256, 0, s>>>(x, p);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,121 @@
+"""GPU parity of the fused requantizing epilogues (mqconv_fwd with mq_requant,
+mqconv_dgrad_requant): the output goes from the accumulators straight into
+packed 8x8 CBF blocks, its T_scale built from a caller-supplied statistic
+(the Hindsight scheme of MicroQonv §VII).
+
+The reference is the oracle quantizer applied, with the same statistic, to the
+fp32 result the same kernels write without the epilogue (identical mainloop
+and accumulation order, so identical fp32 values): codes, scales and T_scale
+must match bit for bit, and amax_out must equal max |result|.  The fp32
+output written alongside the packed one must equal the unfused output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import microscaling_quantized_convolution_only_b300 as mq
+import oracle
+import synthetic as S
+from mqtest import LayerRun, assert_packed_equal
+from synthetic import Layer
+
+pytestmark = pytest.mark.gpu
+
+LAYERS = [
+    Layer(8, 16, 8, 8, 16, 3, 1, 1),      # halo kernel, tiny
+    Layer(16, 32, 9, 7, 48, 3, 1, 1),     # halo kernel, ragged positions
+    Layer(8, 16, 9, 7, 32, 3, 2, 1),      # generic kernel (stride 2)
+    Layer(8, 24, 10, 10, 16, 1, 2, 0),    # generic kernel (1x1 stride 2)
+    Layer(32, 64, 12, 12, 64, 3, 1, 1),   # halo kernel, several tiles
+]
+
+
+def _inputs(L, seed):
+    rng = np.random.default_rng(seed)
+    X = np.maximum(rng.standard_normal(L.x_shape()), 0).astype(np.float32)
+    W = (rng.standard_normal(L.w_shape()) * np.sqrt(2 / (L.Cin * L.k * L.k))).astype(np.float32)
+    dY = (rng.standard_normal(L.y_shape()) * 0.1).astype(np.float32)
+    return X, W, dY
+
+
+def _check(packed, ref_hwcn, fmt, role, stat, amax_out, what):
+    ref = oracle.quantize(ref_hwcn, fmt, role, "hwcn", amax_in=stat)
+    assert_packed_equal(packed, ref, what)
+    assert float(amax_out.item()) == float(np.max(np.abs(ref_hwcn))), f"{what}: amax_out"
+
+
+@pytest.mark.parametrize("fmt_in,fmt_out", [("e2m1", "e2m1"), ("e2m3", "e2m3"), ("e4m3", "e4m3"), ("e2m1", "e2m3")])
+@pytest.mark.parametrize("L", LAYERS, ids=lambda L: L.name())
+@pytest.mark.parametrize("factor", [1.0, 1.7])
+def test_fwd_requant(cuda_device, fmt_in, fmt_out, L, factor):
+    run = LayerRun(L, fmt_in, "f32", *_inputs(L, L.N + L.Cout), cuda_device, check_quant=False)
+    y = run.fwd()
+    y_np = y.cpu().numpy()
+    stat = float(np.float32(np.max(np.abs(y_np)) * factor))
+    out = mq.Packed(fmt_out, "act", L.y_shape(), device=cuda_device)
+    ain = torch.tensor([stat], device=cuda_device)
+    aout = torch.zeros(1, device=cuda_device)
+    y2 = torch.full_like(y, float("nan"))
+    mq.fwd(L, run.xq, run.wq, y2, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
+    mq.check_device_status()
+    assert torch.equal(y2, y), "fp32 output beside the fused epilogue differs from the unfused one"
+    _check(out, y_np, fmt_out, "act", stat, aout, f"fwd requant {fmt_in}->{fmt_out} {L.name()}")
+    # packed output only
+    out2 = mq.Packed(fmt_out, "act", L.y_shape(), device=cuda_device)
+    mq.fwd(L, run.xq, run.wq, None, rq_out=out2, rq_amax_in=ain, rq_amax_out=aout)
+    mq.check_device_status()
+    assert torch.equal(out2.codes, out.codes) and torch.equal(out2.scales, out.scales)
+
+
+@pytest.mark.parametrize("fmt_in,fmt_out", [("e2m1", "e2m1"), ("e2m3", "e2m3"), ("e4m3", "e4m3")])
+@pytest.mark.parametrize("L", LAYERS, ids=lambda L: L.name())
+def test_dgrad_requant(cuda_device, fmt_in, fmt_out, L):
+    run = LayerRun(L, fmt_in, "f32", *_inputs(L, 7 + L.N), cuda_device, check_quant=False)
+    dx = run.dgrad()
+    dx_np = dx.cpu().numpy()
+    stat = float(np.float32(np.max(np.abs(dx_np)) * 1.25))
+    out = mq.Packed(fmt_out, "grad", L.x_shape(), device=cuda_device)
+    ain = torch.tensor([stat], device=cuda_device)
+    aout = torch.zeros(1, device=cuda_device)
+    dx2 = torch.full_like(dx, float("nan"))
+    mq.dgrad(L, run.wq, run.gq, dx2, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
+    mq.check_device_status()
+    assert torch.equal(dx2, dx), "fp32 dX beside the fused epilogue differs from the unfused one"
+    _check(out, dx_np, fmt_out, "grad", stat, aout, f"dgrad requant {fmt_in}->{fmt_out} {L.name()}")
+    out2 = mq.Packed(fmt_out, "grad", L.x_shape(), device=cuda_device)
+    mq.dgrad(L, run.wq, run.gq, None, rq_out=out2, rq_amax_in=ain, rq_amax_out=aout)
+    mq.check_device_status()
+    assert torch.equal(out2.codes, out.codes) and torch.equal(out2.scales, out.scales)
+
+
+def test_stack_layer_requant_full_size(cuda_device):
+    """The 56x56 C128 stack layer (batch 64) in NVFP4: fused fwd and dgrad
+    epilogues against the oracle quantizer on the unfused fp32 results."""
+    wl = S.WORKLOADS[4]
+    L = S.scaled_layer(wl.layers[0], N=64)
+    X = S.draw_x(wl, 0, L.x_shape())
+    W = S.draw_w(wl, 0, L.w_shape())
+    dY = S.draw_dy(wl, 0, L.y_shape())
+    run = LayerRun(L, wl.fmt, wl.dtype, X, W, dY, cuda_device, check_quant=False)
+    for op, role, shape in (("fwd", "act", L.y_shape()), ("dgrad", "grad", L.x_shape())):
+        ref = run.fwd() if op == "fwd" else run.dgrad()
+        ref_np = ref.cpu().numpy()
+        stat = float(np.float32(np.max(np.abs(ref_np))))
+        out = mq.Packed(wl.fmt, role, shape, device=cuda_device)
+        ain = torch.tensor([stat], device=cuda_device)
+        aout = torch.zeros(1, device=cuda_device)
+        if op == "fwd":
+            mq.fwd(L, run.xq, run.wq, None, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
+        else:
+            mq.dgrad(L, run.wq, run.gq, None, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
+        mq.check_device_status()
+        _check(out, ref_np, wl.fmt, role, stat, aout, f"stack layer {op} requant")
+
+
+def test_requant_rejects_wrong_role(cuda_device):
+    L = LAYERS[0]
+    run = LayerRun(L, "e2m1", "f32", *_inputs(L, 3), cuda_device, check_quant=False)
+    out = mq.Packed("e2m1", "act", L.x_shape(), device=cuda_device)     # dgrad wants role grad
+    ain = torch.ones(1, device=cuda_device)
+    with pytest.raises(mq.MQError, match="invalid argument"):
+        mq.dgrad(L, run.wq, run.gq, None, rq_out=out, rq_amax_in=ain)
