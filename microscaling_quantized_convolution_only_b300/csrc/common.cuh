@@ -378,30 +378,58 @@ namespace mq {
 // T_scale s_t: exact RN of the real quotient x / (bs * s_t) with the bracket
 // and fma-sign tie test of resolve_tie.  Returns the packed row: element j at
 // bits 4j (E2M1), 6j (E2M3) or 8j (E4M3).
-template <int F> __device__ __forceinline__ uint64_t encode_row8(const float (&v)[8], float bs, float s_t) {
-  float inv_lo = 0.0f, inv_hi = 0.0f;
+// Bracket multipliers of the quotient x / (bs * s_t) (0 when bs is 0).
+__device__ __forceinline__ void quot_bracket(float bs, float s_t, float &inv_lo, float &inv_hi) {
+  inv_lo = inv_hi = 0.0f;
   if (bs > 0.0f) {
     const float inv = __frcp_rn(bs * s_t);
     inv_lo = inv * (1.0f - QEPS);
     inv_hi = inv * (1.0f + QEPS);
   }
+}
+
+template <int F>
+__device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs, float s_t, float inv_lo, float inv_hi);
+
+template <int F> __device__ __forceinline__ uint64_t encode_row8(const float (&v)[8], float bs, float s_t) {
+  float inv_lo, inv_hi;
+  quot_bracket(bs, s_t, inv_lo, inv_hi);
+  return encode_row8_b<F>(v, bs, s_t, inv_lo, inv_hi);
+}
+
+// encode_row8 with the bracket multipliers of quot_bracket precomputed.  The
+// codes of both bracket ends are formed a pair at a time; when a pair agrees
+// (the common case) it is placed as is, otherwise each element of the pair is
+// settled by resolve_tie.
+template <int F>
+__device__ __forceinline__ uint32_t fix_pair(uint32_t lo, uint32_t hi, float v0, float v1, float bs, float s_t) {
   constexpr uint32_t cmask = F == 4 ? 0xFu : 0xFFu;
   constexpr int sh = F == 4 ? 4 : 8;
+  uint32_t pair = 0;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const uint32_t cl = (lo >> (e * sh)) & cmask, ch = (hi >> (e * sh)) & cmask;
+    const float x = e ? v1 : v0;
+    const uint32_t c = cl == ch ? cl
+                                : resolve_tie<F>(fabsf(x), bs, s_t, cl & Fmt<F>::MAG, ch & Fmt<F>::MAG) |
+                                      (signbit(x) ? Fmt<F>::SBIT : 0u);
+    pair |= c << (e * sh);
+  }
+  return pair;
+}
+
+template <int F>
+__device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs, float s_t, float inv_lo, float inv_hi) {
   uint64_t bits = 0;
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
     const uint32_t lo = cvt2<F>(v[2 * jj] * inv_lo, v[2 * jj + 1] * inv_lo);
     const uint32_t hi = cvt2<F>(v[2 * jj] * inv_hi, v[2 * jj + 1] * inv_hi);
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const uint32_t cl = (lo >> (e * sh)) & cmask, ch = (hi >> (e * sh)) & cmask;
-      uint32_t cc = cl;
-      if (cl != ch) {
-        const float x = v[2 * jj + e];
-        cc = resolve_tie<F>(fabsf(x), bs, s_t, cl & Fmt<F>::MAG, ch & Fmt<F>::MAG) | (signbit(x) ? Fmt<F>::SBIT : 0u);
-      }
-      bits |= (uint64_t)cc << ((2 * jj + e) * (F == 4 ? 4 : F == 6 ? 6 : 8));
-    }
+    uint32_t pair = lo;
+    if (lo != hi) pair = fix_pair<F>(lo, hi, v[2 * jj], v[2 * jj + 1], bs, s_t);
+    if (F == 4) bits |= (uint64_t)pair << (8 * jj);                                    // two nibbles
+    else if (F == 8) bits |= (uint64_t)pair << (16 * jj);                              // two bytes
+    else bits |= (uint64_t)((pair & 0x3Fu) | ((pair >> 8) << 6)) << (12 * jj);          // two 6-bit codes
   }
   return bits;
 }

@@ -133,44 +133,11 @@ __device__ __forceinline__ void hc_requant16(const HaloConv &p, const float (&y)
     if (!row_ok || co >= p.NC) continue;
     const uint32_t bsc = block_scale_code_r<F>(__uint_as_float(m), s_t, inv_den);
     const float bs = code_value<8>(bsc);
-    // codes of the eight values (exact RN of the real quotient, as the quantizer)
-    float inv_lo = 0.0f, inv_hi = 0.0f;
-    if (bs > 0.0f) {
-      const float inv = __frcp_rn(bs * s_t);
-      inv_lo = inv * (1.0f - QEPS);
-      inv_hi = inv * (1.0f + QEPS);
-    }
-    constexpr uint32_t cmask = F == 4 ? 0xFu : 0xFFu;
-    constexpr int sh = F == 4 ? 4 : 8;
-    uint64_t bits = 0;
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const uint32_t lo = cvt2<F>(v[2 * jj] * inv_lo, v[2 * jj + 1] * inv_lo);
-      const uint32_t hi = cvt2<F>(v[2 * jj] * inv_hi, v[2 * jj + 1] * inv_hi);
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const uint32_t cl = (lo >> (e * sh)) & cmask, ch = (hi >> (e * sh)) & cmask;
-        uint32_t cc = cl;
-        if (cl != ch) {
-          const float x = v[2 * jj + e];
-          cc = resolve_tie<F>(fabsf(x), bs, s_t, cl & Fmt<F>::MAG, ch & Fmt<F>::MAG) |
-               (signbit(x) ? Fmt<F>::SBIT : 0u);
-        }
-        bits |= (uint64_t)cc << ((2 * jj + e) * (F == 4 ? 4 : F == 6 ? 6 : 8));
-      }
-    }
+    float inv_lo, inv_hi;
+    quot_bracket(bs, s_t, inv_lo, inv_hi);
+    const uint64_t bits = encode_row8_b<F>(v, bs, s_t, inv_lo, inv_hi);
     const int64_t blk = blk_pos_ng + co / 8;
-    uint8_t *dst = p.rq.codes + blk * Fmt<F>::BLOCK_BYTES;
-    if (F == 4) {
-      reinterpret_cast<uint32_t *>(dst)[n_in] = (uint32_t)bits;
-    } else if (F == 6) {
-      uint16_t *d16 = reinterpret_cast<uint16_t *>(dst + 6 * n_in);
-      d16[0] = (uint16_t)bits;
-      d16[1] = (uint16_t)(bits >> 16);
-      d16[2] = (uint16_t)(bits >> 32);
-    } else {
-      reinterpret_cast<uint64_t *>(dst)[n_in] = bits;
-    }
+    store_row8<F>(p.rq.codes + blk * Fmt<F>::BLOCK_BYTES, n_in, bits);
     if (n_in == 0) p.rq.scales[blk] = (uint8_t)bsc;
   }
 }

@@ -245,6 +245,15 @@ __global__ void __launch_bounds__(256) quantize_kernel(const T *__restrict__ src
 }
 
 
+// raw input bits (bf16 zero-extended) and their fp32 bit pattern
+__device__ __forceinline__ uint32_t load_bits(const float *p) { return __float_as_uint(__ldg(p)); }
+__device__ __forceinline__ uint32_t load_bits(const __nv_bfloat16 *p) {
+  return (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p));
+}
+template <typename T> __device__ __forceinline__ uint32_t to_bits32(uint32_t raw) {
+  return sizeof(T) == 2 ? raw << 16 : raw;
+}
+
 // ------------------------------------------------------ NCHW / OIHW path
 // Dense NCHW (or OIHW: a = Cout, b = Cin, hw = tap) input is contiguous along
 // hw; the packed output is contiguous along the b-groups of one (hw, a-group).
@@ -255,25 +264,28 @@ __global__ void __launch_bounds__(256) quantize_kernel(const T *__restrict__ src
 // one contiguous run.
 constexpr int QN_HW = 32, QN_GB = 8;
 
+// CTA shape: GBT b-groups (one warp each) x (8 / GBT) chunks of 32 positions;
+// GBT = min(8, B / 8) so that narrow tensors keep all warps busy.
 template <int FMT, typename T>
-__global__ void __launch_bounds__(256) quantize_nchw_kernel(const T *__restrict__ src, QuantParams p) {
+__global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2) quantize_nchw_kernel(const T *__restrict__ src, QuantParams p) {
   constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
-  constexpr int OPITCH = QN_GB * BB + 16;                    // staged bytes per position (+16: banks)
-  __shared__ __align__(16) uint8_t obuf[QN_HW * OPITCH];
+  __shared__ __align__(16) uint8_t obuf[QN_HW * QN_GB * BB + QN_HW * QN_GB * 16];   // HWT * opitch at most
   __shared__ uint8_t sbuf[QN_HW * QN_GB];
   const int GA = (int)(p.d0 / 8), GB = (int)(p.d1 / 8);
+  const int GBT = GB < QN_GB ? GB : QN_GB, HWT = QN_HW * (QN_GB / GBT);
   const int64_t HW = p.d2 * p.d3;
-  const int64_t hw_tiles = (HW + QN_HW - 1) / QN_HW;
-  const int gb_tiles = (GB + QN_GB - 1) / QN_GB;
+  const int64_t hw_tiles = (HW + HWT - 1) / HWT;
+  const int gb_tiles = (GB + GBT - 1) / GBT;
   int64_t r = blockIdx.x;
-  const int64_t hw0 = (r % hw_tiles) * QN_HW;
+  const int64_t hw0 = (r % hw_tiles) * HWT;
   r /= hw_tiles;
-  const int gb0 = (int)(r % gb_tiles) * QN_GB;
+  const int gb0 = (int)(r % gb_tiles) * GBT;
   const int ga = (int)(r / gb_tiles);
-  const int ngb = min(QN_GB, GB - gb0);
-  const int nhw = (int)(HW - hw0 < (int64_t)QN_HW ? HW - hw0 : (int64_t)QN_HW);
-  const int wl = threadIdx.x >> 5, hl = threadIdx.x & 31;
-
+  const int ngb = min(GBT, GB - gb0);
+  const int nhw = (int)(HW - hw0 < (int64_t)HWT ? HW - hw0 : (int64_t)HWT);
+  const int warp = threadIdx.x >> 5;
+  const int wl = warp % GBT, hl = (warp / GBT) * 32 + (threadIdx.x & 31);
+  const int opitch = GBT * BB + 16;    // staged bytes per position
   const float amax_src = __uint_as_float(*p.amax_src_bits);
   const float s_t = __fdiv_rn(amax_src, Fmt<FMT>::DENOM);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -283,26 +295,54 @@ __global__ void __launch_bounds__(256) quantize_nchw_kernel(const T *__restrict_
 
   uint32_t my_amax = 0;
   if (wl < ngb && hl < nhw) {
-    const T *base = src + ((int64_t)(ga * 8) * p.d1 + (gb0 + wl) * 8) * HW + hw0 + hl;
-    // pass 1: block amax; pass 2 re-reads the rows (now cache hits) and
-    // encodes them eight at a time, which keeps the register count low
-    uint32_t mb = 0;
+    // the block's 64 inputs, row a = 8 consecutive b; rows and columns are
+    // HW elements apart, addressed by pointer increments
+    const T *row = src + ((int64_t)(ga * 8) * p.d1 + (gb0 + wl) * 8) * HW + hw0 + hl;
+    const int64_t rstride = p.d1 * HW;
+    // values held as fp32 bit patterns; bf16 inputs two per register
+    constexpr int PK = sizeof(T) == 2 ? 2 : 1;
+    uint32_t raw[64 / PK];
 #pragma unroll
-    for (int i = 0; i < 64; ++i)
-      mb = max(mb, __float_as_uint(load_elem(base + ((i >> 3) * p.d1 + (i & 7)) * HW)) & 0x7FFFFFFFu);
+    for (int a = 0; a < 8; ++a, row += rstride) {
+      const T *q = row;
+#pragma unroll
+      for (int b = 0; b < 8; b += PK, q += PK * HW) {
+        if (PK == 2) raw[(a * 8 + b) / 2] = load_bits(q) | (load_bits(q + HW) << 16);
+        else raw[a * 8 + b] = load_bits(q);
+      }
+    }
+    uint32_t mb = 0;
+    if (PK == 2) {
+      uint32_t m2 = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) m2 = __vmaxu2(m2, raw[i] & 0x7FFF7FFFu);
+      mb = max(m2 << 16, m2 & 0xFFFF0000u);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64 / PK; ++i) mb = max(mb, raw[i] & 0x7FFFFFFFu);
+    }
     my_amax = mb;
     if (mb >= 0x7F800000u) atomicOr(p.status, ST_NONFINITE);
     const uint32_t bs_code = block_scale_code<FMT>(__uint_as_float(mb), s_t);
     const float bs = code_value<8>(bs_code);
-    uint8_t *ob = obuf + hl * OPITCH + wl * BB;
-#pragma unroll 2
+    float inv_lo, inv_hi;
+    quot_bracket(bs, s_t, inv_lo, inv_hi);
+    uint8_t *ob = obuf + hl * opitch + wl * BB;
+#pragma unroll
     for (int a = 0; a < 8; ++a) {
       float x[8];
 #pragma unroll
-      for (int b = 0; b < 8; ++b) x[b] = load_elem(base + (a * p.d1 + b) * HW);
-      store_row8<FMT>(ob, a, encode_row8<FMT>(x, bs, s_t));
+      for (int b = 0; b < 8; ++b) {
+        if (PK == 2) {
+          const uint32_t w = raw[(a * 8 + b) / 2];
+          x[b] = __uint_as_float((b & 1) ? (w & 0xFFFF0000u) : (w << 16));
+        } else {
+          x[b] = __uint_as_float(raw[a * 8 + b]);
+        }
+      }
+      store_row8<FMT>(ob, a, encode_row8_b<FMT>(x, bs, s_t, inv_lo, inv_hi));
     }
-    sbuf[hl * QN_GB + wl] = (uint8_t)bs_code;
+    sbuf[hl * GBT + wl] = (uint8_t)bs_code;
   }
   __syncthreads();
   {
@@ -310,11 +350,11 @@ __global__ void __launch_bounds__(256) quantize_nchw_kernel(const T *__restrict_
     for (int w = threadIdx.x; w < nhw * units; w += 256) {
       const int h = w / units, u = w - h * units;
       const int64_t blk0 = ((hw0 + h) * GA + ga) * (int64_t)GB + gb0;
-      reinterpret_cast<uint4 *>(p.codes + blk0 * BB)[u] = reinterpret_cast<const uint4 *>(obuf + h * OPITCH)[u];
+      reinterpret_cast<uint4 *>(p.codes + blk0 * BB)[u] = reinterpret_cast<const uint4 *>(obuf + h * opitch)[u];
     }
     for (int w = threadIdx.x; w < nhw * ngb; w += 256) {
       const int h = w / ngb, b = w - h * ngb;
-      p.scales[((hw0 + h) * GA + ga) * (int64_t)GB + gb0 + b] = sbuf[h * QN_GB + b];
+      p.scales[((hw0 + h) * GA + ga) * (int64_t)GB + gb0 + b] = sbuf[h * GBT + b];
     }
   }
   if (p.amax_meas_bits) {
@@ -335,9 +375,10 @@ static cudaError_t launch_q(const void *src, int layout, const QuantParams &p, c
     quantize_kernel<FMT, T, 1><<<grid, 256, 0, s>>>(x, p);
     return cudaGetLastError();
   }
-  // NCHW / OIHW: 32 positions x 8 b-groups per CTA, contiguous output runs
-  const int64_t HW = p.d2 * p.d3;
-  const int64_t grid = (p.d0 / 8) * ((p.d1 / 8 + QN_GB - 1) / QN_GB) * ((HW + QN_HW - 1) / QN_HW);
+  // NCHW / OIHW: GBT b-groups x 256 / GBT positions per CTA, contiguous output runs
+  const int64_t HW = p.d2 * p.d3, GB = p.d1 / 8;
+  const int64_t GBT = GB < QN_GB ? GB : QN_GB, HWT = QN_HW * (QN_GB / GBT);
+  const int64_t grid = (p.d0 / 8) * ((GB + GBT - 1) / GBT) * ((HW + HWT - 1) / HWT);
   quantize_nchw_kernel<FMT, T><<<(unsigned)grid, 256, 0, s>>>(x, p);
   return cudaGetLastError();
 }
