@@ -125,7 +125,7 @@ class ClockSampler:
 
 # --------------------------------------------------------------- timing
 class NullTimer:
-    def begin(self, name):
+    def begin(self, name, layer=None):
         pass
 
     def end(self):
@@ -133,7 +133,8 @@ class NullTimer:
 
 
 class OpTimer:
-    """CUDA events around each op group, on the current (launching) stream."""
+    """CUDA events around each op group, on the current (launching) stream;
+    `layer` optionally tags the op with a layer index."""
 
     def __init__(self):
         import torch
@@ -141,20 +142,29 @@ class OpTimer:
         self.pairs = []
         self.cur = None
 
-    def begin(self, name):
-        e = self.torch.cuda.Event(enable_timing=True)
+    def begin(self, name, layer=None):
+        # external: inside a CUDA-graph capture the record becomes an event
+        # node that fires on every replay
+        e = self.torch.cuda.Event(enable_timing=True, external=True)
         e.record()
-        self.cur = (name, e)
+        self.cur = (name, layer, e)
 
     def end(self):
-        e = self.torch.cuda.Event(enable_timing=True)
+        e = self.torch.cuda.Event(enable_timing=True, external=True)
         e.record()
-        self.pairs.append((self.cur[0], self.cur[1], e))
+        self.pairs.append((self.cur[0], self.cur[1], self.cur[2], e))
 
     def times(self):
         out = {}
-        for name, a, b in self.pairs:
+        for name, _, a, b in self.pairs:
             out.setdefault(name, []).append(a.elapsed_time(b))
+        return out
+
+    def layer_times(self):
+        out = {}
+        for name, layer, a, b in self.pairs:
+            if layer is not None:
+                out.setdefault((layer, name), []).append(a.elapsed_time(b))
         return out
 
 
@@ -226,7 +236,7 @@ class StackStep:
         tm.end()
         # forward: fused requantization of Y_l into X_{l+1}
         for l in range(nl):
-            tm.begin("fwd")
+            tm.begin("fwd", l)
             if l < nl - 1:
                 mq.fwd(L, self.xq[l], self.wq[l], None, rq_out=self.xq[l + 1], rq_amax_in=self.y_stat[l:l + 1],
                        rq_amax_out=self.y_amax[l:l + 1])
@@ -238,10 +248,10 @@ class StackStep:
         mq.quantize_cbf(self.dy, "nchw", self.gq[nl - 1], amax_out=self.amax[8:9])
         tm.end()
         for l in range(nl - 1, -1, -1):
-            tm.begin("wgrad")
+            tm.begin("wgrad", l)
             mq.wgrad(L, self.gq[l], self.xq[l], self.dw[l], self.ws)
             tm.end()
-            tm.begin("dgrad")
+            tm.begin("dgrad", l)
             if l > 0:   # fused requantization of dX_l into dY_{l-1}
                 mq.dgrad(L, self.wq[l], self.gq[l], None, rq_out=self.gq[l - 1], rq_amax_in=self.dx_stat[l:l + 1],
                          rq_amax_out=self.dx_amax[l:l + 1])
@@ -310,20 +320,20 @@ class LayersStep:
     def run(self, tm=None):
         mq = self.mq
         tm = tm or NullTimer()
-        for d in self.layers:
+        for li, d in enumerate(self.layers):
             L = d["L"]
-            tm.begin("quant")
+            tm.begin("quant", li)
             mq.quantize_cbf(d["x"], "nchw", d["xq"], amax_out=d["amax"][0:1])
             mq.quantize_cbf(d["w"], "oihw", d["wq"], amax_out=d["amax"][1:2])
             mq.quantize_cbf(d["dy"], "nchw", d["gq"], amax_out=d["amax"][2:3])
             tm.end()
-            tm.begin("fwd")
+            tm.begin("fwd", li)
             mq.fwd(L, d["xq"], d["wq"], d["y"])
             tm.end()
-            tm.begin("dgrad")
+            tm.begin("dgrad", li)
             mq.dgrad(L, d["wq"], d["gq"], d["dx"])
             tm.end()
-            tm.begin("wgrad")
+            tm.begin("wgrad", li)
             mq.wgrad(L, d["gq"], d["xq"], d["dw"], d["ws"])
             tm.end()
 
@@ -400,25 +410,58 @@ def run_gpu(args):
     torch.cuda.synchronize()
     mq.check_device_status()
 
-    # ---- device-timed steps (inputs resident in HBM)
+    # ---- the step as CUDA graphs: a plain one (timed as a whole) and one with
+    #      CUDA events around each op group (per-op times without host gaps)
+    graph = None
+    timed_graph, tm_graph = None, None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step.run()
+        timed_graph, tm_graph = torch.cuda.CUDAGraph(), OpTimer()
+        with torch.cuda.graph(timed_graph):
+            step.run(tm_graph)
+        graph.replay()
+        timed_graph.replay()
+        torch.cuda.synchronize()
+
+    def one_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step.run()
+
     groups = ["quant", "fwd", "dgrad", "wgrad"]
     per_kernel = {g: [] for g in groups}
-    step_ms = []
+    per_layer = {}
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     for _ in range(args.steps):
         flush.zero_()                                   # L2 flush between steps (outside the timing)
-        tm = OpTimer()
+        if timed_graph is not None:
+            tm = tm_graph
+            timed_graph.replay()
+        else:
+            tm = OpTimer()
+            step.run(tm)
+        torch.cuda.synchronize()
+        for g, v in tm.times().items():
+            per_kernel[g].extend(v)
+        for k, v in tm.layer_times().items():
+            per_layer.setdefault(k, []).extend(v)
+
+    # ---- device-timed steps (inputs resident in HBM)
+    step_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record()
-        step.run(tm)
+        one_step()
         s1.record()
         torch.cuda.synchronize()
         step_ms.append(s0.elapsed_time(s1))
-        for g, v in tm.times().items():
-            per_kernel[g].extend(v)
     clk = clocks.stop()
     barrier(world)
     mq.check_device_status()
@@ -463,6 +506,20 @@ def run_gpu(args):
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                 "peak_source": f"{peaks['source']} HBM copy"}
 
+    layers_out = []
+    for li, L in enumerate(wl.layers):
+        if (li, "fwd") not in per_layer:
+            break
+        row = {"layer": L.name()}
+        xe, we, ye = (int(np.prod(sh)) for sh in (L.x_shape(), L.w_shape(), L.y_shape()))
+        fb = packed_bytes(wl.fmt, 1)
+        byts = {"fwd": fb * (xe + we) + 4 * ye, "dgrad": fb * (we + ye) + 4 * xe, "wgrad": fb * (ye + xe) + 4 * we}
+        for op in ("fwd", "dgrad", "wgrad"):
+            t = mean(per_layer[(li, op)])
+            t_roof = max(L.flops / (peaks["bf16_tflops_sustained"] * 1e12), byts[op] / (peaks["hbm_gbs"] * 1e9))
+            row[op] = {"ms": t, "tflops": L.flops / (t * 1e-3) / 1e12, "frac_roofline": t_roof / (t * 1e-3)}
+        layers_out.append(row)
+
     # ---- end to end through the public API with host buffers
     pinned = step.pinned()
     e2e_ms = []
@@ -473,7 +530,7 @@ def run_gpu(args):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         step.upload(pinned)
-        step.run()
+        one_step()
         step.download(pinned)
         t1.record()
         torch.cuda.synchronize()
@@ -498,8 +555,12 @@ def run_gpu(args):
         "config": {"workload": wl.name, "layers": [L.name() for L in wl.layers], "element_format": wl.fmt,
                    "input_dtype": wl.dtype, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed (256 MB write) before every timed step; inputs also exceed L2",
+                   "execution": "eager launches" if graph is None else
+                                "one CUDA graph per step; per-op times from a copy of the graph with CUDA events "
+                                "around each op group",
                    "conv_flops_per_step": flops_step},
         "ops": ops,
+        "layers": layers_out,
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": step.launches_per_step * args.steps,
@@ -602,6 +663,7 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stack4-nvfp4")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of one CUDA graph per step")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch N (multiple of 8) for small profiling captures; "
                          "the default runs the workload as specified")

@@ -108,7 +108,7 @@ float pre_mult(int fa, int fb) { return (fa == MQ_FMT_E4M3 ? 4.0f : 1.0f) * (fb 
 // (stride 1), the generic implicit-im2col kernel otherwise.
 mq_status run_conv(mq::ConvParams &p, int num_sms, cudaStream_t s) {
   mq::HaloConv h;
-  if (mq::halo_plan(p, h)) return mq::halo_launch(p, h, num_sms, s) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+  if (mq::halo_plan(p, h, num_sms)) return mq::halo_launch(p, h, num_sms, s) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
   mq::conv_plan(p);
   return mq::launch_conv(p, num_sms, s) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
 }

@@ -776,7 +776,7 @@ int pow2_at_least32(int x) {
 // Plans the halo kernel for a stride-1 forward or data-gradient convolution;
 // returns false when the layer does not fit its constraints (the caller then
 // uses the generic kernel).
-bool halo_plan(const ConvParams &cp, HaloConv &h) {
+bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
   std::memset(&h, 0, sizeof(h));
   if (cp.stride != 1 || (cp.op != OP_FWD && cp.op != OP_DGRAD)) return false;
   h.op = cp.op;
@@ -815,22 +815,52 @@ bool halo_plan(const ConvParams &cp, HaloConv &h) {
   h.P = best;
   h.G = 16 / best;
   const int bba = block_bytes(cp.a.fmt), bbb = block_bytes(cp.b.fmt);
-  h.BN = std::min(256, (h.NC + 15) / 16 * 16);
-  for (;;) {
-    h.NB = h.BN / 8;
-    h.acc_cols = pow2_at_least32(h.BN);
-    // two accumulator sets, so one tile's epilogue overlaps the next tile's MMAs
-    h.nbuf = 2 * h.acc_cols <= 512 ? 2 : 1;
-    h.R = std::min(std::min(MAX_R / h.nbuf, 512 / (h.nbuf * h.acc_cols)), std::min(4, h.Hout));
-    size_t sm = 0;
-    while (h.R >= 1 && (sm = halo_smem(h, bba, bbb)) == 0) --h.R;
-    if (h.R >= 1 && sm) {
-      h.smem = sm;
-      break;
+  // Tile choice: output channels per tile BN and output rows per tile R, by
+  // a small cost model: rounds of tiles over the SMs x time per tile.  In
+  // isolation a 128 x BN x 16 MMA costs max(BN / 2, 40) cycles (narrow N runs
+  // below the peak rate; N = 64 was measured at 48); a tile pays a fixed
+  // pipeline fill / epilogue overhead of about two chunks.
+  const int taps = h.Kh * h.Kw;
+  const int bn_max = std::min(256, (h.NC + 15) / 16 * 16);
+  double best_cost = 1e300;
+  HaloConv best_h = h;
+  bool found = false;
+  // narrower than 128 columns only when the layer itself is (N < 128 MMAs run
+  // below the peak rate and duplicate the halo decode across column tiles)
+  const int bn_min = std::min(bn_max, 128);
+  for (int BN = bn_max; BN >= bn_min; BN = BN > bn_min ? std::max(bn_min, BN / 2 / 16 * 16) : 0) {
+    for (int R = 4; R >= 1; --R) {
+      HaloConv c = h;
+      c.BN = BN;
+      c.NB = BN / 8;
+      c.acc_cols = pow2_at_least32(BN);
+      // two accumulator sets, so one tile's epilogue overlaps the next tile's MMAs
+      c.nbuf = 2 * c.acc_cols <= 512 ? 2 : 1;
+      if (R > h.Hout || R * c.nbuf > MAX_R || R * c.nbuf * c.acc_cols > 512) continue;
+      c.R = R;
+      const size_t sm = halo_smem(c, bba, bbb);
+      if (!sm) continue;
+      c.smem = sm;
+      const int64_t tiles = (int64_t)(h.NG / h.G) * ((h.Wout + h.P - 1) / h.P) * ((h.Hout + R - 1) / R) *
+                            ((h.NC + BN - 1) / BN);
+      // per chunk the MMAs and the decode of its halo + weight blocks overlap;
+      // measured in this kernel: ~2x the isolated MMA cost, ~5 cycles per
+      // decoded block (8 decode warps)
+      const double mma = 2.0 * std::max(BN / 2.0, BN == 64 ? 48.0 : 40.0);
+      const double chunk_t = std::max((double)R * taps * mma, 5.0 * (c.nh_blocks + c.nb_blocks));
+      const double tile_t = (h.nchunks + 2.0) * chunk_t;
+      const double rounds = (double)((tiles + num_sms - 1) / num_sms);
+      const double cost = rounds * tile_t;
+      if (cost < best_cost * 0.98) {
+        best_cost = cost;
+        best_h = c;
+        found = true;
+      }
     }
-    if (h.BN <= 16) return false;
-    h.BN = std::max(16, h.BN / 2 / 16 * 16);
+    if (BN == bn_min) break;
   }
+  if (!found) return false;
+  h = best_h;
   h.gran_h = pow2_part(h.G * h.CGin);
   h.gran_w = h.op == OP_FWD ? pow2_part(h.CIG * std::gcd(h.COG, h.NB)) : pow2_part(std::gcd(h.CIG, h.NB));
   h.tiles_g = h.NG / h.G;

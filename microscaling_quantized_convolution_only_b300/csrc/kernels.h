@@ -112,7 +112,7 @@ struct HaloWgrad {
   size_t smem;
 };
 
-bool halo_plan(const ConvParams &cp, HaloConv &h);
+bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms);
 // max_splits <= 0: no limit
 bool halo_wgrad_plan(const ConvParams &cp, HaloWgrad &h, int max_splits);
 cudaError_t halo_wgrad_launch(const ConvParams &cp, HaloWgrad &h, int num_sms, cudaStream_t s);
