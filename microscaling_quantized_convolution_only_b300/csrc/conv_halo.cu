@@ -284,6 +284,11 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
         uint8_t *decb = dec + p.dec_b_off;
         const uint8_t *pkb = pk + p.pk_b_off;
         const uint8_t *scw = sc + p.scw_off;
+        // dgrad: block (tap, kc, nb) has scale (tap * COG + c * CGC + kc) * NB + nb
+        // = blk + tap * (COG - CGC) * NB + c * CGC * NB; tap = blk / (CGC * NB)
+        // is carried along the thread's stride instead of divided out per row
+        const int tap_span = CGC * p.NB, step_blk = HC_DEC_THREADS / 8;
+        int d_tap = (tid >> 3) / tap_span, d_rem = (tid >> 3) - d_tap * tap_span;
         for (int i = tid; i < nbr; i += HC_DEC_THREADS) {
           const int blk = i >> 3, r = i & 7;
           int si;
@@ -291,8 +296,12 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
             const int tn = blk / CGC, kc = blk - tn * CGC;
             si = tn * p.CIG + c * CGC + kc;
           } else {              // block (tap, kc, nb); scales [tap][cog][nb]
-            const int tk = blk / p.NB, nb = blk - tk * p.NB, tap = tk / CGC, kc = tk - tap * CGC;
-            si = (tap * p.COG + c * CGC + kc) * p.NB + nb;
+            si = blk + (d_tap * (p.COG - CGC) + c * CGC) * p.NB;
+            d_rem += step_blk;
+            while (d_rem >= tap_span) {
+              d_rem -= tap_span;
+              ++d_tap;
+            }
           }
           const uint8_t s = scw[si];
           const uint4 v = decode_raw<FB>(lds_row<FB>(pkb + blk * BBB, r), scale_pair<FB>(s));
