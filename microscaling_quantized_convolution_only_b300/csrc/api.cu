@@ -311,7 +311,7 @@ mq_status mqconv_quantize_cbf(const void *src, int32_t dtype, int32_t layout, co
     p.amax_meas_bits = reinterpret_cast<uint32_t *>(amax_out);
     if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), s) != cudaSuccess) return MQ_ERR_CUDA;
   }
-  if (mq::launch_quantize(src, dtype, layout, dst->fmt, p, s) != cudaSuccess) return MQ_ERR_CUDA;
+  if (mq::launch_quantize(src, dtype, layout, dst->fmt, p, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
   return MQ_OK;
 }
 

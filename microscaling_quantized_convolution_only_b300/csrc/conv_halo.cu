@@ -716,9 +716,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major tensor of `rank` dims (dims[0] innermost, in elements of
-// `esize` bytes), box `box`, no swizzle, zero fill out of range.
-bool make_map(CUtensorMap *m, const void *base, int esize, int rank, const uint64_t *dims, const uint32_t *box) {
+}  // namespace
+
+// Row-major tensor of `rank` dims (dims[0] innermost, in elements of `esize`
+// bytes), box `box`, no swizzle, zero fill out of range.  `map` points to a
+// 64-byte aligned CUtensorMap.
+bool make_tensor_map(void *map, const void *base, int esize, int rank, const uint64_t *dims, const uint32_t *box) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gd[5], gs[4];
@@ -733,12 +736,15 @@ bool make_map(CUtensorMap *m, const void *base, int esize, int rank, const uint6
   }
   const CUtensorMapDataType dt = esize == 8 ? CU_TENSOR_MAP_DATA_TYPE_UINT64
                                  : esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                 : esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
                                               : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void *>(base), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+  CUresult r = fn(static_cast<CUtensorMap *>(map), dt, (cuuint32_t)rank, const_cast<void *>(base), gd, gs, bd, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 
@@ -932,7 +938,7 @@ cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStre
   {
     const uint64_t d[4] = {(uint64_t)h.CGin * bba / 8, (uint64_t)h.NG, (uint64_t)h.Win, (uint64_t)h.Hin};
     const uint32_t bx[4] = {(uint32_t)(CGC * bba / 8), (uint32_t)h.G, (uint32_t)h.WP, (uint32_t)h.RH};
-    if (!make_map(&ma, cp.a.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
+    if (!make_tensor_map(&ma, cp.a.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
   }
   {
     // weights [taps][COG][CIG * BBB]
@@ -943,7 +949,7 @@ cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStre
     } else {
       bx[0] = (uint32_t)(h.NB * bbb / 8); bx[1] = (uint32_t)CGC; bx[2] = (uint32_t)(h.Kh * h.Kw);
     }
-    if (!make_map(&mb, cp.b.codes, 8, 3, d, bx)) return cudaErrorInvalidValue;
+    if (!make_tensor_map(&mb, cp.b.codes, 8, 3, d, bx)) return cudaErrorInvalidValue;
   }
   const int grid = std::min(h.num_tiles, num_sms);
   const int fa = cp.a.fmt, fb = cp.b.fmt;
@@ -1060,13 +1066,13 @@ cudaError_t halo_wgrad_launch(const ConvParams &cp, HaloWgrad &h, int num_sms, c
     // dY codes [Ho][Wo][NG][COG * BBA]; box: 16 channel groups x G x P x 1 row
     const uint64_t d[4] = {(uint64_t)h.COG * bba / 8, (uint64_t)h.NG, (uint64_t)h.Wo, (uint64_t)h.Ho};
     const uint32_t bx[4] = {(uint32_t)(16 * bba / 8), (uint32_t)h.G, (uint32_t)h.P, 1u};
-    if (!make_map(&ma, cp.a.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
+    if (!make_tensor_map(&ma, cp.a.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
   }
   {
     // X codes [H][W][NG][CIG * BBB]; box: CB channel groups x G x WP x 1 row
     const uint64_t d[4] = {(uint64_t)h.CIG * bbb / 8, (uint64_t)h.NG, (uint64_t)h.W, (uint64_t)h.H};
     const uint32_t bx[4] = {(uint32_t)(h.CB * bbb / 8), (uint32_t)h.G, (uint32_t)h.WP, 1u};
-    if (!make_map(&mb, cp.b.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
+    if (!make_tensor_map(&mb, cp.b.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
   }
   const int grid = std::min(h.num_tiles, num_sms);
   auto go = [&](auto kern) -> cudaError_t {

@@ -118,8 +118,14 @@ bool halo_wgrad_plan(const ConvParams &cp, HaloWgrad &h, int max_splits);
 cudaError_t halo_wgrad_launch(const ConvParams &cp, HaloWgrad &h, int num_sms, cudaStream_t s);
 cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStream_t s);
 
+// Tiled TMA descriptor of a row-major tensor (dims[0] innermost, elements of
+// esize bytes) with box `box`, zero fill outside; `map` is a 64-byte aligned
+// CUtensorMap.  False if the driver entry point or the encode fails.
+bool make_tensor_map(void *map, const void *base, int esize, int rank, const uint64_t *dims, const uint32_t *box);
+
 cudaError_t launch_amax(const void *src, int dtype, int64_t n, uint32_t *amax_bits, int num_sms, cudaStream_t s);
-cudaError_t launch_quantize(const void *src, int dtype, int layout, int fmt, const QuantParams &p, cudaStream_t s);
+cudaError_t launch_quantize(const void *src, int dtype, int layout, int fmt, const QuantParams &p, int num_sms,
+                            cudaStream_t s);
 
 // Fills the tiling fields of p for `num_sms` and returns the number of tiles.
 int64_t conv_plan(ConvParams &p);

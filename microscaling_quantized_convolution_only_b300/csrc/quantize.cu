@@ -14,6 +14,7 @@
 // hardware RN conversions on a bracket [q(1-eps), q(1+eps)] of the quotient
 // and resolves the rare bracket that straddles a rounding midpoint with an
 // exact fma-sign test.  Codes and the scale byte are written once.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -365,9 +366,226 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2) quantize_nchw_ker
   }
 }
 
+
+// ------------------------------------------------- NCHW / OIHW, TMA path
+// Same tiling and arithmetic as quantize_nchw_kernel, but the input tile
+// (8 rows of a x GBT*8 rows of b x HWT positions) arrives by one tiled TMA
+// copy into a QT_STAGES-deep shared ring, filled by a producer warp while the
+// eight compute warps quantize the previous tiles from shared memory.  The
+// global-load latency then no longer waits on the encode work.
+constexpr int QT_STAGES = 2;
+constexpr int QT_CWARPS = 8;
+constexpr int QT_THREADS = (QT_CWARPS + 1) * 32;
+
+struct QtCtl {
+  uint64_t full[QT_STAGES], empty[QT_STAGES];
+  int abort;
+};
+
+// bounded wait: gives up after 2 s, or at once when another warp has given
+// up, so that every warp leaves its loop and the CTA still meets at its
+// barriers
+__device__ __forceinline__ bool qt_wait(uint64_t *bar, uint32_t parity, QtCtl *ctl, uint32_t *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*reinterpret_cast<volatile int *>(&ctl->abort)) return false;
+    if (globaltimer_ns() - t0 > 2000000000ull) {
+      atomicOr(status, ST_TIMEOUT);
+      *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
+      return false;
+    }
+  }
+}
+
+template <int FMT, typename T, int GBT>
+__global__ void __launch_bounds__(QT_THREADS, 2)
+    quantize_tma_kernel(const __grid_constant__ CUtensorMap tm, QuantParams p, int ntiles, int hw_tiles, int gb_tiles) {
+  constexpr int HWT = QN_HW * (QN_GB / GBT);
+  constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
+  constexpr int STAGE = HWT * GBT * 64 * (int)sizeof(T);
+  constexpr int OPITCH = GBT * BB + 16;
+  extern __shared__ __align__(1024) uint8_t qraw[];
+  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(qraw) + 1023) & ~uintptr_t(1023));
+  uint8_t *obuf = ring + QT_STAGES * STAGE;
+  uint8_t *sbuf = obuf + HWT * OPITCH;
+  QtCtl *ctl = reinterpret_cast<QtCtl *>(sbuf + ((HWT * GBT + 15) / 16) * 16);
+  const int GA = (int)(p.d0 / 8), GB = (int)(p.d1 / 8);
+  const int64_t HW = p.d2 * p.d3;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const float amax_src = __uint_as_float(*p.amax_src_bits);
+  const float s_t = __fdiv_rn(amax_src, Fmt<FMT>::DENOM);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < QT_STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], QT_CWARPS);
+    }
+    ctl->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (blockIdx.x == 0) {
+      *p.s_t_out = s_t;
+      if (!(amax_src <= 3.4028234663852886e38f)) atomicOr(p.status, ST_NONFINITE);
+    }
+  }
+  __syncthreads();
+
+  if (warp == QT_CWARPS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int s = it % QT_STAGES;
+        if (!qt_wait(&ctl->empty[s], ((it / QT_STAGES) & 1) ^ 1, ctl, p.status)) break;
+        const int hwt = t % hw_tiles, rest = t / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
+        mbar_expect_tx(&ctl->full[s], STAGE);
+        tma_load_3d(ring + s * STAGE, &tm, &ctl->full[s], hwt * HWT, gbt * GBT * 8, ga * 8);
+      }
+      for (int i = 0; i < QT_STAGES && i < it; ++i) {   // copies in flight land before exit
+        const int q = it - 1 - i;
+        mbar_wait(&ctl->full[q % QT_STAGES], (q / QT_STAGES) & 1, p.status);   // ignores the abort flag
+      }
+    }
+    __syncwarp();
+    return;
+  }
+
+  // --------------------------------------------------------------- compute
+  const int wl = warp % GBT, hl = (warp / GBT) * 32 + lane;
+  uint32_t my_amax = 0;
+  int it = 0;
+  for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    const int s = it % QT_STAGES;
+    // a failed wait still takes part in the named barriers below
+    const bool ok = qt_wait(&ctl->full[s], (it / QT_STAGES) & 1, ctl, p.status);
+    const int hwt = t % hw_tiles, rest = t / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
+    const int64_t hw0 = (int64_t)hwt * HWT;
+    const int gb0 = gbt * GBT;
+    const int ngb = min(GBT, GB - gb0);
+    const int nhw = (int)(HW - hw0 < (int64_t)HWT ? HW - hw0 : (int64_t)HWT);
+    // tile in shared memory: [a (8)][b (GBT*8)][hw (HWT)], hw fastest
+    const T *tile = reinterpret_cast<const T *>(ring + s * STAGE) + (wl * 8) * HWT + hl;
+    const bool mine = ok && wl < ngb && hl < nhw;
+    uint32_t raw[sizeof(T) == 2 ? 32 : 64];
+    if (mine) {
+#pragma unroll
+      for (int a = 0; a < 8; ++a) {
+#pragma unroll
+        for (int b = 0; b < 8; b += (sizeof(T) == 2 ? 2 : 1)) {
+          const T *q = tile + (a * GBT * 8 + b) * HWT;
+          if (sizeof(T) == 2) {
+            const uint32_t lo = *reinterpret_cast<const unsigned short *>(q);
+            const uint32_t hi = *reinterpret_cast<const unsigned short *>(q + HWT);
+            raw[(a * 8 + b) / 2] = lo | (hi << 16);
+          } else {
+            raw[a * 8 + b] = *reinterpret_cast<const uint32_t *>(q);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->empty[s]);          // tile consumed (values are in registers)
+    if (mine) {
+      uint32_t mb = 0;
+      if (sizeof(T) == 2) {
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) m2 = __vmaxu2(m2, raw[i] & 0x7FFF7FFFu);
+        mb = max(m2 << 16, m2 & 0xFFFF0000u);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) mb = max(mb, raw[i & 63] & 0x7FFFFFFFu);
+      }
+      my_amax = max(my_amax, mb);
+      if (mb >= 0x7F800000u) atomicOr(p.status, ST_NONFINITE);
+      const uint32_t bs_code = block_scale_code<FMT>(__uint_as_float(mb), s_t);
+      const float bs = code_value<8>(bs_code);
+      float inv_lo, inv_hi;
+      quot_bracket(bs, s_t, inv_lo, inv_hi);
+      uint8_t *ob = obuf + hl * OPITCH + wl * BB;
+#pragma unroll
+      for (int a = 0; a < 8; ++a) {
+        float x[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (sizeof(T) == 2) {
+            const uint32_t w = raw[((a * 8 + b) / 2) & 31];
+            x[b] = __uint_as_float((b & 1) ? (w & 0xFFFF0000u) : (w << 16));
+          } else {
+            x[b] = __uint_as_float(raw[(a * 8 + b) & 63]);
+          }
+        }
+        store_row8<FMT>(ob, a, encode_row8_b<FMT>(x, bs, s_t, inv_lo, inv_hi));
+      }
+      sbuf[hl * GBT + wl] = (uint8_t)bs_code;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(QT_CWARPS * 32) : "memory");
+    if (!*reinterpret_cast<volatile int *>(&ctl->abort)) {
+      const int units = ngb * BB / 16;
+      for (int w = threadIdx.x; w < nhw * units; w += QT_CWARPS * 32) {
+        const int h = w / units, u = w - h * units;
+        const int64_t blk0 = ((hw0 + h) * GA + ga) * (int64_t)GB + gb0;
+        reinterpret_cast<uint4 *>(p.codes + blk0 * BB)[u] = reinterpret_cast<const uint4 *>(obuf + h * OPITCH)[u];
+      }
+      for (int w = threadIdx.x; w < nhw * ngb; w += QT_CWARPS * 32) {
+        const int h = w / ngb, b = w - h * ngb;
+        p.scales[((hw0 + h) * GA + ga) * (int64_t)GB + gb0 + b] = sbuf[h * GBT + b];
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(QT_CWARPS * 32) : "memory");
+  }
+  if (p.amax_meas_bits) {
+    uint32_t m = my_amax;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0 && m) atomicMax(p.amax_meas_bits, m);
+  }
+}
+
+template <int FMT, typename T, int GBT>
+static cudaError_t launch_tma_q(const T *src, const QuantParams &p, int num_sms, cudaStream_t s) {
+  constexpr int HWT = QN_HW * (QN_GB / GBT);
+  const int64_t HW = p.d2 * p.d3, GB = p.d1 / 8, GA = p.d0 / 8;
+  alignas(64) uint8_t map[128];
+  const uint64_t dims[3] = {(uint64_t)HW, (uint64_t)p.d1, (uint64_t)p.d0};
+  const uint32_t box[3] = {(uint32_t)HWT, (uint32_t)(GBT * 8), 8u};
+  if (!make_tensor_map(map, src, (int)sizeof(T), 3, dims, box)) return cudaErrorInvalidValue;
+  const int64_t hw_tiles = (HW + HWT - 1) / HWT, gb_tiles = (GB + GBT - 1) / GBT;
+  const int64_t ntiles = GA * gb_tiles * hw_tiles;
+  constexpr size_t STAGE = (size_t)HWT * GBT * 64 * sizeof(T);
+  const size_t smem = 1024 + QT_STAGES * STAGE + (size_t)HWT * (GBT * Fmt<FMT>::BLOCK_BYTES + 16) +
+                      ((HWT * GBT + 15) / 16) * 16 + sizeof(QtCtl);
+  auto k = quantize_tma_kernel<FMT, T, GBT>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, QT_THREADS, smem);
+  const int64_t grid = std::min<int64_t>(ntiles, (int64_t)num_sms * std::max(1, per_sm));
+  k<<<(unsigned)grid, QT_THREADS, smem, s>>>(*reinterpret_cast<const CUtensorMap *>(map), p, (int)ntiles,
+                                             (int)hw_tiles, (int)gb_tiles);
+  return cudaGetLastError();
+}
+
+// TMA path when the rows are 16-byte aligned and the ring fits, else the
+// direct-load kernel
+template <int FMT, typename T>
+static bool try_tma_q(const T *src, const QuantParams &p, int num_sms, cudaStream_t s, cudaError_t &err) {
+  const int64_t HW = p.d2 * p.d3, GB = p.d1 / 8;
+  if ((HW * (int64_t)sizeof(T)) % 16 || (reinterpret_cast<uintptr_t>(src) & 15) || HW >= ((int64_t)1 << 31) ||
+      p.d0 * p.d1 >= ((int64_t)1 << 31))
+    return false;
+  if (sizeof(T) == 4 && GB >= 8) return false;   // two 64 KB stages per CTA leave one CTA per SM; direct kernel
+  if (GB >= 8) err = launch_tma_q<FMT, T, 8>(src, p, num_sms, s);
+  else if (GB >= 4) err = launch_tma_q<FMT, T, 4>(src, p, num_sms, s);
+  else if (GB >= 2) err = launch_tma_q<FMT, T, 2>(src, p, num_sms, s);
+  else err = launch_tma_q<FMT, T, 1>(src, p, num_sms, s);
+  return true;
+}
+
 // ----------------------------------------------------------------- launch
 template <int FMT, typename T>
-static cudaError_t launch_q(const void *src, int layout, const QuantParams &p, cudaStream_t s) {
+static cudaError_t launch_q(const void *src, int layout, const QuantParams &p, int num_sms, cudaStream_t s) {
   const int64_t nblk = (p.d0 / 8) * (p.d1 / 8) * p.d2 * p.d3;
   const T *x = static_cast<const T *>(src);
   if (layout == 1) {
@@ -375,6 +593,8 @@ static cudaError_t launch_q(const void *src, int layout, const QuantParams &p, c
     quantize_kernel<FMT, T, 1><<<grid, 256, 0, s>>>(x, p);
     return cudaGetLastError();
   }
+  cudaError_t err = cudaSuccess;
+  if (try_tma_q<FMT, T>(x, p, num_sms, s, err)) return err;
   // NCHW / OIHW: GBT b-groups x 256 / GBT positions per CTA, contiguous output runs
   const int64_t HW = p.d2 * p.d3, GB = p.d1 / 8;
   const int64_t GBT = GB < QN_GB ? GB : QN_GB, HWT = QN_HW * (QN_GB / GBT);
@@ -392,15 +612,16 @@ cudaError_t launch_amax(const void *src, int dtype, int64_t n, uint32_t *amax_bi
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize(const void *src, int dtype, int layout, int fmt, const QuantParams &p, cudaStream_t s) {
+cudaError_t launch_quantize(const void *src, int dtype, int layout, int fmt, const QuantParams &p, int num_sms,
+                            cudaStream_t s) {
   if (dtype == 0) {
-    if (fmt == 4) return launch_q<4, float>(src, layout, p, s);
-    if (fmt == 6) return launch_q<6, float>(src, layout, p, s);
-    return launch_q<8, float>(src, layout, p, s);
+    if (fmt == 4) return launch_q<4, float>(src, layout, p, num_sms, s);
+    if (fmt == 6) return launch_q<6, float>(src, layout, p, num_sms, s);
+    return launch_q<8, float>(src, layout, p, num_sms, s);
   }
-  if (fmt == 4) return launch_q<4, __nv_bfloat16>(src, layout, p, s);
-  if (fmt == 6) return launch_q<6, __nv_bfloat16>(src, layout, p, s);
-  return launch_q<8, __nv_bfloat16>(src, layout, p, s);
+  if (fmt == 4) return launch_q<4, __nv_bfloat16>(src, layout, p, num_sms, s);
+  if (fmt == 6) return launch_q<6, __nv_bfloat16>(src, layout, p, num_sms, s);
+  return launch_q<8, __nv_bfloat16>(src, layout, p, num_sms, s);
 }
 
 }  // namespace mq

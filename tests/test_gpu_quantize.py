@@ -20,7 +20,8 @@ def rand(shape, seed, scale=1.0):
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("shape", [(8, 16, 8, 8), (16, 24, 7, 5), (64, 32, 3, 9), (8, 8, 1, 1)])
+@pytest.mark.parametrize("shape", [(8, 16, 8, 8), (16, 24, 7, 5), (64, 32, 3, 9), (8, 8, 1, 1),
+                                   (16, 64, 5, 8), (24, 40, 4, 6), (8, 24, 2, 4), (16, 136, 6, 12)])
 def test_nchw(cuda_device, fmt, dtype, shape):
     x = rand(shape, sum(shape))
     if dtype == "bf16":
