@@ -1,5 +1,6 @@
-// conv_halo.cu -- stride-1 forward and data-gradient convolutions that decode
-// every packed input block once per tile and reuse it for all taps.
+// conv_halo.cu -- forward (stride 1 and 2), stride-1 data-gradient and
+// weight-gradient (stride 1 and 2) convolutions that decode every packed
+// input block once per tile and reuse it for all taps.
 //
 // MicroQonv §IV-A builds the channel-batch-first im2col X' on chip: each
 // contiguous CBF block crosses the off-chip/on-chip boundary once and is then
@@ -13,6 +14,12 @@
 // shared-memory matrix descriptor whose start address is shifted by
 // ((s + u) * (P + Kw - 1) + v) halo positions.  The weights of the chunk
 // (all taps, BN output channels) are staged and decoded the same way.
+//
+// Stride 2: the halo spans 2 (R - 1) + Kh rows and its even and odd input
+// columns are staged as two phases (two TMA boxes through a [H][W/2][2]
+// view of the codes), so output position p, tap v reads phase v % 2 at
+// position p + v / 2: the rows of one tap are again unit-stride halo
+// positions and one descriptor per tap still covers the 128 GEMM rows.
 //
 // The data gradient of a stride-1 layer is the same correlation run on dY
 // with the taps mirrored and the weight blocks read transposed
@@ -200,13 +207,17 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
       if (!__shfl_sync(0xFFFFFFFFu, okw, 0)) break;
       uint8_t *scd = smem + p.off_sc + tb * p.sc_stride;
       {
-        // halo block scales: one run of G * CGin bytes per halo position
+        // halo block scales: one run of G * CGin bytes per halo position,
+        // positions ordered (column phase, row, column) like the code boxes;
+        // the padding positions at the end of a phase get zeros
         const int run = p.G * p.CGin;
         copy_runs_rt(
-            p.gran_h, scd, p.RH * p.WP, run, run,
+            p.gran_h, scd, p.NPH * p.PHP, run, run,
             [&](int r) -> const uint8_t * {
-              const int hr = r / p.WP, wc = r - hr * p.WP;
-              const int hi = tc.h0 - p.padh + hr, wi = tc.w0 - p.padw + wc;
+              const int ph = r / p.PHP, rr = r - ph * p.PHP;
+              const int hr = rr / p.WP, wc = rr - hr * p.WP;
+              if (hr >= p.RH) return nullptr;
+              const int hi = p.S * tc.h0 - p.padh + hr, wi = p.S * tc.w0 - p.padw + ph + p.S * wc;
               if ((unsigned)hi >= (unsigned)p.Hin || (unsigned)wi >= (unsigned)p.Win) return nullptr;
               return p.in_scales + (((int64_t)hi * p.Win + wi) * p.NG + tc.g0) * p.CGin;
             },
@@ -235,7 +246,18 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
           if (!hc_wait(&ctl->pempty[ps], ((pit / p.PS) & 1) ^ 1, p, ctl)) { ok = false; break; }
           mbar_expect_tx(&ctl->pfull[ps], p.pk_bytes);
           uint8_t *dst = smem + p.off_pk + ps * p.pk_stage;
-          tma_load_4d(dst, &tm_in, &ctl->pfull[ps], c * CGC * BBA / 8, tc.g0, tc.w0 - p.padw, tc.h0 - p.padh);
+          if (p.S == 1) {
+            tma_load_4d(dst, &tm_in, &ctl->pfull[ps], c * CGC * BBA / 8, tc.g0, tc.w0 - p.padw, tc.h0 - p.padh);
+          } else {
+            // stride 2: halo phase ph holds the input columns 2 w0 - padw + ph + 2 k,
+            // read through the view [H][W/2][2][NG][..] of the same codes
+            const uint32_t ph_bytes = (uint32_t)(p.PHP * p.G * CGC * BBA);   // a multiple of 128
+            for (int ph = 0; ph < p.NPH; ++ph) {
+              const int wc0 = 2 * tc.w0 - p.padw + ph, gph = wc0 & 1;
+              tma_load_5d(dst + ph * ph_bytes, &tm_in, &ctl->pfull[ps], c * CGC * BBA / 8, tc.g0, gph,
+                          (wc0 - gph) / 2, 2 * tc.h0 - p.padh);
+            }
+          }
           if (OP == OP_FWD)
             tma_load_3d(dst + p.pk_b_off, &tm_w, &ctl->pfull[ps], c * CGC * BBB / 8, tc.n0 / 8, 0);
           else
@@ -323,17 +345,33 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, p.BN, false, OP == OP_DGRAD);
-      // Descriptors are built once and stepped: the start-address field is
-      // bits 0-13 of (address >> 4), so moving an operand by `bytes` adds
-      // bytes >> 4 to the descriptor (addresses stay below 256 KB).
-      const uint64_t d_row = (uint64_t)((p.WP * p.G * CGC * 128) >> 4);   // one halo row
-      const uint64_t d_col = (uint64_t)((p.G * CGC * 128) >> 4);          // one halo position
-      const uint64_t d_tap = (uint64_t)((p.NB * CGC * 128) >> 4);         // one weight tap
-      const uint64_t d_stage = (uint64_t)(p.dec_stage >> 4);
-      const uint64_t a_base = sdesc(smem_u32(smem + p.off_dec), 128, CGC * 128);
-      const uint64_t b_base = OP == OP_FWD ? sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), 128, CGC * 128)
+      // Descriptor words: the high word (stride fields, version) is fixed;
+      // the low word holds (address >> 4) in bits 0-13, so moving an operand
+      // by `bytes` adds bytes >> 4 to it (addresses stay below 256 KB).
+      const uint64_t a_desc = sdesc(smem_u32(smem + p.off_dec), 128, CGC * 128);
+      const uint64_t b_desc = OP == OP_FWD ? sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), 128, CGC * 128)
                                            : sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), p.NB * 128, 128);
+      const uint32_t a_hi = (uint32_t)(a_desc >> 32), b_hi = (uint32_t)(b_desc >> 32);
+      const uint32_t d_row = (uint32_t)((p.WP * p.G * CGC * 128) >> 4);     // one halo row
+      const uint32_t d_col = (uint32_t)((p.G * CGC * 128) >> 4);            // one halo position
+      const uint32_t d_phase = (uint32_t)((p.PHP * p.G * CGC * 128) >> 4);  // one column phase
+      const uint32_t d_tap = (uint32_t)((p.NB * CGC * 128) >> 4);           // one weight tap
+      const uint32_t d_stage = p.dec_stage >> 4;
+      const int sh = p.S - 1;   // tap v sits in column phase v & sh, v >> sh positions in
       const int taps = p.Kh * p.Kw;
+      // Per-tap operand offsets, built once: tap t = (u, v) reads the halo
+      // at row u, phase v & sh, position v >> sh, and the weights of tap t
+      // (fwd) or of the mirrored tap taps - 1 - t (dgrad).  Up to UT taps
+      // the issue loop is unrolled over this table: one add per operand per
+      // MMA.
+      constexpr int UT = 9;
+      uint32_t a_off[UT], b_off[UT];
+#pragma unroll
+      for (int t = 0; t < UT; ++t) {
+        const int u = t / p.Kw, v = t - u * p.Kw;
+        a_off[t] = (uint32_t)u * d_row + (uint32_t)(v & sh) * d_phase + (uint32_t)(v >> sh) * d_col;
+        b_off[t] = (uint32_t)(OP == OP_FWD ? t : taps - 1 - t) * d_tap;
+      }
       int dit = 0, k = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
@@ -341,9 +379,8 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
           const int ds = dit % DSTAGES;
           if (!hc_wait(&ctl->dfull[ds], (dit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t a_stage = a_base + ds * d_stage;
-          // dgrad walks the weight taps mirrored: W tap (Kh-1-u, Kw-1-v) = taps-1-(u*Kw+v)
-          const uint64_t b_first = b_base + ds * d_stage + (OP == OP_FWD ? 0 : (uint64_t)(taps - 1) * d_tap);
+          const uint32_t a_stage = (uint32_t)a_desc + (uint32_t)ds * d_stage;
+          const uint32_t b_stage = (uint32_t)b_desc + (uint32_t)ds * d_stage;
           const int buf = k % p.nbuf, use = k / p.nbuf;
           for (int s = 0; s < p.R && ok; ++s) {
             const int slot = buf * p.R + s;
@@ -352,14 +389,19 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
               tc_fence_after();
             }
             const uint32_t d = tmem + slot * p.acc_cols;
-            uint64_t a_u = a_stage + s * d_row, bd = b_first;
-            uint32_t acc = c > 0 ? 1u : 0u;
-            for (int u = 0; u < p.Kh; ++u, a_u += d_row) {
-              uint64_t ad = a_u;
-              for (int v = 0; v < p.Kw; ++v, ad += d_col) {
-                umma_f16(d, ad, bd, idesc, acc);
-                acc = 1u;
-                if (OP == OP_FWD) bd += d_tap; else bd -= d_tap;
+            const uint32_t a_s = a_stage + (uint32_t)(s * p.S) * d_row;
+            if (taps <= UT) {
+#pragma unroll
+              for (int tp = 0; tp < UT; ++tp)
+                if (tp < taps)
+                  umma_f16(d, desc_of(a_hi, a_s + a_off[tp]), desc_of(b_hi, b_stage + b_off[tp]), idesc,
+                           (tp > 0 || c > 0) ? 1u : 0u);
+            } else {
+              for (int tp = 0; tp < taps; ++tp) {
+                const int u = tp / p.Kw, v = tp - u * p.Kw;
+                const uint32_t ao = (uint32_t)u * d_row + (uint32_t)(v & sh) * d_phase + (uint32_t)(v >> sh) * d_col;
+                const uint32_t bo = (uint32_t)(OP == OP_FWD ? tp : taps - 1 - tp) * d_tap;
+                umma_f16(d, desc_of(a_hi, a_s + ao), desc_of(b_hi, b_stage + bo), idesc, (tp > 0 || c > 0) ? 1u : 0u);
               }
             }
             if (c == p.nchunks - 1) umma_commit(&ctl->acc_full[slot]);
@@ -538,13 +580,23 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
         if (!__shfl_sync(0xFFFFFFFFu, okw, 0)) { ok = false; break; }
         const int gb = q % p.tiles_g, rest = q / p.tiles_g;
         const int g0 = gb * p.G, wo0 = (rest % p.tiles_w) * p.P, ho = rest / p.tiles_w;
-        const int hi = ho + T.kh - p.pad;
+        const int hi = p.S * ho + T.kh - p.pad;
         uint8_t *stage = smem + p.off_pk + ps * p.pk_stage;
         uint8_t *sc = stage + p.pk_sc_off;
         if (lane == 0) {
           mbar_add_tx(&ctl->pfull[ps], p.pk_bytes);
           tma_load_4d(stage, &tm_a, &ctl->pfull[ps], (T.m0 / 8) * BBA / 8, g0, wo0, ho);
-          tma_load_4d(stage + p.pk_b_off, &tm_b, &ctl->pfull[ps], (T.c0 / 8) * BBB / 8, g0, wo0 - p.pad, hi);
+          if (p.S == 1) {
+            tma_load_4d(stage + p.pk_b_off, &tm_b, &ctl->pfull[ps], (T.c0 / 8) * BBB / 8, g0, wo0 - p.pad, hi);
+          } else {
+            // stride 2: X halo phase ph = input columns 2 wo0 - pad + ph + 2 k
+            const uint32_t ph_bytes = (uint32_t)(p.PHP * p.G * p.CB * BBB);   // a multiple of 128
+            for (int ph = 0; ph < p.NPH; ++ph) {
+              const int wc0 = 2 * wo0 - p.pad + ph, gph = wc0 & 1;
+              tma_load_5d(stage + p.pk_b_off + ph * ph_bytes, &tm_b, &ctl->pfull[ps], (T.c0 / 8) * BBB / 8, g0, gph,
+                          (wc0 - gph) / 2, hi);
+            }
+          }
         }
         // dY block scales: run (p, j) = 16 output-channel groups
         const int mbv = min(16, p.COG - T.m0 / 8);
@@ -556,12 +608,15 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
               return p.a_scales + (((int64_t)ho * p.Wo + wo) * p.NG + g0 + j) * p.COG + T.m0 / 8;
             },
             [&](int) { return mbv; }, p.a_scales, lane);
-        // X halo block scales: run (wc, j) = CB input-channel groups
-        const int cbv = min(p.CB, p.CIG - T.c0 / 8);
+        // X halo block scales: run (phase, wc, j) = CB input-channel groups;
+        // the padding positions at the end of a phase get zeros
+        const int cbv = min(p.CB, p.CIG - T.c0 / 8), ph_runs = p.PHP * p.G;
         copy_runs_rt(
-            p.gran_b, sc + p.na_blocks, p.WP * p.G, p.CB, p.CB,
+            p.gran_b, sc + p.na_blocks, p.NPH * ph_runs, p.CB, p.CB,
             [&](int r) -> const uint8_t * {
-              const int wc = r / p.G, j = r - wc * p.G, wi = wo0 - p.pad + wc;
+              const int ph = r / ph_runs, rr = r - ph * ph_runs;
+              const int wc = rr / p.G, j = rr - wc * p.G, wi = p.S * wo0 - p.pad + ph + p.S * wc;
+              if (wc >= p.WP) return nullptr;
               if ((unsigned)hi >= (unsigned)p.H || (unsigned)wi >= (unsigned)p.W) return nullptr;
               return p.b_scales + (((int64_t)hi * p.W + wi) * p.NG + g0 + j) * p.CIG + T.c0 / 8;
             },
@@ -618,12 +673,16 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, p.BNc, true, true);
       const uint32_t a_lbo = 16 * 128, b_lbo = (uint32_t)p.CB * 128;
-      // descriptors built once and stepped by (bytes >> 4), see the halo kernel
-      const uint64_t a_base = sdesc(smem_u32(smem + p.off_dec), a_lbo, 128);
-      const uint64_t b_base = sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), b_lbo, 128);
-      const uint64_t d_stage = (uint64_t)(p.dec_stage >> 4);
-      const uint64_t a_kk = (uint64_t)((2 * a_lbo) >> 4), b_kk = (uint64_t)((2 * b_lbo) >> 4);
-      const uint64_t b_kw = (uint64_t)((p.G * p.CB * 128) >> 4);
+      // descriptor low words stepped by (bytes >> 4), see the halo kernel
+      const uint64_t a_desc = sdesc(smem_u32(smem + p.off_dec), a_lbo, 128);
+      const uint64_t b_desc = sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), b_lbo, 128);
+      const uint32_t a_hi = (uint32_t)(a_desc >> 32), b_hi = (uint32_t)(b_desc >> 32);
+      const uint32_t d_stage = p.dec_stage >> 4;
+      const uint32_t a_kk = (2 * a_lbo) >> 4, b_kk = (2 * b_lbo) >> 4;   // 16 more K (two k-groups)
+      const uint32_t b_kw = (uint32_t)((p.G * p.CB * 128) >> 4);             // one halo position
+      const uint32_t b_phase = (uint32_t)((p.PHP * p.G * p.CB * 128) >> 4);  // one column phase
+      const int sh = p.S - 1;   // tap kw: column phase kw & sh, kw >> sh positions in
+      constexpr int KK = 8;     // MMAs per tap and chunk: K = 8 P G = 128 (KG = 16)
       int pit = 0, k = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
@@ -634,17 +693,15 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
           const int ds = pit % DSTAGES;
           if (!wg_wait(&ctl->dfull[ds], (pit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t a_stage = a_base + ds * d_stage;
-          uint64_t b_w = b_base + ds * d_stage;
-          const uint32_t acc0 = q > T.q0 ? 1u : 0u;
-          for (int kw = 0; kw < p.Kw; ++kw, b_w += b_kw) {
+          const uint32_t a_stage = (uint32_t)a_desc + (uint32_t)ds * d_stage;
+          const uint32_t b_stage = (uint32_t)b_desc + (uint32_t)ds * d_stage;
+          for (int kw = 0; kw < p.Kw; ++kw) {
             const uint32_t d = tmem + kw * p.acc_cols;
-            uint64_t ad = a_stage, bd = b_w;
-            uint32_t acc = acc0;
-            for (int kk = 0; kk < p.KG / 2; ++kk, ad += a_kk, bd += b_kk) {
-              umma_f16(d, ad, bd, idesc, acc);
-              acc = 1u;
-            }
+            const uint32_t b_w = b_stage + (uint32_t)(kw & sh) * b_phase + (uint32_t)(kw >> sh) * b_kw;
+#pragma unroll
+            for (int kk = 0; kk < KK; ++kk)
+              umma_f16(d, desc_of(a_hi, a_stage + kk * a_kk), desc_of(b_hi, b_w + kk * b_kk), idesc,
+                       (kk > 0 || q > T.q0) ? 1u : 0u);
           }
           umma_commit(&ctl->dempty[ds]);
         }
@@ -722,17 +779,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // bytes), box `box`, no swizzle, zero fill out of range.  `map` points to a
 // 64-byte aligned CUtensorMap.
 bool make_tensor_map(void *map, const void *base, int esize, int rank, const uint64_t *dims, const uint32_t *box) {
+  uint64_t gs[4];
+  uint64_t stride = (uint64_t)esize;
+  for (int i = 0; i < rank; ++i) {
+    if (i > 0) gs[i - 1] = stride;
+    stride *= dims[i];
+  }
+  return make_tensor_map_strided(map, base, esize, rank, dims, gs, box);
+}
+
+bool make_tensor_map_strided(void *map, const void *base, int esize, int rank, const uint64_t *dims,
+                             const uint64_t *strides, const uint32_t *box) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn || rank < 1 || rank > 5) return false;
   cuuint64_t gd[5], gs[4];
   cuuint32_t bd[5], es[5];
-  uint64_t stride = (uint64_t)esize;
   for (int i = 0; i < rank; ++i) {
     gd[i] = dims[i];
     bd[i] = box[i];
     es[i] = 1;
-    if (i > 0) gs[i - 1] = stride;
-    stride *= dims[i];
+    if (i > 0) gs[i - 1] = strides[i - 1];
   }
   const CUtensorMapDataType dt = esize == 8 ? CU_TENSOR_MAP_DATA_TYPE_UINT64
                                  : esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
@@ -750,16 +816,23 @@ constexpr size_t SMEM_LIMIT = 227 * 1024;
 
 size_t halo_smem(HaloConv &h, int bba, int bbb) {
   const int taps = h.Kh * h.Kw;
-  h.WP = h.P + h.Kw - 1;
-  h.RH = h.R + h.Kh - 1;
-  h.nh_blocks = h.RH * h.WP * h.G * CGC;
+  // stride 2: the halo's even and odd input columns are staged as two
+  // phases, so tap v reads phase v % 2 from position v / 2 on
+  h.WP = h.S == 1 ? h.P + h.Kw - 1 : h.P + (h.Kw - 1) / 2;
+  h.NPH = (h.S == 2 && h.Kw > 1) ? 2 : 1;
+  h.RH = h.S * (h.R - 1) + h.Kh;
+  h.PHP = h.RH * h.WP;
+  if (h.NPH > 1)   // each phase's packed box must start 128-byte aligned
+    while ((h.PHP * h.G * CGC * bba) % 128) ++h.PHP;
+  h.nh_blocks = h.NPH * h.PHP * h.G * CGC;
   h.nb_blocks = taps * h.NB * CGC;
   h.dec_b_off = (uint32_t)h.nh_blocks * 128;
   h.dec_stage = (uint32_t)(h.nh_blocks + h.nb_blocks) * 128;
   h.pk_b_off = (uint32_t)((h.nh_blocks * bba + 127) / 128 * 128);
-  h.pk_bytes = (uint32_t)(h.nh_blocks * bba + h.nb_blocks * bbb);
+  // bytes the boxes deliver per chunk (the phase padding is not written)
+  h.pk_bytes = (uint32_t)(h.NPH * h.RH * h.WP * h.G * CGC * bba + h.nb_blocks * bbb);
   h.pk_stage = (uint32_t)((h.pk_b_off + h.nb_blocks * bbb + 127) / 128 * 128);
-  h.sc_bytes = (uint32_t)(h.RH * h.WP * h.G * h.CGin);
+  h.sc_bytes = (uint32_t)(h.NPH * h.PHP * h.G * h.CGin);
   h.scw_off = (h.sc_bytes + 15) / 16 * 16;
   const uint32_t scw = h.op == OP_FWD ? (uint32_t)(taps * h.NB * h.CIG) : (uint32_t)(taps * h.COG * h.NB);
   h.sc_stride = (h.scw_off + scw + 127) / 128 * 128;
@@ -793,8 +866,11 @@ int pow2_at_least32(int x) {
 // uses the generic kernel).
 bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
   std::memset(&h, 0, sizeof(h));
-  if (cp.stride != 1 || (cp.op != OP_FWD && cp.op != OP_DGRAD)) return false;
+  if (cp.op != OP_FWD && cp.op != OP_DGRAD) return false;
+  // stride 2 (forward only) reads the input through a [H][W/2][2] view
+  if (cp.stride != 1 && !(cp.stride == 2 && cp.op == OP_FWD && cp.W % 2 == 0)) return false;
   h.op = cp.op;
+  h.S = cp.stride;
   h.N = cp.N;
   h.NG = cp.NG;
   h.Kh = cp.Kh;
@@ -844,14 +920,17 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
   // below the peak rate and duplicate the halo decode across column tiles)
   const int bn_min = std::min(bn_max, 128);
   for (int BN = bn_max; BN >= bn_min; BN = BN > bn_min ? std::max(bn_min, BN / 2 / 16 * 16) : 0) {
-    for (int R = 4; R >= 1; --R) {
+    for (int cand = 0; cand < 8; ++cand) {
+      const int R = 4 - (cand >> 1);
       HaloConv c = h;
       c.BN = BN;
       c.NB = BN / 8;
       c.acc_cols = pow2_at_least32(BN);
-      // two accumulator sets, so one tile's epilogue overlaps the next tile's MMAs
-      c.nbuf = 2 * c.acc_cols <= 512 ? 2 : 1;
+      // two accumulator sets, so one tile's epilogue overlaps the next
+      // tile's MMAs; one set when that lets a taller tile fit the TMEM
+      c.nbuf = (cand & 1) ? 1 : 2;
       if (R > h.Hout || R * c.nbuf > MAX_R || R * c.nbuf * c.acc_cols > 512) continue;
+      if (R > 1 && h.Kh < h.S) continue;   // the halo rows between output rows would go unused
       c.R = R;
       const size_t sm = halo_smem(c, bba, bbb);
       if (!sm) continue;
@@ -865,7 +944,11 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
       const double chunk_t = std::max((double)R * taps * mma, 5.0 * (c.nh_blocks + c.nb_blocks));
       const double tile_t = (h.nchunks + 2.0) * chunk_t;
       const double rounds = (double)((tiles + num_sms - 1) / num_sms);
-      const double cost = rounds * tile_t;
+      // with one accumulator set the epilogue of every tile but the last
+      // (about 12 cycles per accumulator column and output row) is no
+      // longer hidden behind the next tile's MMAs
+      const double epi_t = 12.0 * BN * R;
+      const double cost = rounds * tile_t + (c.nbuf == 1 ? rounds - 1.0 : 0.0) * epi_t;
       if (cost < best_cost * 0.98) {
         best_cost = cost;
         best_h = c;
@@ -935,10 +1018,18 @@ cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStre
   // input codes [Hin][Win][NG][CGin * BBA] as 8-byte units; box: one chunk's
   // channel groups x G batch groups x WP positions x RH rows
   CUtensorMap ma, mb;
-  {
+  if (h.S == 1) {
     const uint64_t d[4] = {(uint64_t)h.CGin * bba / 8, (uint64_t)h.NG, (uint64_t)h.Win, (uint64_t)h.Hin};
     const uint32_t bx[4] = {(uint32_t)(CGC * bba / 8), (uint32_t)h.G, (uint32_t)h.WP, (uint32_t)h.RH};
     if (!make_tensor_map(&ma, cp.a.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
+  } else {
+    // stride 2: the same codes as [Hin][Win / 2][2 (column parity)][NG][..];
+    // a box holds one column phase
+    const uint64_t pos = (uint64_t)h.NG * h.CGin * bba;
+    const uint64_t d[5] = {(uint64_t)h.CGin * bba / 8, (uint64_t)h.NG, 2, (uint64_t)h.Win / 2, (uint64_t)h.Hin};
+    const uint64_t gs[4] = {(uint64_t)h.CGin * bba, pos, 2 * pos, (uint64_t)h.Win * pos};
+    const uint32_t bx[5] = {(uint32_t)(CGC * bba / 8), (uint32_t)h.G, 1u, (uint32_t)h.WP, (uint32_t)h.RH};
+    if (!make_tensor_map_strided(&ma, cp.a.codes, 8, 5, d, gs, bx)) return cudaErrorInvalidValue;
   }
   {
     // weights [taps][COG][CIG * BBB]
@@ -977,14 +1068,19 @@ cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStre
 namespace {
 
 size_t wgrad_smem(HaloWgrad &h, int bba, int bbb) {
-  h.WP = h.P + h.Kw - 1;
+  h.WP = h.S == 1 ? h.P + h.Kw - 1 : h.P + (h.Kw - 1) / 2;
+  h.NPH = (h.S == 2 && h.Kw > 1) ? 2 : 1;
+  h.PHP = h.WP;
+  if (h.NPH > 1)   // each phase's packed box must start 128-byte aligned
+    while ((h.PHP * h.G * h.CB * bbb) % 128) ++h.PHP;
   h.na_blocks = h.KG * 16;
-  h.nb_blocks = h.WP * h.G * h.CB;
+  h.nb_blocks = h.NPH * h.PHP * h.G * h.CB;
   h.dec_b_off = (uint32_t)h.na_blocks * 128;
   h.dec_stage = (uint32_t)(h.na_blocks + h.nb_blocks) * 128;
   h.pk_b_off = (uint32_t)((h.na_blocks * bba + 127) / 128 * 128);
   h.pk_sc_off = (uint32_t)((h.pk_b_off + h.nb_blocks * bbb + 127) / 128 * 128);
-  h.pk_bytes = (uint32_t)(h.na_blocks * bba + h.nb_blocks * bbb);
+  // bytes the boxes deliver per chunk (the phase padding is not written)
+  h.pk_bytes = (uint32_t)(h.na_blocks * bba + h.NPH * h.WP * h.G * h.CB * bbb);
   h.pk_stage = (uint32_t)((h.pk_sc_off + h.na_blocks + h.nb_blocks + 127) / 128 * 128);
   const size_t fixed = 1024 + (size_t)DSTAGES * h.dec_stage + sizeof(WgCtl) + 128;
   if (fixed + 2 * (size_t)h.pk_stage > SMEM_LIMIT) return 0;
@@ -1001,7 +1097,10 @@ constexpr int WG_TARGET_CTAS = 148;   // split-K sized for one wave on a 148-SM 
 
 bool halo_wgrad_plan(const ConvParams &cp, HaloWgrad &h, int max_splits) {
   std::memset(&h, 0, sizeof(h));
-  if (cp.op != OP_WGRAD || cp.stride != 1) return false;
+  if (cp.op != OP_WGRAD) return false;
+  // stride 2 reads X through a [H][W/2][2] view
+  if (cp.stride != 1 && !(cp.stride == 2 && cp.W % 2 == 0)) return false;
+  h.S = cp.stride;
   h.N = cp.N; h.NG = cp.NG; h.H = cp.H; h.W = cp.W; h.Ho = cp.Ho; h.Wo = cp.Wo;
   h.Cin = cp.Cin; h.Cout = cp.Cout; h.CIG = cp.CIG; h.COG = cp.COG;
   h.Kh = cp.Kh; h.Kw = cp.Kw; h.pad = cp.pad;
@@ -1022,7 +1121,7 @@ bool halo_wgrad_plan(const ConvParams &cp, HaloWgrad &h, int max_splits) {
   if (best < 0) return false;
   h.P = best;
   h.G = 16 / best;
-  h.KG = 16;
+  h.KG = 16;   // the MMA issue loop is unrolled for K = 128 per chunk
   const int bba = block_bytes(cp.a.fmt), bbb = block_bytes(cp.b.fmt);
   h.BNc = std::min(128, (h.Cin + 15) / 16 * 16);
   for (;;) {
@@ -1068,11 +1167,19 @@ cudaError_t halo_wgrad_launch(const ConvParams &cp, HaloWgrad &h, int num_sms, c
     const uint32_t bx[4] = {(uint32_t)(16 * bba / 8), (uint32_t)h.G, (uint32_t)h.P, 1u};
     if (!make_tensor_map(&ma, cp.a.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
   }
-  {
+  if (h.S == 1) {
     // X codes [H][W][NG][CIG * BBB]; box: CB channel groups x G x WP x 1 row
     const uint64_t d[4] = {(uint64_t)h.CIG * bbb / 8, (uint64_t)h.NG, (uint64_t)h.W, (uint64_t)h.H};
     const uint32_t bx[4] = {(uint32_t)(h.CB * bbb / 8), (uint32_t)h.G, (uint32_t)h.WP, 1u};
     if (!make_tensor_map(&mb, cp.b.codes, 8, 4, d, bx)) return cudaErrorInvalidValue;
+  } else {
+    // stride 2: X as [H][W / 2][2 (column parity)][NG][..]; a box holds one
+    // column phase of one row
+    const uint64_t pos = (uint64_t)h.NG * h.CIG * bbb;
+    const uint64_t d[5] = {(uint64_t)h.CIG * bbb / 8, (uint64_t)h.NG, 2, (uint64_t)h.W / 2, (uint64_t)h.H};
+    const uint64_t gs[4] = {(uint64_t)h.CIG * bbb, pos, 2 * pos, (uint64_t)h.W * pos};
+    const uint32_t bx[5] = {(uint32_t)(h.CB * bbb / 8), (uint32_t)h.G, 1u, (uint32_t)h.WP, 1u};
+    if (!make_tensor_map_strided(&mb, cp.b.codes, 8, 5, d, gs, bx)) return cudaErrorInvalidValue;
   }
   const int grid = std::min(h.num_tiles, num_sms);
   auto go = [&](auto kern) -> cudaError_t {

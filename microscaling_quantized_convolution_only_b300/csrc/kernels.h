@@ -65,7 +65,12 @@ struct HaloConv {
   int Hin, Win, CGin;            // correlation input (fwd: X; dgrad: dY) and its channel groups (K)
   int Hout, Wout, NC, NCG;       // output dims and channels (fwd: Ho, Wo, Cout; dgrad: H, W, Cin)
   int Kh, Kw, padh, padw;        // taps and padding of the correlation (dgrad: K - 1 - pad)
-  int P, G, R, WP, RH;           // tile: positions, batch groups, output rows; halo width / height
+  int P, G, R, WP, RH;           // tile: positions, batch groups, output rows; halo width (per
+                                 // column phase) / height
+  int S, NPH;                    // stride; halo column phases (stride 2: even / odd input columns
+                                 // staged apart, so every tap reads unit-stride halo positions)
+  int PHP;                       // halo positions per phase: RH * WP, padded so that every phase's
+                                 // packed box starts 128-byte aligned
   int nbuf;                      // accumulator sets (tiles in flight between MMA and epilogue)
   int BN, NB, acc_cols;          // output channels per tile, their groups, TMEM columns per row
   int nchunks;                   // CGin / 2
@@ -94,7 +99,9 @@ struct HaloConv {
 // chunks and writes one split-K partial.
 struct HaloWgrad {
   int N, NG, H, W, Ho, Wo, Cin, Cout, CIG, COG, Kh, Kw, pad;
-  int P, G, KG, WP;              // chunk: P positions x G batch groups = KG k-groups (K = 8 KG)
+  int P, G, KG, WP;              // chunk: P positions x G batch groups = KG k-groups (K = 8 KG);
+                                 // X halo width per column phase
+  int S, NPH, PHP;               // stride; X halo column phases and positions per phase (as in HaloConv)
   int BNc, CB, acc_cols;         // input channels per tile, their groups, TMEM columns per tap
   int m_tiles, c_tiles, splits, chunks_per_split, total_chunks;
   int tiles_w, tiles_g;
@@ -122,6 +129,9 @@ cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStre
 // esize bytes) with box `box`, zero fill outside; `map` is a 64-byte aligned
 // CUtensorMap.  False if the driver entry point or the encode fails.
 bool make_tensor_map(void *map, const void *base, int esize, int rank, const uint64_t *dims, const uint32_t *box);
+// The same with explicit byte strides of dims 1 .. rank-1 (multiples of 16).
+bool make_tensor_map_strided(void *map, const void *base, int esize, int rank, const uint64_t *dims,
+                             const uint64_t *strides, const uint32_t *box);
 
 cudaError_t launch_amax(const void *src, int dtype, int64_t n, uint32_t *amax_bits, int num_sms, cudaStream_t s);
 cudaError_t launch_quantize(const void *src, int dtype, int layout, int fmt, const QuantParams &p, int num_sms,

@@ -25,6 +25,12 @@ SMALL = [
     Layer(24, 48, 4, 6, 40, 3, 1, 1),     # ragged channels vs tile widths
     Layer(8, 16, 7, 7, 272, 3, 1, 1),     # more than 256 output channels
     Layer(8, 264, 3, 3, 16, 3, 2, 1),     # more than 256 input channels
+    Layer(8, 16, 9, 8, 32, 3, 2, 1),      # stride 2, even width (halo column phases), ragged rows
+    Layer(16, 32, 10, 14, 48, 3, 2, 1),   # stride 2, two channel chunks, ragged positions
+    Layer(8, 32, 12, 12, 24, 1, 2, 0),    # 1x1 stride 2 through the halo path
+    Layer(8, 16, 8, 6, 16, 3, 2, 0),      # stride 2 without padding
+    Layer(24, 16, 14, 10, 136, 3, 2, 1),  # stride 2, three batch groups, two output-channel tiles
+    Layer(8, 16, 11, 12, 16, 5, 2, 2),    # 5x5 stride 2 (three taps per column phase)
 ]
 
 

@@ -27,6 +27,7 @@ LAYERS = [
     Layer(8, 16, 9, 7, 32, 3, 2, 1),      # generic kernel (stride 2)
     Layer(8, 24, 10, 10, 16, 1, 2, 0),    # generic kernel (1x1 stride 2)
     Layer(32, 64, 12, 12, 64, 3, 1, 1),   # halo kernel, several tiles
+    Layer(16, 32, 10, 14, 48, 3, 2, 1),   # halo kernel, stride 2
 ]
 
 
