@@ -36,7 +36,10 @@
 // (tcgen05.ld; warps w and w+4 share TMEM lane quadrant w % 4 and take
 // alternate 16-column chunks) into fp32 HWCN outputs or requantized CBF
 // blocks, warp 16 copies block scales and issues the TMA loads (lane 0),
-// warp 17 lane 0 issues tcgen05.mma.  Every wait is
+// lane 0 of warps 17 and 18 issue tcgen05.mma (the conv kernel splits the
+// output rows between the two issuers: the issue loop of one thread, not
+// the tensor pipe, bounds the MMA rate of a single issuer here; the
+// weight-gradient kernel has one).  Every wait is
 // bounded; on expiry the CTA records MQ_ERR_TIMEOUT, stops, lets its copies
 // and MMAs in flight finish and frees its TMEM.
 #include <cuda.h>
@@ -60,6 +63,10 @@ constexpr int HC_EPI_WARPS = 8;   // two per TMEM lane quadrant, alternating 16-
 constexpr int HC_TMA_WARP = 16;
 constexpr int HC_MMA_WARP = 17;
 constexpr int HC_THREADS = 18 * 32;
+// the conv kernel has a second MMA-issuing warp: output rows are split
+// between the two issuers, so their issue loops run side by side
+constexpr int HC_MMA_WARP2 = 18;
+constexpr int HC_CONV_THREADS = 19 * 32;
 constexpr int HC_DEC_THREADS = HC_DEC_WARPS * 32;
 constexpr int CGC = 2;          // channel groups (8 channels each) per chunk: K = 16 per tap
 constexpr int DSTAGES = 2;      // decoded ring depth
@@ -154,7 +161,7 @@ __device__ __forceinline__ void hc_requant16(const HaloConv &p, const float (&y)
 // FA: format of the input blocks (X or dY), FB: of the weights, FR: format of
 // the fused requantization of the output (0 = none).
 template <int OP, int FA, int FB, int FR>
-__global__ void __launch_bounds__(HC_THREADS, 1)
+__global__ void __launch_bounds__(HC_CONV_THREADS, 1)
     halo_conv_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_w,
                      const HaloConv p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -170,7 +177,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
     }
     for (int s = 0; s < DSTAGES; ++s) {
       mbar_init(&ctl->dfull[s], HC_DEC_WARPS);
-      mbar_init(&ctl->dempty[s], 1);
+      mbar_init(&ctl->dempty[s], p.R >= 2 ? 2 : 1);   // one commit per issuer
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl->sfull[s], 64);
@@ -180,7 +187,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
       mbar_init(&ctl->acc_full[s], 1);
       mbar_init(&ctl->acc_empty[s], HC_EPI_WARPS);
     }
-    mbar_init(&ctl->done, 1);
+    mbar_init(&ctl->done, p.R >= 2 ? 2 : 1);
     ctl->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -341,9 +348,13 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
         if (lane == 0) mbar_arrive(&ctl->sempty[tb]);
       }
     }
-  } else if (warp == HC_MMA_WARP) {
-    // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+  } else if (warp == HC_MMA_WARP || warp == HC_MMA_WARP2) {
+    // ---------------------------------------------------------- MMA issuers
+    // issuer i (lane 0 of warp HC_MMA_WARP + i) takes the output rows
+    // s = i, i + NI, ...; both wait for each decoded stage and each commits
+    // its MMAs to the stage's release barrier (count NI)
+    const int issuer = warp - HC_MMA_WARP, NI = p.R >= 2 ? 2 : 1;
+    if (lane == 0 && issuer < NI) {
       const uint32_t idesc = idesc_f16(128, p.BN, false, OP == OP_DGRAD);
       // Descriptor words: the high word (stride fields, version) is fixed;
       // the low word holds (address >> 4) in bits 0-13, so moving an operand
@@ -382,7 +393,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
           const uint32_t a_stage = (uint32_t)a_desc + (uint32_t)ds * d_stage;
           const uint32_t b_stage = (uint32_t)b_desc + (uint32_t)ds * d_stage;
           const int buf = k % p.nbuf, use = k / p.nbuf;
-          for (int s = 0; s < p.R && ok; ++s) {
+          for (int s = issuer; s < p.R && ok; s += NI) {
             const int slot = buf * p.R + s;
             if (c == 0) {
               if (!hc_wait(&ctl->acc_empty[slot], (use & 1) ^ 1, p, ctl)) { ok = false; break; }
@@ -979,7 +990,7 @@ cudaError_t hc_launch(const CUtensorMap &a, const CUtensorMap &b, const HaloConv
   auto k = halo_conv_kernel<OP, FA, FB, FR>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, HC_THREADS, h.smem, st>>>(a, b, h);
+  k<<<grid, HC_CONV_THREADS, h.smem, st>>>(a, b, h);
   return cudaGetLastError();
 }
 
