@@ -38,6 +38,15 @@ template <> struct Fmt<8> {   // E4M3 element (8-bit variant)
   static constexpr uint32_t SBIT = 0x80, MAG = 0x7F;
 };
 
+// (a0 * b, a1 * b), each rounded to nearest even: one packed f32x2 multiply
+__device__ __forceinline__ void mul2(float a0, float a1, float b, float &d0, float &d1) {
+  uint64_t a, bb, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(b));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(bb));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+
 // Two fp32 -> two codes, round-to-nearest-even, saturating.  The returned
 // value holds the code of `lo` in its low container (low nibble for E2M1,
 // low byte for E2M3/E4M3) and the code of `hi` in the next one.
@@ -430,20 +439,35 @@ __device__ __forceinline__ uint32_t fix_pair(uint32_t lo, uint32_t hi, float v0,
   return pair;
 }
 
-template <int F>
-__device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs, float s_t, float inv_lo, float inv_hi) {
+// four code pairs (containers as cvt2 returns them) -> one packed row
+template <int F> __device__ __forceinline__ uint64_t place_row(const uint32_t (&pr)[4]) {
   uint64_t bits = 0;
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
-    const uint32_t lo = cvt2<F>(v[2 * jj] * inv_lo, v[2 * jj + 1] * inv_lo);
-    const uint32_t hi = cvt2<F>(v[2 * jj] * inv_hi, v[2 * jj + 1] * inv_hi);
-    uint32_t pair = lo;
-    if (lo != hi) pair = fix_pair<F>(lo, hi, v[2 * jj], v[2 * jj + 1], bs, s_t);
-    if (F == 4) bits |= (uint64_t)pair << (8 * jj);                                    // two nibbles
-    else if (F == 8) bits |= (uint64_t)pair << (16 * jj);                              // two bytes
-    else bits |= (uint64_t)((pair & 0x3Fu) | ((pair >> 8) << 6)) << (12 * jj);          // two 6-bit codes
+    if (F == 4) bits |= (uint64_t)pr[jj] << (8 * jj);                                  // two nibbles
+    else if (F == 8) bits |= (uint64_t)pr[jj] << (16 * jj);                            // two bytes
+    else bits |= (uint64_t)((pr[jj] & 0x3Fu) | ((pr[jj] >> 8) << 6)) << (12 * jj);     // two 6-bit codes
   }
   return bits;
+}
+
+template <int F>
+__device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs, float s_t, float inv_lo, float inv_hi) {
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    float l0, l1, h0, h1;
+    mul2(v[2 * jj], v[2 * jj + 1], inv_lo, l0, l1);
+    mul2(v[2 * jj], v[2 * jj + 1], inv_hi, h0, h1);
+    lo[jj] = cvt2<F>(l0, l1);
+    hi[jj] = cvt2<F>(h0, h1);
+  }
+  const uint64_t row_lo = place_row<F>(lo);
+  if (row_lo == place_row<F>(hi)) return row_lo;   // the common case: no element near a midpoint
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj)
+    if (lo[jj] != hi[jj]) lo[jj] = fix_pair<F>(lo[jj], hi[jj], v[2 * jj], v[2 * jj + 1], bs, s_t);
+  return place_row<F>(lo);
 }
 
 // store one packed row (8 codes) at byte offset 4r / 6r / 8r of its block

@@ -28,9 +28,10 @@
 //
 // GEMM per tile: rows = (output row s, position p, batch group j, n), columns
 // = output channels (BN), K = (chunk, tap, 16 channels).  One accumulator of
-// 128 x BN fp32 per output row s lives in TMEM, in two sets (2 R BN <= 512
-// columns) used by alternate tiles, so the epilogue of one tile overlaps the
-// MMAs of the next.
+// 128 x BN fp32 per output row s lives in TMEM, in a ring of NS slots that
+// fills the TMEM: row s of the k-th tile uses slot (k R + s) % NS, so while
+// the epilogue drains one tile the next tile's rows already accumulate in
+// the spare slots and in the slots drained first.
 //
 // Warp roles: warps 0-7 decode, warps 8-15 drain the accumulators
 // (tcgen05.ld; warps w and w+4 share TMEM lane quadrant w % 4 and take
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
       mbar_init(&ctl->sfull[s], 64);
       mbar_init(&ctl->sempty[s], HC_DEC_WARPS);
     }
-    for (int s = 0; s < p.R * p.nbuf; ++s) {
+    for (int s = 0; s < p.NS; ++s) {
       mbar_init(&ctl->acc_full[s], 1);
       mbar_init(&ctl->acc_empty[s], HC_EPI_WARPS);
     }
@@ -392,9 +393,9 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
           tc_fence_after();
           const uint32_t a_stage = (uint32_t)a_desc + (uint32_t)ds * d_stage;
           const uint32_t b_stage = (uint32_t)b_desc + (uint32_t)ds * d_stage;
-          const int buf = k % p.nbuf, use = k / p.nbuf;
           for (int s = issuer; s < p.R && ok; s += NI) {
-            const int slot = buf * p.R + s;
+            // accumulator ring: row s of the k-th tile uses slot (k R + s) % NS
+            const int ring = k * p.R + s, slot = ring % p.NS, use = ring / p.NS;
             if (c == 0) {
               if (!hc_wait(&ctl->acc_empty[slot], (use & 1) ^ 1, p, ctl)) { ok = false; break; }
               tc_fence_after();
@@ -443,9 +444,8 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
       const TileCoord tc = hc_tile(p, t);
       const int wo = tc.w0 + pp, ng = tc.g0 + j, n = ng * 8 + n_in;
       bool stop = false;
-      const int buf = k % p.nbuf, use = k / p.nbuf;
       for (int s = 0; s < p.R; ++s) {
-        const int slot = buf * p.R + s;
+        const int ring = k * p.R + s, slot = ring % p.NS, use = ring / p.NS;
         if (!hc_wait(&ctl->acc_full[slot], use & 1, p, ctl)) { stop = true; break; }
         tc_fence_after();
         const int ho = tc.h0 + s;
@@ -931,16 +931,16 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
   // below the peak rate and duplicate the halo decode across column tiles)
   const int bn_min = std::min(bn_max, 128);
   for (int BN = bn_max; BN >= bn_min; BN = BN > bn_min ? std::max(bn_min, BN / 2 / 16 * 16) : 0) {
-    for (int cand = 0; cand < 8; ++cand) {
-      const int R = 4 - (cand >> 1);
+    for (int R = 4; R >= 1; --R) {
       HaloConv c = h;
       c.BN = BN;
       c.NB = BN / 8;
       c.acc_cols = pow2_at_least32(BN);
-      // two accumulator sets, so one tile's epilogue overlaps the next
-      // tile's MMAs; one set when that lets a taller tile fit the TMEM
-      c.nbuf = (cand & 1) ? 1 : 2;
-      if (R > h.Hout || R * c.nbuf > MAX_R || R * c.nbuf * c.acc_cols > 512) continue;
+      // accumulator ring of NS slots (all of the TMEM): rows of successive
+      // tiles take successive slots, so the NS - R slots beyond a tile's own
+      // let the next tile's MMAs start while the epilogue drains this one
+      c.NS = std::min(MAX_R, 512 / c.acc_cols);
+      if (R > h.Hout || R > c.NS) continue;
       if (R > 1 && h.Kh < h.S) continue;   // the halo rows between output rows would go unused
       c.R = R;
       const size_t sm = halo_smem(c, bba, bbb);
@@ -948,18 +948,21 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
       c.smem = sm;
       const int64_t tiles = (int64_t)(h.NG / h.G) * ((h.Wout + h.P - 1) / h.P) * ((h.Hout + R - 1) / R) *
                             ((h.NC + BN - 1) / BN);
-      // per chunk the MMAs and the decode of its halo + weight blocks overlap;
-      // measured in this kernel: ~2x the isolated MMA cost, ~5 cycles per
-      // decoded block (8 decode warps)
+      // per chunk the MMAs and the decode of its halo + weight blocks
+      // overlap; measured in this kernel (two issuers, 8 decode warps):
+      // ~2x the isolated MMA cost and ~7.7 cycles per decoded block
       const double mma = 2.0 * std::max(BN / 2.0, BN == 64 ? 48.0 : 40.0);
-      const double chunk_t = std::max((double)R * taps * mma, 5.0 * (c.nh_blocks + c.nb_blocks));
+      const double chunk_t = std::max((double)R * taps * mma, 7.7 * (c.nh_blocks + c.nb_blocks));
       const double tile_t = (h.nchunks + 2.0) * chunk_t;
       const double rounds = (double)((tiles + num_sms - 1) / num_sms);
-      // with one accumulator set the epilogue of every tile but the last
-      // (about 12 cycles per accumulator column and output row) is no
-      // longer hidden behind the next tile's MMAs
-      const double epi_t = 12.0 * BN * R;
-      const double cost = rounds * tile_t + (c.nbuf == 1 ? rounds - 1.0 : 0.0) * epi_t;
+      // the epilogue of a tile (measured: ~8.5 cycles per accumulator
+      // column and row with fp32 output, ~40 with the requantizing
+      // epilogue) is hidden behind the next tile's MMAs as far as the ring
+      // has spare slots for that tile's rows
+      const double epi_t = (cp.rq.codes ? 40.0 : 8.5) * BN * R;
+      const int spare = c.NS - R;
+      const double exposed = spare >= R ? 0.0 : 1.0 - (double)spare / R;
+      const double cost = rounds * tile_t + (rounds - 1.0) * exposed * epi_t;
       if (cost < best_cost * 0.98) {
         best_cost = cost;
         best_h = c;

@@ -71,7 +71,7 @@ struct HaloConv {
                                  // staged apart, so every tap reads unit-stride halo positions)
   int PHP;                       // halo positions per phase: RH * WP, padded so that every phase's
                                  // packed box starts 128-byte aligned
-  int nbuf;                      // accumulator sets (tiles in flight between MMA and epilogue)
+  int NS;                        // accumulator slots (TMEM ring; row s of tile k uses slot (k R + s) % NS)
   int BN, NB, acc_cols;          // output channels per tile, their groups, TMEM columns per row
   int nchunks;                   // CGin / 2
   int tiles_g, tiles_w, tiles_h, tiles_n, num_tiles;
