@@ -125,36 +125,68 @@ __device__ __forceinline__ TileCoord hc_tile(const HaloConv &p, int t) {
   return c;
 }
 
-// Requantize 16 fp32 columns of one row into two blocks of the next layer's
-// activations (see quantize.cu for the rounding).  Lanes 8q..8q+7 hold the
-// eight batch rows of one block; the block amax is their shuffle-max.
-template <int F>
-__device__ __forceinline__ void hc_requant16(const HaloConv &p, const float (&y)[16], int64_t blk_pos_ng, int n_in,
-                                             int co0, bool row_ok, float s_t, float inv_den, uint32_t &amax_acc) {
+// Requantize 8 NBK fp32 columns of one row into NBK blocks of the next
+// layer's activations (see quantize.cu for the rounding).  Lanes 8q..8q+7
+// hold the eight batch rows of one block; the block amax is their
+// shuffle-max.  The blocks are processed side by side (independent chains
+// for the shuffles, the scale rounding and the encoding).
+template <int F, int NBK>
+__device__ __forceinline__ void hc_requant(const HaloConv &p, const float *y, int64_t blk_pos_ng, int n_in, int co0,
+                                           bool row_ok, float s_t, float inv_den, uint32_t &amax_acc) {
+  uint32_t m[NBK];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NBK; ++h) {
+    uint32_t mm = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mm = max(mm, __float_as_uint(y[8 * h + j]) & 0x7FFFFFFFu);
+    m[h] = (row_ok && co0 + 8 * h < p.NC) ? mm : 0u;
+  }
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+    for (int h = 0; h < NBK; ++h) m[h] = max(m[h], __shfl_xor_sync(0xFFFFFFFFu, m[h], o));
+#pragma unroll
+  for (int h = 0; h < NBK; ++h) {
+    amax_acc = max(amax_acc, m[h]);
     const int co = co0 + 8 * h;
-    float v[8];
-    uint32_t m = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      v[j] = y[8 * h + j];
-      m = max(m, __float_as_uint(v[j]) & 0x7FFFFFFFu);
-    }
-    if (!row_ok || co >= p.NC) m = 0;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    amax_acc = max(amax_acc, m);
-    if (!row_ok || co >= p.NC) continue;
-    const uint32_t bsc = block_scale_code_r<F>(__uint_as_float(m), s_t, inv_den);
+    const uint32_t bsc = block_scale_code_r<F>(__uint_as_float(m[h]), s_t, inv_den);
     const float bs = code_value<8>(bsc);
     float inv_lo, inv_hi;
     quot_bracket(bs, s_t, inv_lo, inv_hi);
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = y[8 * h + j];
     const uint64_t bits = encode_row8_b<F>(v, bs, s_t, inv_lo, inv_hi);
-    const int64_t blk = blk_pos_ng + co / 8;
-    store_row8<F>(p.rq.codes + blk * Fmt<F>::BLOCK_BYTES, n_in, bits);
-    if (n_in == 0) p.rq.scales[blk] = (uint8_t)bsc;
+    if (row_ok && co < p.NC) {
+      const int64_t blk = blk_pos_ng + co / 8;
+      store_row8<F>(p.rq.codes + blk * Fmt<F>::BLOCK_BYTES, n_in, bits);
+      if (n_in == 0) p.rq.scales[blk] = (uint8_t)bsc;
+    }
   }
+}
+
+// One accumulator row chunk of W columns (W = 16 or 32) starting at column
+// c0: scaled fp32 HWCN stores and / or the fused requantization.
+template <int FR, int W>
+__device__ __forceinline__ void hc_epi_chunk(const HaloConv &p, uint32_t taddr, float f, int64_t obase,
+                                             int64_t rq_blk, int n_in, int co0, bool valid, float rq_st,
+                                             float rq_inv, uint32_t &amax_acc) {
+  float y[W];
+  {
+    uint32_t r[W];
+    if constexpr (W == 32) tmem_ld32(taddr, r);
+    else tmem_ld16(taddr, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int jj = 0; jj < W; jj += 2) mul2(__uint_as_float(r[jj]), __uint_as_float(r[jj + 1]), f, y[jj], y[jj + 1]);
+  }
+  if (p.out && valid) {
+    float *o = p.out + obase + (int64_t)co0 * p.N;
+#pragma unroll
+    for (int jj = 0; jj < W; ++jj)
+      if (co0 + jj < p.NC) o[(int64_t)jj * p.N] = y[jj];
+  }
+  if constexpr (FR != 0) hc_requant<FR, W / 8>(p, y, rq_blk, n_in, co0, valid, rq_st, rq_inv, amax_acc);
 }
 
 }  // namespace
@@ -454,21 +486,15 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
         const int64_t obase = pos * p.NC * (int64_t)p.N + n;
         const int64_t rq_blk = (pos * p.NG + ng) * p.NCG;
         const uint32_t tb = tmem + slot * p.acc_cols + ((uint32_t)(q * 32) << 16);
-        for (int c0 = 16 * half; c0 < p.BN; c0 += 32) {
-          uint32_t r[16];
-          tmem_ld16(tb + c0, r);
-          tmem_wait_ld();
-          float y[16];
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) y[jj] = __uint_as_float(r[jj]) * f;
-          const int co0 = tc.n0 + c0;
-          if (p.out && valid) {
-            float *o = p.out + obase + (int64_t)co0 * p.N;
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              if (co0 + jj < p.NC) o[(int64_t)jj * p.N] = y[jj];
-          }
-          if (FR) hc_requant16<FR ? FR : 4>(p, y, rq_blk, n_in, co0, valid, rq_st, rq_inv, amax_acc);
+        // the two warps of a lane quadrant take alternate column chunks: 32
+        // columns (four blocks side by side) for a requantize-only epilogue
+        // when BN is a multiple of 64, else 16
+        if (FR != 0 && !p.out && p.BN % 64 == 0) {
+          for (int c0 = 32 * half; c0 < p.BN; c0 += 64)
+            hc_epi_chunk<FR, 32>(p, tb + c0, f, obase, rq_blk, n_in, tc.n0 + c0, valid, rq_st, rq_inv, amax_acc);
+        } else {
+          for (int c0 = 16 * half; c0 < p.BN; c0 += 32)
+            hc_epi_chunk<FR, 16>(p, tb + c0, f, obase, rq_blk, n_in, tc.n0 + c0, valid, rq_st, rq_inv, amax_acc);
         }
         tc_fence_before();
         __syncwarp();
