@@ -410,11 +410,16 @@ namespace mq {
 // T_scale s_t: exact RN of the real quotient x / (bs * s_t) with the bracket
 // and fma-sign tie test of resolve_tie.  Returns the packed row: element j at
 // bits 4j (E2M1), 6j (E2M3) or 8j (E4M3).
-// Bracket multipliers of the quotient x / (bs * s_t) (0 when bs is 0).
+// Bracket multipliers of the quotient x / (bs * s_t) (0 when bs is 0).  The
+// reciprocal is the hardware approximation (relative error below 2^-22);
+// with the product bs * s_t and the three later roundings (each 2^-24) the
+// computed ends still lie below and above the exact quotient, since the
+// bracket half-width is 2^-20.
 __device__ __forceinline__ void quot_bracket(float bs, float s_t, float &inv_lo, float &inv_hi) {
   inv_lo = inv_hi = 0.0f;
   if (bs > 0.0f) {
-    const float inv = __frcp_rn(bs * s_t);
+    float inv;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(inv) : "f"(bs * s_t));
     inv_lo = inv * (1.0f - QEPS);
     inv_hi = inv * (1.0f + QEPS);
   }

@@ -527,6 +527,17 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
 // both once; tap kw reads the halo through a descriptor shifted by kw
 // positions.  Accumulator kw (128 x BNc fp32) sits at TMEM column kw * acc.
 // Both operands are MN-major: a block row is 8 channels of one batch element.
+// warp roles of the weight-gradient kernel: ten decoders (its two operands
+// are both decoded per chunk), eight epilogue warps, the TMA / scale
+// producer and the MMA issuer
+constexpr int WG_DEC_WARPS = 10;
+constexpr int WG_DEC_THREADS = WG_DEC_WARPS * 32;
+constexpr int WG_EPI_WARP0 = 10;
+constexpr int WG_EPI_WARPS = 8;
+constexpr int WG_TMA_WARP = 18;
+constexpr int WG_MMA_WARP = 19;
+constexpr int WG_THREADS = 20 * 32;
+
 struct WgCtl {
   uint64_t pfull[MAX_PS], pempty[MAX_PS];
   uint64_t dfull[DSTAGES], dempty[DSTAGES];
@@ -571,7 +582,7 @@ __device__ __forceinline__ bool wg_wait(uint64_t *bar, uint32_t parity, const Ha
 }
 
 template <int FA, int FB>
-__global__ void __launch_bounds__(HC_THREADS, 1)
+__global__ void __launch_bounds__(WG_THREADS, 1)
     halo_wgrad_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                       const HaloWgrad p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -583,25 +594,25 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.PS; ++s) {
       mbar_init(&ctl->pfull[s], 64);
-      mbar_init(&ctl->pempty[s], HC_DEC_WARPS);
+      mbar_init(&ctl->pempty[s], WG_DEC_WARPS);
     }
     for (int s = 0; s < DSTAGES; ++s) {
-      mbar_init(&ctl->dfull[s], HC_DEC_WARPS);
+      mbar_init(&ctl->dfull[s], WG_DEC_WARPS);
       mbar_init(&ctl->dempty[s], 1);
     }
     mbar_init(&ctl->acc_full, 1);
-    mbar_init(&ctl->acc_empty, HC_EPI_WARPS);
+    mbar_init(&ctl->acc_empty, WG_EPI_WARPS);
     mbar_init(&ctl->done, 1);
     ctl->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == HC_MMA_WARP) tmem_alloc(&ctl->tmem_base, 512);
+  if (warp == WG_MMA_WARP) tmem_alloc(&ctl->tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  if (warp == HC_TMA_WARP) {
+  if (warp == WG_TMA_WARP) {
     // ----------------------------------------------------------- producer
     // lane 0 issues the two code boxes, all lanes copy the chunk's block
     // scales asynchronously (zero where the block is out of range); 64
@@ -669,7 +680,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp < HC_DEC_WARPS) {
+  } else if (warp < WG_DEC_WARPS) {
     // ------------------------------------------------------------ decoders
     const int tid = threadIdx.x;
     int pit = 0;
@@ -684,7 +695,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
         const uint8_t *sc = pk + p.pk_sc_off;
         uint8_t *dec = smem + p.off_dec + ds * p.dec_stage;
         const int na = p.na_blocks * 8;
-        for (int i = tid; i < na; i += HC_DEC_THREADS) {
+        for (int i = tid; i < na; i += WG_DEC_THREADS) {
           const int blk = i >> 3, r = i & 7;
           const uint4 v = decode_raw<FA>(lds_row<FA>(pk + blk * BBA, r), scale_pair<FA>(sc[blk]));
           *reinterpret_cast<uint4 *>(dec + i * 16) = v;
@@ -692,7 +703,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
         const int nb = p.nb_blocks * 8;
         const uint8_t *pkb = pk + p.pk_b_off;
         uint8_t *decb = dec + p.dec_b_off;
-        for (int i = tid; i < nb; i += HC_DEC_THREADS) {
+        for (int i = tid; i < nb; i += WG_DEC_THREADS) {
           const int blk = i >> 3, r = i & 7;
           const uint4 v = decode_raw<FB>(lds_row<FB>(pkb + blk * BBB, r), scale_pair<FB>(sc[p.na_blocks + blk]));
           *reinterpret_cast<uint4 *>(decb + i * 16) = v;
@@ -705,7 +716,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
         }
       }
     }
-  } else if (warp == HC_MMA_WARP) {
+  } else if (warp == WG_MMA_WARP) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, p.BNc, true, true);
@@ -749,10 +760,10 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
       wg_wait(&ctl->done, 0, p, ctl);
     }
     __syncwarp();
-  } else if (warp >= HC_EPI_WARP0 && warp < HC_EPI_WARP0 + HC_EPI_WARPS) {
+  } else if (warp >= WG_EPI_WARP0 && warp < WG_EPI_WARP0 + WG_EPI_WARPS) {
     // ------------------------------------------------------------- epilogue
     const int qd = warp & 3;
-    const int half = (warp - HC_EPI_WARP0) >> 2;
+    const int half = (warp - WG_EPI_WARP0) >> 2;
     const int row = qd * 32 + lane;
     int k = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++k) {
@@ -790,7 +801,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == HC_MMA_WARP) tmem_dealloc(tmem, 512);
+  if (warp == WG_MMA_WARP) tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------ host
@@ -1225,7 +1236,7 @@ cudaError_t halo_wgrad_launch(const ConvParams &cp, HaloWgrad &h, int num_sms, c
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, HC_THREADS, h.smem, st>>>(ma, mb, h);
+    kern<<<grid, WG_THREADS, h.smem, st>>>(ma, mb, h);
     return cudaGetLastError();
   };
   const int fa = cp.a.fmt, fb = cp.b.fmt;
