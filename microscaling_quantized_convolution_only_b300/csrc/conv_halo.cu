@@ -128,8 +128,10 @@ __device__ __forceinline__ TileCoord hc_tile(const HaloConv &p, int t) {
 // Requantize 8 NBK fp32 columns of one row into NBK blocks of the next
 // layer's activations (see quantize.cu for the rounding).  Lanes 8q..8q+7
 // hold the eight batch rows of one block; the block amax is their
-// shuffle-max.  The blocks are processed side by side (independent chains
-// for the shuffles, the scale rounding and the encoding).
+// shuffle-max.  The per-block scale work (E4M3 block scale, bracket
+// multipliers) is done once per block: lane 8q + j computes it for block
+// j % NBK and the group reads it back by shuffles.  The blocks are processed
+// side by side (independent chains).
 template <int F, int NBK>
 __device__ __forceinline__ void hc_requant(const HaloConv &p, const float *y, int64_t blk_pos_ng, int n_in, int co0,
                                            bool row_ok, float s_t, float inv_den, uint32_t &amax_acc) {
@@ -145,14 +147,23 @@ __device__ __forceinline__ void hc_requant(const HaloConv &p, const float *y, in
   for (int o = 1; o < 8; o <<= 1)
 #pragma unroll
     for (int h = 0; h < NBK; ++h) m[h] = max(m[h], __shfl_xor_sync(0xFFFFFFFFu, m[h], o));
+  // this lane's block: hb = n_in % NBK
+  const int hb = n_in & (NBK - 1);
+  uint32_t mine = m[0];
+#pragma unroll
+  for (int h = 1; h < NBK; ++h) mine = hb == h ? m[h] : mine;
+  const uint32_t bsc_mine = block_scale_code_r<F>(__uint_as_float(mine), s_t, inv_den);
+  float lo_mine, hi_mine;
+  quot_bracket(code_value<8>(bsc_mine), s_t, lo_mine, hi_mine);
+  const int src0 = (threadIdx.x & 31) & ~7;
 #pragma unroll
   for (int h = 0; h < NBK; ++h) {
     amax_acc = max(amax_acc, m[h]);
     const int co = co0 + 8 * h;
-    const uint32_t bsc = block_scale_code_r<F>(__uint_as_float(m[h]), s_t, inv_den);
+    const uint32_t bsc = __shfl_sync(0xFFFFFFFFu, bsc_mine, src0 + h);
+    const float inv_lo = __shfl_sync(0xFFFFFFFFu, lo_mine, src0 + h);
+    const float inv_hi = __shfl_sync(0xFFFFFFFFu, hi_mine, src0 + h);
     const float bs = code_value<8>(bsc);
-    float inv_lo, inv_hi;
-    quot_bracket(bs, s_t, inv_lo, inv_hi);
     float v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = y[8 * h + j];
