@@ -63,7 +63,6 @@ constexpr int HC_EPI_WARP0 = 8;
 constexpr int HC_EPI_WARPS = 8;   // two per TMEM lane quadrant, alternating 16-column chunks
 constexpr int HC_TMA_WARP = 16;
 constexpr int HC_MMA_WARP = 17;
-constexpr int HC_THREADS = 18 * 32;
 // the conv kernel has a second MMA-issuing warp: output rows are split
 // between the two issuers, so their issue loops run side by side
 constexpr int HC_MMA_WARP2 = 18;
@@ -179,11 +178,14 @@ __device__ __forceinline__ void hc_requant(const HaloConv &p, const float *y, in
 // One accumulator row chunk of W columns (W = 16 or 32) starting at column
 // c0: scaled fp32 HWCN stores and / or the fused requantization.
 template <int FR, int W>
-__device__ __forceinline__ void hc_epi_chunk(const HaloConv &p, uint32_t taddr, float f, int64_t obase,
+__device__ __forceinline__ void hc_epi_chunk(const HaloConv &p, uint32_t taddr, bool zero, float f, int64_t obase,
                                              int64_t rq_blk, int n_in, int co0, bool valid, float rq_st,
                                              float rq_inv, uint32_t &amax_acc) {
   float y[W];
-  {
+  if (zero) {   // accumulator never written (warp-uniform)
+#pragma unroll
+    for (int jj = 0; jj < W; ++jj) y[jj] = 0.0f;
+  } else {
     uint32_t r[W];
     if constexpr (W == 32) tmem_ld32(taddr, r);
     else tmem_ld16(taddr, r);
@@ -201,6 +203,175 @@ __device__ __forceinline__ void hc_epi_chunk(const HaloConv &p, uint32_t taddr, 
 }
 
 }  // namespace
+
+// MMA issuers (see the kernel); QDM: the stride-2 data gradient in output quads
+template <int OP, bool QDM>
+__device__ __forceinline__ void hc_issue(const HaloConv &p, HcCtl *ctl, uint8_t *smem, uint32_t tmem, int warp, int lane) {
+  // ---------------------------------------------------------- MMA issuers
+  // issuer i (lane 0 of warp HC_MMA_WARP + i) takes the accumulators
+  // i, i + NI, ... of a tile (output rows; with QD, (row, phase) pairs);
+  // both wait for each decoded stage and each commits its MMAs to the
+  // stage's release barrier (count NI)
+  const int issuer = warp - HC_MMA_WARP, NI = p.RT >= 2 ? 2 : 1;
+  if (lane == 0 && issuer < NI) {
+    const uint32_t idesc = idesc_f16(128, p.BN, false, OP == OP_DGRAD);
+    // Descriptor words: the high word (stride fields, version) is fixed;
+    // the low word holds (address >> 4) in bits 0-13, so moving an operand
+    // by `bytes` adds bytes >> 4 to it (addresses stay below 256 KB).
+    const uint64_t a_desc = sdesc(smem_u32(smem + p.off_dec), 128, CGC * 128);
+    const uint64_t b_desc = OP == OP_FWD ? sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), 128, CGC * 128)
+                                         : sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), p.NB * 128, 128);
+    const uint32_t a_hi = (uint32_t)(a_desc >> 32), b_hi = (uint32_t)(b_desc >> 32);
+    const uint32_t d_row = (uint32_t)((p.WP * p.G * CGC * 128) >> 4);     // one halo row
+    const uint32_t d_col = (uint32_t)((p.G * CGC * 128) >> 4);            // one halo position
+    const uint32_t d_phase = (uint32_t)((p.PHP * p.G * CGC * 128) >> 4);  // one column phase
+    const uint32_t d_tap = (uint32_t)((p.NB * CGC * 128) >> 4);           // one weight tap
+    const uint32_t d_stage = p.dec_stage >> 4;
+    const int sh = p.S - 1;   // tap v sits in column phase v & sh, v >> sh positions in
+    const int taps = p.Kh * p.Kw;
+    // Per-tap operand offsets, built once: tap t = (u, v) reads the halo
+    // at row u, phase v & sh, position v >> sh, and the weights of tap t
+    // (fwd) or of the mirrored tap taps - 1 - t (dgrad).  Up to UT taps
+    // the issue loop is unrolled over this table: one add per operand per
+    // MMA.
+    // With QD the table is in phase order: entry j is tap qorder[j], whose
+    // dY offsets (dh, dw) = ((a + pad - kh) / 2, (b + pad - kw) / 2) are
+    // taken from the halo origin (-padh, -padw).
+    constexpr int UT = 9;
+    uint32_t a_off[UT], b_off[UT];
+#pragma unroll
+    for (int t = 0; t < UT; ++t) {
+      if (QDM) {
+        const int tq = p.qorder[t], u = tq / p.Kw, v = tq - u * p.Kw;
+        const int ah = ((u - p.qpad) % 2 + 2) % 2, aw = ((v - p.qpad) % 2 + 2) % 2;
+        const int dh = (ah + p.qpad - u) / 2 + p.padh, dw = (aw + p.qpad - v) / 2 + p.padw;
+        a_off[t] = (uint32_t)dh * d_row + (uint32_t)dw * d_col;
+        b_off[t] = (uint32_t)tq * d_tap;
+      } else {
+        const int u = t / p.Kw, v = t - u * p.Kw;
+        a_off[t] = (uint32_t)u * d_row + (uint32_t)(v & sh) * d_phase + (uint32_t)(v >> sh) * d_col;
+        b_off[t] = (uint32_t)(OP == OP_FWD ? t : taps - 1 - t) * d_tap;
+      }
+    }
+    int dit = 0, k = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
+      for (int c = 0; c < p.nchunks; ++c, ++dit) {
+        const int ds = dit % DSTAGES;
+        if (!hc_wait(&ctl->dfull[ds], (dit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_stage = (uint32_t)a_desc + (uint32_t)ds * d_stage;
+        const uint32_t b_stage = (uint32_t)b_desc + (uint32_t)ds * d_stage;
+        for (int sl = issuer; sl < p.RT && ok; sl += NI) {
+          // accumulator ring: accumulator sl of the k-th tile uses slot
+          // (k RT + sl) % NS; it is output row s = sl / NPHS (phase
+          // f = gray(sl % 4) with QD)
+          const int ring = k * p.RT + sl, slot = ring % p.NS, use = ring / p.NS;
+          const int s = QDM ? sl >> 2 : sl;   // NPHS = 4 with QD, else 1
+          if (c == 0) {
+            if (!hc_wait(&ctl->acc_empty[slot], (use & 1) ^ 1, p, ctl)) { ok = false; break; }
+            tc_fence_after();
+          }
+          const uint32_t d = tmem + slot * p.acc_cols;
+          const uint32_t a_s = a_stage + (uint32_t)(s * p.S) * d_row;
+          if (QDM) {
+            const int f = (sl & 3) ^ ((sl & 3) >> 1);
+            const int beg = p.qbeg[f], end = p.qbeg[f + 1];
+#pragma unroll
+            for (int j = 0; j < UT; ++j)
+              if (j >= beg && j < end)
+                umma_f16(d, desc_of(a_hi, a_s + a_off[j]), desc_of(b_hi, b_stage + b_off[j]), idesc,
+                         (j > beg || c > 0) ? 1u : 0u);
+          } else if (taps <= UT) {
+#pragma unroll
+            for (int tp = 0; tp < UT; ++tp)
+              if (tp < taps)
+                umma_f16(d, desc_of(a_hi, a_s + a_off[tp]), desc_of(b_hi, b_stage + b_off[tp]), idesc,
+                         (tp > 0 || c > 0) ? 1u : 0u);
+          } else {
+            for (int tp = 0; tp < taps; ++tp) {
+              const int u = tp / p.Kw, v = tp - u * p.Kw;
+              const uint32_t ao = (uint32_t)u * d_row + (uint32_t)(v & sh) * d_phase + (uint32_t)(v >> sh) * d_col;
+              const uint32_t bo = (uint32_t)(OP == OP_FWD ? tp : taps - 1 - tp) * d_tap;
+              umma_f16(d, desc_of(a_hi, a_s + ao), desc_of(b_hi, b_stage + bo), idesc, (tp > 0 || c > 0) ? 1u : 0u);
+            }
+          }
+          if (c == p.nchunks - 1) umma_commit(&ctl->acc_full[slot]);
+        }
+        umma_commit(&ctl->dempty[ds]);
+      }
+    }
+    umma_commit(&ctl->done);
+    hc_wait(&ctl->done, 0, p, ctl);
+  }
+  __syncwarp();
+}
+
+// Epilogue warps (see the kernel); QDM: the stride-2 data gradient in output quads
+template <int FR, bool QDM>
+__device__ __forceinline__ void hc_epilogue(const HaloConv &p, HcCtl *ctl, uint32_t tmem, int warp, int lane) {
+  // ------------------------------------------------------------- epilogue
+  const int q = warp & 3;                       // TMEM lanes 32q .. 32q+31
+  const int half = (warp - HC_EPI_WARP0) >> 2;  // 16-column chunks half, half + 2, ...
+  const int row = q * 32 + lane;
+  const int g = row >> 3, n_in = row & 7, pp = g / p.G, j = g - pp * p.G;
+  const float f = (*p.sa) * (*p.sb) * p.pre_mult;
+  float rq_st = 0.0f;
+  float rq_inv = 0.0f;
+  if (FR) {
+    rq_st = __fdiv_rn(*p.rq.amax_in, Fmt<FR ? FR : 4>::DENOM);
+    rq_inv = __frcp_rn(Fmt<FR ? FR : 4>::EMAX * rq_st);
+  }
+  uint32_t amax_acc = 0;
+  int k = 0;
+  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++k) {
+    const TileCoord tc = hc_tile(p, t);
+    const int ng = tc.g0 + j, n = ng * 8 + n_in;
+    bool stop = false;
+    for (int sl = 0; sl < p.RT; ++sl) {
+      const int ring = k * p.RT + sl, slot = ring % p.NS, use = ring / p.NS;
+      if (!hc_wait(&ctl->acc_full[slot], use & 1, p, ctl)) { stop = true; break; }
+      tc_fence_after();
+      int ho = tc.h0 + (QDM ? sl >> 2 : sl), wo = tc.w0 + pp;
+      bool zero = false;
+      if (QDM) {
+        // output phase f = gray(sl % 4) = 2 a + b: dX pixel (2 ho + a, 2 wo + b);
+        // a phase no tap reaches is zero
+        const int fq = (sl & 3) ^ ((sl & 3) >> 1);
+        ho = 2 * ho + (fq >> 1);
+        wo = 2 * wo + (fq & 1);
+        zero = p.qbeg[fq + 1] == p.qbeg[fq];
+      }
+      const bool valid = ho < p.outH && wo < p.outW;
+      const int64_t pos = (int64_t)ho * p.outW + wo;
+      const int64_t obase = pos * p.NC * (int64_t)p.N + n;
+      const int64_t rq_blk = (pos * p.NG + ng) * p.NCG;
+      const uint32_t tb = tmem + slot * p.acc_cols + ((uint32_t)(q * 32) << 16);
+      // the two warps of a lane quadrant take alternate column chunks: 32
+      // columns (four blocks side by side) for a requantize-only epilogue
+      // when BN is a multiple of 64, else 16
+      if (FR != 0 && !p.out && p.BN % 64 == 0) {
+        for (int c0 = 32 * half; c0 < p.BN; c0 += 64)
+          hc_epi_chunk<FR, 32>(p, tb + c0, zero, f, obase, rq_blk, n_in, tc.n0 + c0, valid, rq_st, rq_inv,
+                               amax_acc);
+      } else {
+        for (int c0 = 16 * half; c0 < p.BN; c0 += 32)
+          hc_epi_chunk<FR, 16>(p, tb + c0, zero, f, obase, rq_blk, n_in, tc.n0 + c0, valid, rq_st, rq_inv,
+                               amax_acc);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->acc_empty[slot]);
+    }
+    if (stop) break;
+  }
+  if (FR) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax_acc = max(amax_acc, __shfl_xor_sync(0xFFFFFFFFu, amax_acc, o));
+    if (lane == 0 && amax_acc && p.rq.amax_out_bits) atomicMax(p.rq.amax_out_bits, amax_acc);
+    if (blockIdx.x == 0 && row == 0 && half == 0) *p.rq.s_t_out = rq_st;
+  }
+}
 
 // FA: format of the input blocks (X or dY), FB: of the weights, FR: format of
 // the fused requantization of the output (0 = none).
@@ -221,7 +392,7 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
     }
     for (int s = 0; s < DSTAGES; ++s) {
       mbar_init(&ctl->dfull[s], HC_DEC_WARPS);
-      mbar_init(&ctl->dempty[s], p.R >= 2 ? 2 : 1);   // one commit per issuer
+      mbar_init(&ctl->dempty[s], p.RT >= 2 ? 2 : 1);   // one commit per issuer
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl->sfull[s], 64);
@@ -231,7 +402,7 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
       mbar_init(&ctl->acc_full[s], 1);
       mbar_init(&ctl->acc_empty[s], HC_EPI_WARPS);
     }
-    mbar_init(&ctl->done, p.R >= 2 ? 2 : 1);
+    mbar_init(&ctl->done, p.RT >= 2 ? 2 : 1);
     ctl->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -240,7 +411,6 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int taps = p.Kh * p.Kw;
 
   if (warp == HC_TMA_WARP) {
     // ------------------------------------------------------- TMA producer
@@ -393,132 +563,11 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
       }
     }
   } else if (warp == HC_MMA_WARP || warp == HC_MMA_WARP2) {
-    // ---------------------------------------------------------- MMA issuers
-    // issuer i (lane 0 of warp HC_MMA_WARP + i) takes the output rows
-    // s = i, i + NI, ...; both wait for each decoded stage and each commits
-    // its MMAs to the stage's release barrier (count NI)
-    const int issuer = warp - HC_MMA_WARP, NI = p.R >= 2 ? 2 : 1;
-    if (lane == 0 && issuer < NI) {
-      const uint32_t idesc = idesc_f16(128, p.BN, false, OP == OP_DGRAD);
-      // Descriptor words: the high word (stride fields, version) is fixed;
-      // the low word holds (address >> 4) in bits 0-13, so moving an operand
-      // by `bytes` adds bytes >> 4 to it (addresses stay below 256 KB).
-      const uint64_t a_desc = sdesc(smem_u32(smem + p.off_dec), 128, CGC * 128);
-      const uint64_t b_desc = OP == OP_FWD ? sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), 128, CGC * 128)
-                                           : sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), p.NB * 128, 128);
-      const uint32_t a_hi = (uint32_t)(a_desc >> 32), b_hi = (uint32_t)(b_desc >> 32);
-      const uint32_t d_row = (uint32_t)((p.WP * p.G * CGC * 128) >> 4);     // one halo row
-      const uint32_t d_col = (uint32_t)((p.G * CGC * 128) >> 4);            // one halo position
-      const uint32_t d_phase = (uint32_t)((p.PHP * p.G * CGC * 128) >> 4);  // one column phase
-      const uint32_t d_tap = (uint32_t)((p.NB * CGC * 128) >> 4);           // one weight tap
-      const uint32_t d_stage = p.dec_stage >> 4;
-      const int sh = p.S - 1;   // tap v sits in column phase v & sh, v >> sh positions in
-      const int taps = p.Kh * p.Kw;
-      // Per-tap operand offsets, built once: tap t = (u, v) reads the halo
-      // at row u, phase v & sh, position v >> sh, and the weights of tap t
-      // (fwd) or of the mirrored tap taps - 1 - t (dgrad).  Up to UT taps
-      // the issue loop is unrolled over this table: one add per operand per
-      // MMA.
-      constexpr int UT = 9;
-      uint32_t a_off[UT], b_off[UT];
-#pragma unroll
-      for (int t = 0; t < UT; ++t) {
-        const int u = t / p.Kw, v = t - u * p.Kw;
-        a_off[t] = (uint32_t)u * d_row + (uint32_t)(v & sh) * d_phase + (uint32_t)(v >> sh) * d_col;
-        b_off[t] = (uint32_t)(OP == OP_FWD ? t : taps - 1 - t) * d_tap;
-      }
-      int dit = 0, k = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
-        for (int c = 0; c < p.nchunks; ++c, ++dit) {
-          const int ds = dit % DSTAGES;
-          if (!hc_wait(&ctl->dfull[ds], (dit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t a_stage = (uint32_t)a_desc + (uint32_t)ds * d_stage;
-          const uint32_t b_stage = (uint32_t)b_desc + (uint32_t)ds * d_stage;
-          for (int s = issuer; s < p.R && ok; s += NI) {
-            // accumulator ring: row s of the k-th tile uses slot (k R + s) % NS
-            const int ring = k * p.R + s, slot = ring % p.NS, use = ring / p.NS;
-            if (c == 0) {
-              if (!hc_wait(&ctl->acc_empty[slot], (use & 1) ^ 1, p, ctl)) { ok = false; break; }
-              tc_fence_after();
-            }
-            const uint32_t d = tmem + slot * p.acc_cols;
-            const uint32_t a_s = a_stage + (uint32_t)(s * p.S) * d_row;
-            if (taps <= UT) {
-#pragma unroll
-              for (int tp = 0; tp < UT; ++tp)
-                if (tp < taps)
-                  umma_f16(d, desc_of(a_hi, a_s + a_off[tp]), desc_of(b_hi, b_stage + b_off[tp]), idesc,
-                           (tp > 0 || c > 0) ? 1u : 0u);
-            } else {
-              for (int tp = 0; tp < taps; ++tp) {
-                const int u = tp / p.Kw, v = tp - u * p.Kw;
-                const uint32_t ao = (uint32_t)u * d_row + (uint32_t)(v & sh) * d_phase + (uint32_t)(v >> sh) * d_col;
-                const uint32_t bo = (uint32_t)(OP == OP_FWD ? tp : taps - 1 - tp) * d_tap;
-                umma_f16(d, desc_of(a_hi, a_s + ao), desc_of(b_hi, b_stage + bo), idesc, (tp > 0 || c > 0) ? 1u : 0u);
-              }
-            }
-            if (c == p.nchunks - 1) umma_commit(&ctl->acc_full[slot]);
-          }
-          umma_commit(&ctl->dempty[ds]);
-        }
-      }
-      umma_commit(&ctl->done);
-      hc_wait(&ctl->done, 0, p, ctl);
-    }
-    __syncwarp();
+    if (OP == OP_DGRAD && p.QD) hc_issue<OP, true>(p, ctl, smem, tmem, warp, lane);
+    else hc_issue<OP, false>(p, ctl, smem, tmem, warp, lane);
   } else if (warp >= HC_EPI_WARP0 && warp < HC_EPI_WARP0 + HC_EPI_WARPS) {
-    // ------------------------------------------------------------- epilogue
-    const int q = warp & 3;                       // TMEM lanes 32q .. 32q+31
-    const int half = (warp - HC_EPI_WARP0) >> 2;  // 16-column chunks half, half + 2, ...
-    const int row = q * 32 + lane;
-    const int g = row >> 3, n_in = row & 7, pp = g / p.G, j = g - pp * p.G;
-    const float f = (*p.sa) * (*p.sb) * p.pre_mult;
-    float rq_st = 0.0f;
-    float rq_inv = 0.0f;
-    if (FR) {
-      rq_st = __fdiv_rn(*p.rq.amax_in, Fmt<FR ? FR : 4>::DENOM);
-      rq_inv = __frcp_rn(Fmt<FR ? FR : 4>::EMAX * rq_st);
-    }
-    uint32_t amax_acc = 0;
-    int k = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++k) {
-      const TileCoord tc = hc_tile(p, t);
-      const int wo = tc.w0 + pp, ng = tc.g0 + j, n = ng * 8 + n_in;
-      bool stop = false;
-      for (int s = 0; s < p.R; ++s) {
-        const int ring = k * p.R + s, slot = ring % p.NS, use = ring / p.NS;
-        if (!hc_wait(&ctl->acc_full[slot], use & 1, p, ctl)) { stop = true; break; }
-        tc_fence_after();
-        const int ho = tc.h0 + s;
-        const bool valid = ho < p.Hout && wo < p.Wout;
-        const int64_t pos = (int64_t)ho * p.Wout + wo;
-        const int64_t obase = pos * p.NC * (int64_t)p.N + n;
-        const int64_t rq_blk = (pos * p.NG + ng) * p.NCG;
-        const uint32_t tb = tmem + slot * p.acc_cols + ((uint32_t)(q * 32) << 16);
-        // the two warps of a lane quadrant take alternate column chunks: 32
-        // columns (four blocks side by side) for a requantize-only epilogue
-        // when BN is a multiple of 64, else 16
-        if (FR != 0 && !p.out && p.BN % 64 == 0) {
-          for (int c0 = 32 * half; c0 < p.BN; c0 += 64)
-            hc_epi_chunk<FR, 32>(p, tb + c0, f, obase, rq_blk, n_in, tc.n0 + c0, valid, rq_st, rq_inv, amax_acc);
-        } else {
-          for (int c0 = 16 * half; c0 < p.BN; c0 += 32)
-            hc_epi_chunk<FR, 16>(p, tb + c0, f, obase, rq_blk, n_in, tc.n0 + c0, valid, rq_st, rq_inv, amax_acc);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->acc_empty[slot]);
-      }
-      if (stop) break;
-    }
-    if (FR) {
-#pragma unroll
-      for (int o = 16; o; o >>= 1) amax_acc = max(amax_acc, __shfl_xor_sync(0xFFFFFFFFu, amax_acc, o));
-      if (lane == 0 && amax_acc && p.rq.amax_out_bits) atomicMax(p.rq.amax_out_bits, amax_acc);
-      if (blockIdx.x == 0 && row == 0 && half == 0) *p.rq.s_t_out = rq_st;
-    }
+    if (OP == OP_DGRAD && p.QD) hc_epilogue<FR, true>(p, ctl, tmem, warp, lane);
+    else hc_epilogue<FR, false>(p, ctl, tmem, warp, lane);
   }
 
   tc_fence_before();
@@ -877,9 +926,9 @@ size_t halo_smem(HaloConv &h, int bba, int bbb) {
   const int taps = h.Kh * h.Kw;
   // stride 2: the halo's even and odd input columns are staged as two
   // phases, so tap v reads phase v % 2 from position v / 2 on
-  h.WP = h.S == 1 ? h.P + h.Kw - 1 : h.P + (h.Kw - 1) / 2;
+  h.WP = h.S == 1 ? h.P + h.HKw - 1 : h.P + (h.HKw - 1) / 2;
   h.NPH = (h.S == 2 && h.Kw > 1) ? 2 : 1;
-  h.RH = h.S * (h.R - 1) + h.Kh;
+  h.RH = h.S * (h.R - 1) + h.HKh;
   h.PHP = h.RH * h.WP;
   if (h.NPH > 1)   // each phase's packed box must start 128-byte aligned
     while ((h.PHP * h.G * CGC * bba) % 128) ++h.PHP;
@@ -920,16 +969,19 @@ int pow2_at_least32(int x) {
 
 }  // namespace
 
-// Plans the halo kernel for a stride-1 forward or data-gradient convolution;
+// Plans the halo kernel for a forward (stride 1 or 2) or data-gradient
+// (stride 1, or stride 2 as output quads) convolution;
 // returns false when the layer does not fit its constraints (the caller then
 // uses the generic kernel).
 bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
   std::memset(&h, 0, sizeof(h));
   if (cp.op != OP_FWD && cp.op != OP_DGRAD) return false;
-  // stride 2 (forward only) reads the input through a [H][W/2][2] view
-  if (cp.stride != 1 && !(cp.stride == 2 && cp.op == OP_FWD && cp.W % 2 == 0)) return false;
+  // stride-2 forward reads the input through a [H][W/2][2] view; the
+  // stride-2 data gradient runs as output quads (all four phases per tile)
+  const bool qd = cp.op == OP_DGRAD && cp.stride == 2;
+  if (cp.stride != 1 && !(cp.stride == 2 && cp.op == OP_FWD && cp.W % 2 == 0) && !qd) return false;
   h.op = cp.op;
-  h.S = cp.stride;
+  h.S = qd ? 1 : cp.stride;
   h.N = cp.N;
   h.NG = cp.NG;
   h.Kh = cp.Kh;
@@ -940,12 +992,49 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
     h.Hin = cp.H; h.Win = cp.W; h.CGin = cp.CIG;
     h.Hout = cp.Ho; h.Wout = cp.Wo; h.NC = cp.Cout;
     h.padh = cp.pad; h.padw = cp.pad;
-  } else {
+  } else if (!qd) {
     if (cp.pad > cp.Kh - 1 || cp.pad > cp.Kw - 1) return false;
     h.Hin = cp.Ho; h.Win = cp.Wo; h.CGin = cp.COG;
     h.Hout = cp.H; h.Wout = cp.W; h.NC = cp.Cin;
     h.padh = cp.Kh - 1 - cp.pad; h.padw = cp.Kw - 1 - cp.pad;
+  } else {
+    // dX[2i + a] = sum over taps kh with (a + pad - kh) even of
+    // W[kh] dY[i + (a + pad - kh) / 2]: per output phase a stride-1
+    // correlation over dY; the dY rows read span the offsets dmin..dmax
+    // a 1-tap dimension leaves output phases no tap reaches: three quarters
+    // of the tile would be zeros (the generic kernel is faster there)
+    if (cp.Kh * cp.Kw > 9 || cp.Kh < 2 || cp.Kw < 2) return false;
+    auto span = [&](int K, int &dmin, int &dmax) {
+      dmin = 1 << 20; dmax = -(1 << 20);
+      for (int k = 0; k < K; ++k) {
+        const int a = ((k - cp.pad) % 2 + 2) % 2, d = (a + cp.pad - k) / 2;
+        dmin = std::min(dmin, d); dmax = std::max(dmax, d);
+      }
+    };
+    int dminh, dmaxh, dminw, dmaxw;
+    span(cp.Kh, dminh, dmaxh);
+    span(cp.Kw, dminw, dmaxw);
+    h.QD = 1; h.qpad = cp.pad;
+    // taps grouped by output phase f = 2 a + b
+    int n = 0;
+    for (int f = 0; f < 4; ++f) {
+      h.qbeg[f] = (uint8_t)n;
+      for (int t = 0; t < cp.Kh * cp.Kw; ++t) {
+        const int kh = t / cp.Kw, kw = t % cp.Kw;
+        const int a = ((kh - cp.pad) % 2 + 2) % 2, b = ((kw - cp.pad) % 2 + 2) % 2;
+        if (2 * a + b == f) h.qorder[n++] = (uint8_t)t;
+      }
+    }
+    h.qbeg[4] = (uint8_t)n;
+    h.Hin = cp.Ho; h.Win = cp.Wo; h.CGin = cp.COG;
+    h.Hout = (cp.H + 1) / 2; h.Wout = (cp.W + 1) / 2; h.NC = cp.Cin;
+    h.padh = -dminh; h.padw = -dminw;
+    h.HKh = dmaxh - dminh + 1; h.HKw = dmaxw - dminw + 1;
   }
+  if (!qd) { h.HKh = h.Kh; h.HKw = h.Kw; }
+  h.NPHS = qd ? 4 : 1;
+  h.outH = qd ? cp.H : h.Hout;
+  h.outW = qd ? cp.W : h.Wout;
   h.NCG = h.NC / 8;
   if (h.CGin % CGC) return false;
   h.nchunks = h.CGin / CGC;
@@ -988,7 +1077,8 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
       // tiles take successive slots, so the NS - R slots beyond a tile's own
       // let the next tile's MMAs start while the epilogue drains this one
       c.NS = std::min(MAX_R, 512 / c.acc_cols);
-      if (R > h.Hout || R > c.NS) continue;
+      c.RT = R * h.NPHS;
+      if (R > h.Hout || c.RT > c.NS) continue;
       if (R > 1 && h.Kh < h.S) continue;   // the halo rows between output rows would go unused
       c.R = R;
       const size_t sm = halo_smem(c, bba, bbb);
@@ -1007,9 +1097,9 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
       // column and row with fp32 output, ~40 with the requantizing
       // epilogue) is hidden behind the next tile's MMAs as far as the ring
       // has spare slots for that tile's rows
-      const double epi_t = (cp.rq.codes ? 40.0 : 8.5) * BN * R;
-      const int spare = c.NS - R;
-      const double exposed = spare >= R ? 0.0 : 1.0 - (double)spare / R;
+      const double epi_t = (cp.rq.codes ? 40.0 : 8.5) * BN * c.RT;
+      const int spare = c.NS - c.RT;
+      const double exposed = spare >= c.RT ? 0.0 : 1.0 - (double)spare / c.RT;
       const double cost = rounds * tile_t + (rounds - 1.0) * exposed * epi_t;
       if (cost < best_cost * 0.98) {
         best_cost = cost;

@@ -71,6 +71,13 @@ struct HaloConv {
                                  // staged apart, so every tap reads unit-stride halo positions)
   int PHP;                       // halo positions per phase: RH * WP, padded so that every phase's
                                  // packed box starts 128-byte aligned
+  int HKh, HKw;                  // halo extent in taps (Kh, Kw except for QD)
+  int QD;                        // stride-2 data gradient: a tile covers R rows x P positions of output
+                                 // quads (2 x 2 dX pixels), one accumulator per (row, output phase)
+  int NPHS, RT;                  // accumulator phases per row (4 with QD, else 1); accumulators per tile R NPHS
+  int qpad;                      // QD: padding of the forward convolution
+  uint8_t qorder[9], qbeg[5];    // QD: taps grouped by output phase; phase f owns qorder[qbeg[f] .. qbeg[f + 1])
+  int outH, outW;                // output rows / columns (Hout, Wout count quads with QD)
   int NS;                        // accumulator slots (TMEM ring; row s of tile k uses slot (k R + s) % NS)
   int BN, NB, acc_cols;          // output channels per tile, their groups, TMEM columns per row
   int nchunks;                   // CGin / 2
