@@ -266,7 +266,7 @@ __device__ __forceinline__ void hc_issue(const HaloConv &p, HcCtl *ctl, uint8_t 
           // accumulator ring: accumulator sl of the k-th tile uses slot
           // (k RT + sl) % NS; it is output row s = sl / NPHS (phase
           // f = gray(sl % 4) with QD)
-          const int ring = k * p.RT + sl, slot = ring % p.NS, use = ring / p.NS;
+          const int ring = k * p.RT + sl, slot = ring & (p.NS - 1), use = ring >> p.ns_log2;
           const int s = QDM ? sl >> 2 : sl;   // NPHS = 4 with QD, else 1
           if (c == 0) {
             if (!hc_wait(&ctl->acc_empty[slot], (use & 1) ^ 1, p, ctl)) { ok = false; break; }
@@ -329,7 +329,7 @@ __device__ __forceinline__ void hc_epilogue(const HaloConv &p, HcCtl *ctl, uint3
     const int ng = tc.g0 + j, n = ng * 8 + n_in;
     bool stop = false;
     for (int sl = 0; sl < p.RT; ++sl) {
-      const int ring = k * p.RT + sl, slot = ring % p.NS, use = ring / p.NS;
+      const int ring = k * p.RT + sl, slot = ring & (p.NS - 1), use = ring >> p.ns_log2;
       if (!hc_wait(&ctl->acc_full[slot], use & 1, p, ctl)) { stop = true; break; }
       tc_fence_after();
       int ho = tc.h0 + (QDM ? sl >> 2 : sl), wo = tc.w0 + pp;
@@ -1076,7 +1076,9 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
       // accumulator ring of NS slots (all of the TMEM): rows of successive
       // tiles take successive slots, so the NS - R slots beyond a tile's own
       // let the next tile's MMAs start while the epilogue drains this one
-      c.NS = std::min(MAX_R, 512 / c.acc_cols);
+      c.NS = std::min(MAX_R, 512 / c.acc_cols);   // a power of two
+      c.ns_log2 = 0;
+      while ((1 << c.ns_log2) < c.NS) ++c.ns_log2;
       c.RT = R * h.NPHS;
       if (R > h.Hout || c.RT > c.NS) continue;
       if (R > 1 && h.Kh < h.S) continue;   // the halo rows between output rows would go unused

@@ -78,7 +78,8 @@ struct HaloConv {
   int qpad;                      // QD: padding of the forward convolution
   uint8_t qorder[9], qbeg[5];    // QD: taps grouped by output phase; phase f owns qorder[qbeg[f] .. qbeg[f + 1])
   int outH, outW;                // output rows / columns (Hout, Wout count quads with QD)
-  int NS;                        // accumulator slots (TMEM ring; row s of tile k uses slot (k R + s) % NS)
+  int NS, ns_log2;               // accumulator slots (TMEM ring, a power of two; accumulator a of tile k
+                                 // uses slot (k RT + a) % NS)
   int BN, NB, acc_cols;          // output channels per tile, their groups, TMEM columns per row
   int nchunks;                   // CGin / 2
   int tiles_g, tiles_w, tiles_h, tiles_n, num_tiles;
