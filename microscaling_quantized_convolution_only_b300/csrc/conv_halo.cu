@@ -262,6 +262,10 @@ __device__ __forceinline__ void hc_issue(const HaloConv &p, HcCtl *ctl, uint8_t 
         tc_fence_after();
         const uint32_t a_stage = (uint32_t)a_desc + (uint32_t)ds * d_stage;
         const uint32_t b_stage = (uint32_t)b_desc + (uint32_t)ds * d_stage;
+        // the weight descriptors of the chunk, shared by all its rows
+        uint32_t bq[UT];
+#pragma unroll
+        for (int tp = 0; tp < UT; ++tp) bq[tp] = b_stage + b_off[tp];
         for (int sl = issuer; sl < p.RT && ok; sl += NI) {
           // accumulator ring: accumulator sl of the k-th tile uses slot
           // (k RT + sl) % NS; it is output row s = sl / NPHS (phase
@@ -280,14 +284,16 @@ __device__ __forceinline__ void hc_issue(const HaloConv &p, HcCtl *ctl, uint8_t 
 #pragma unroll
             for (int j = 0; j < UT; ++j)
               if (j >= beg && j < end)
-                umma_f16(d, desc_of(a_hi, a_s + a_off[j]), desc_of(b_hi, b_stage + b_off[j]), idesc,
-                         (j > beg || c > 0) ? 1u : 0u);
-          } else if (taps <= UT) {
+                umma_f16(d, desc_of(a_hi, a_s + a_off[j]), desc_of(b_hi, bq[j]), idesc, (j > beg || c > 0) ? 1u : 0u);
+          } else if (taps == UT) {   // 3x3: no per-tap predicate
+            umma_f16(d, desc_of(a_hi, a_s + a_off[0]), desc_of(b_hi, bq[0]), idesc, c > 0 ? 1u : 0u);
+#pragma unroll
+            for (int tp = 1; tp < UT; ++tp) umma_f16_acc(d, desc_of(a_hi, a_s + a_off[tp]), desc_of(b_hi, bq[tp]), idesc);
+          } else if (taps < UT) {
 #pragma unroll
             for (int tp = 0; tp < UT; ++tp)
               if (tp < taps)
-                umma_f16(d, desc_of(a_hi, a_s + a_off[tp]), desc_of(b_hi, b_stage + b_off[tp]), idesc,
-                         (tp > 0 || c > 0) ? 1u : 0u);
+                umma_f16(d, desc_of(a_hi, a_s + a_off[tp]), desc_of(b_hi, bq[tp]), idesc, (tp > 0 || c > 0) ? 1u : 0u);
           } else {
             for (int tp = 0; tp < taps; ++tp) {
               const int u = tp / p.Kw, v = tp - u * p.Kw;
