@@ -812,10 +812,10 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
           for (int kw = 0; kw < p.Kw; ++kw) {
             const uint32_t d = tmem + kw * p.acc_cols;
             const uint32_t b_w = b_stage + (uint32_t)(kw & sh) * b_phase + (uint32_t)(kw >> sh) * b_kw;
+            umma_f16(d, desc_of(a_hi, a_stage), desc_of(b_hi, b_w), idesc, q > T.q0 ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < KK; ++kk)
-              umma_f16(d, desc_of(a_hi, a_stage + kk * a_kk), desc_of(b_hi, b_w + kk * b_kk), idesc,
-                       (kk > 0 || q > T.q0) ? 1u : 0u);
+            for (int kk = 1; kk < KK; ++kk)
+              umma_f16_acc(d, desc_of(a_hi, a_stage + kk * a_kk), desc_of(b_hi, b_w + kk * b_kk), idesc);
           }
           umma_commit(&ctl->dempty[ds]);
         }
