@@ -500,6 +500,19 @@ __device__ __forceinline__ uint64_t cvt_row_e4m3(const float (&q)[8]) {
   return r;
 }
 
+__device__ __forceinline__ uint64_t cvt_row_e2m3(const float (&q)[8]) {
+  uint64_t r;
+  asm("{ .reg .b16 a, b, c, d;\n"
+      "  cvt.rn.satfinite.e2m3x2.f32 a, %2, %1;\n"
+      "  cvt.rn.satfinite.e2m3x2.f32 b, %4, %3;\n"
+      "  cvt.rn.satfinite.e2m3x2.f32 c, %6, %5;\n"
+      "  cvt.rn.satfinite.e2m3x2.f32 d, %8, %7;\n"
+      "  mov.b64 %0, {a, b, c, d}; }"
+      : "=l"(r)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return r;
+}
+
 template <int F>
 __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs, float s_t, float inv_lo, float inv_hi) {
   float ql[8], qh[8];
@@ -508,28 +521,18 @@ __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs,
     mul2(v[2 * jj], v[2 * jj + 1], inv_lo, ql[2 * jj], ql[2 * jj + 1]);
     mul2(v[2 * jj], v[2 * jj + 1], inv_hi, qh[2 * jj], qh[2 * jj + 1]);
   }
+  // whole rows at once (pairs in byte / 16-bit containers); the pairs are
+  // unpacked only for the E2M3 bit packing or when the ends differ
+  const uint64_t row_lo = F == 4 ? (uint64_t)cvt_row_e2m1(ql) : F == 8 ? cvt_row_e4m3(ql) : cvt_row_e2m3(ql);
+  const uint64_t row_hi = F == 4 ? (uint64_t)cvt_row_e2m1(qh) : F == 8 ? cvt_row_e4m3(qh) : cvt_row_e2m3(qh);
+  constexpr int SH = F == 4 ? 8 : 16;
+  constexpr uint64_t M = F == 4 ? 0xFFu : 0xFFFFu;
   uint32_t lo[4], hi[4];
-  if (F == 4 || F == 8) {
-    // whole rows at once; the pairs are unpacked only when the ends differ
-    const uint64_t row_lo = F == 4 ? (uint64_t)cvt_row_e2m1(ql) : cvt_row_e4m3(ql);
-    const uint64_t row_hi = F == 4 ? (uint64_t)cvt_row_e2m1(qh) : cvt_row_e4m3(qh);
-    if (row_lo == row_hi) return row_lo;   // the common case: no element near a midpoint
-    constexpr int SH = F == 4 ? 8 : 16;
-    constexpr uint64_t M = F == 4 ? 0xFFu : 0xFFFFu;
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      lo[jj] = (uint32_t)((row_lo >> (SH * jj)) & M);
-      hi[jj] = (uint32_t)((row_hi >> (SH * jj)) & M);
-    }
-  } else {
+  for (int jj = 0; jj < 4; ++jj) lo[jj] = (uint32_t)((row_lo >> (SH * jj)) & M);
+  if (row_lo == row_hi) return F == 6 ? place_row<F>(lo) : row_lo;   // common case: no element near a midpoint
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      lo[jj] = cvt2<F>(ql[2 * jj], ql[2 * jj + 1]);
-      hi[jj] = cvt2<F>(qh[2 * jj], qh[2 * jj + 1]);
-    }
-    const uint64_t row_lo = place_row<F>(lo);
-    if (row_lo == place_row<F>(hi)) return row_lo;
-  }
+  for (int jj = 0; jj < 4; ++jj) hi[jj] = (uint32_t)((row_hi >> (SH * jj)) & M);
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj)
     if (lo[jj] != hi[jj]) lo[jj] = fix_pair<F>(lo[jj], hi[jj], v[2 * jj], v[2 * jj + 1], bs, s_t);
