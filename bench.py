@@ -494,16 +494,17 @@ def run_gpu(args):
             step.conv_bytes[op] / (peaks["hbm_gbs"] * 1e9) else "hbm"
     dom = max(("fwd", "dgrad", "wgrad"), key=lambda o: ops[o]["ms_per_step"])
     d = ops[dom]
+    traffic = captured_traffic(wl.name, f"conv_{dom}", wl.layers[0].N)
     if d["bound"] == "tensor":
         achieved = step.flops[dom] / d["launches_per_step"] / (d["ms_per_launch"] * 1e-3) / 1e12
         roof = {"kernel": f"conv_{dom}", "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": None,
+                "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} bf16 dense, sustained (fp16 MMA runs at the bf16 rate)"}
     else:
         achieved = step.conv_bytes[dom] / d["launches_per_step"] / (d["ms_per_launch"] * 1e-3) / 1e9
         roof = {"kernel": f"conv_{dom}", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} HBM copy"}
 
     layers_out = []
@@ -607,6 +608,40 @@ def oracle_sample_step(wl, budget_s, state):
     per_out = 2 * Ls.Cin * Ls.k * Ls.k
     flops = (len(state["idx_f"]) + len(state["idx_d"])) * per_out + len(state["idx_w"]) * 2 * Ls.N * Ls.Ho * Ls.Wo
     return flops, dt, {"quantized_elements": X.size + W.size + dY.size}
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# dominant kernel, averaged over its launches in one step, from an ncu
+# capture of the same workload at a smaller batch (profiles/, command there),
+# scaled by the batch.  The writes of the captured launches are a lower
+# bound (output lines still in L2 when a launch ends are not counted).  Valid
+# only while the kernel sources are the captured ones.
+TRAFFIC = {
+    ("stack4-56x56-c128-nvfp4", "conv_dgrad"): {
+        "bytes_per_launch": (4 * 13.435e6 + 48.189e6) / 4, "batch": 64,
+        "sources_sha1": "dbf10f75ac7dd745df28107705522e7ab0f7902f"},
+}
+
+
+def kernel_sources_sha1():
+    import hashlib
+    import glob
+    here = os.path.dirname(os.path.abspath(__file__))
+    files = sorted(glob.glob(os.path.join(here, "microscaling_quantized_convolution_only_b300", "csrc", "*")))
+    files.append(os.path.join(here, "include", "mqconv.h"))
+    h = hashlib.sha1()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def captured_traffic(workload, kernel, batch):
+    t = TRAFFIC.get((workload, kernel))
+    if t is None or t["sources_sha1"] != kernel_sources_sha1():
+        return None
+    return t["bytes_per_launch"] * batch / t["batch"]
 
 
 def cpu_baseline(wl, budget_s=15.0):
