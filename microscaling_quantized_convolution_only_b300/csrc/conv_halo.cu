@@ -537,6 +537,7 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
         // = blk + tap * (COG - CGC) * NB + c * CGC * NB; tap = blk / (CGC * NB)
         // is carried along the thread's stride instead of divided out per row
         const int tap_span = CGC * p.NB, step_blk = HC_DEC_THREADS / 8;
+        const int q_step = step_blk / tap_span, r_step = step_blk - q_step * tap_span;
         int d_tap = (tid >> 3) / tap_span, d_rem = (tid >> 3) - d_tap * tap_span;
         for (int i = tid; i < nbr; i += HC_DEC_THREADS) {
           const int blk = i >> 3, r = i & 7;
@@ -546,11 +547,13 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
             si = tn * p.CIG + c * CGC + kc;
           } else {              // block (tap, kc, nb); scales [tap][cog][nb]
             si = blk + (d_tap * (p.COG - CGC) + c * CGC) * p.NB;
-            d_rem += step_blk;
-            while (d_rem >= tap_span) {
-              d_rem -= tap_span;
-              ++d_tap;
-            }
+            // advance (d_tap, d_rem) by step_blk blocks without a loop, so the
+            // row loop stays straight-line
+            d_tap += q_step;
+            d_rem += r_step;
+            const bool wrap = d_rem >= tap_span;
+            d_rem -= wrap ? tap_span : 0;
+            d_tap += wrap ? 1 : 0;
           }
           const uint8_t s = scw[si];
           const uint4 v = decode_raw<FB>(lds_row<FB>(pkb + blk * BBB, r), scale_pair<FB>(s));
