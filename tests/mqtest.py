@@ -72,16 +72,19 @@ class LayerRun:
     oracle) and run fwd/dgrad/wgrad."""
 
     def __init__(self, layer, fmt, dtype, X, W, dY, device, check_quant=True):
+        # fmt: one element format for X, W and dY, or a (X, W, dY) triple
+        # (MicroQonv+: each tensor in its own format)
         self.layer, self.fmt, self.dtype, self.device = layer, fmt, dtype, device
+        fx, fw, fg = fmt if isinstance(fmt, tuple) else (fmt, fmt, fmt)
         L = layer
         self.Xd, self.Wd, self.dYd = (to_dev(a, dtype, device) for a in (X, W, dY))
-        self.xq, _ = gpu_quantize(self.Xd, fmt, "act", "nchw", L.x_shape())
-        self.wq, _ = gpu_quantize(self.Wd, fmt, "weight", "oihw", L.w_shape())
-        self.gq, _ = gpu_quantize(self.dYd, fmt, "grad", "nchw", L.y_shape())
+        self.xq, _ = gpu_quantize(self.Xd, fx, "act", "nchw", L.x_shape())
+        self.wq, _ = gpu_quantize(self.Wd, fw, "weight", "oihw", L.w_shape())
+        self.gq, _ = gpu_quantize(self.dYd, fg, "grad", "nchw", L.y_shape())
         if check_quant:
-            for p, a, role, lay in ((self.xq, X, "act", "nchw"), (self.wq, W, "weight", "oihw"),
-                                    (self.gq, dY, "grad", "nchw")):
-                assert_packed_equal(p, oracle.quantize(a, fmt, role, lay), f"{role} quantization")
+            for p, a, f, role, lay in ((self.xq, X, fx, "act", "nchw"), (self.wq, W, fw, "weight", "oihw"),
+                                       (self.gq, dY, fg, "grad", "nchw")):
+                assert_packed_equal(p, oracle.quantize(a, f, role, lay), f"{role} quantization")
 
     def fwd(self):
         L = self.layer

@@ -55,6 +55,22 @@ def test_small_layers_full(cuda_device, fmt, L):
     run_full(LayerRun(L, fmt, "f32", X, W, dY, cuda_device), f"{fmt} {L.name()}")
 
 
+MIXED_LAYERS = [Layer(8, 16, 8, 8, 16, 3, 1, 1), Layer(16, 32, 10, 14, 48, 3, 2, 1), Layer(32, 64, 12, 12, 64, 3, 1, 1)]
+
+
+@pytest.mark.parametrize("fmts", [("e2m1", "e4m3", "e2m3"), ("e4m3", "e2m1", "e4m3"), ("e2m3", "e2m3", "e2m1")],
+                         ids=lambda f: "-".join(f))
+@pytest.mark.parametrize("L", MIXED_LAYERS, ids=lambda L: L.name())
+def test_mixed_formats(cuda_device, fmts, L):
+    """MicroQonv+: X, W and dY each in their own element format; every GEMM
+    mixes two formats (fp16 decode of each operand, E4M3 pairs pre-scaled)."""
+    rng = np.random.default_rng(L.N + 3 * L.Cin + L.Cout)
+    X = np.maximum(rng.standard_normal(L.x_shape()), 0).astype(np.float32)
+    W = (rng.standard_normal(L.w_shape()) * np.sqrt(2 / (L.Cin * L.k * L.k))).astype(np.float32)
+    dY = (rng.standard_normal(L.y_shape()) * 0.1).astype(np.float32)
+    run_full(LayerRun(L, fmts, "f32", X, W, dY, cuda_device), f"{fmts} {L.name()}")
+
+
 @pytest.mark.parametrize("li", range(5))
 def test_workload1_full(cuda_device, li):
     wl = S.WORKLOADS[1]
