@@ -57,8 +57,8 @@ struct ConvParams {
   uint32_t *status;
 };
 
-// Stride-1 forward / data-gradient convolution with per-tile halo reuse
-// (conv_halo.cu).  Filled by halo_plan() from a ConvParams.
+// Forward / data-gradient convolution (stride 1 or 2) with per-tile halo
+// reuse (conv_halo.cu).  Filled by halo_plan() from a ConvParams.
 struct HaloConv {
   int op;
   int N, NG;
@@ -101,7 +101,7 @@ struct HaloConv {
   size_t smem;
 };
 
-// Stride-1 weight gradient with per-chunk halo reuse (conv_halo.cu).  Each
+// Weight gradient (stride 1 or 2) with per-chunk halo reuse (conv_halo.cu).  Each
 // CTA tile accumulates one kernel row (kh) x Kw taps x BNc input channels x
 // 128 output channels over a range of (output row, positions, batch groups)
 // chunks and writes one split-K partial.
