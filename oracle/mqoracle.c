@@ -24,7 +24,7 @@
  *       §II-A "Forward Pass"), generalised to floor((H + 2p - K) / s) + 1 as
  *       the paper states its method is independent of stride and padding.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - T_scale = fl32(amax / (maxB_ef * 448)): one correctly rounded fp32 division.
  *   - Both roundings act on the exact real quotient (no intermediate rounded
  *     quotient), nearest grid value, ties to the code with an even mantissa,
