@@ -31,6 +31,8 @@ SMALL = [
     Layer(8, 16, 8, 6, 16, 3, 2, 0),      # stride 2 without padding
     Layer(24, 16, 14, 10, 136, 3, 2, 1),  # stride 2, three batch groups, two output-channel tiles
     Layer(8, 16, 11, 12, 16, 5, 2, 2),    # 5x5 stride 2 (three taps per column phase)
+    Layer(8, 16, 8, 8, 16, 2, 2, 0),      # 2x2 stride 2 (one tap per output phase)
+    Layer(16, 32, 9, 10, 16, 3, 2, 2),    # stride 2, padding 2 (dgrad phases start one row in)
 ]
 
 
