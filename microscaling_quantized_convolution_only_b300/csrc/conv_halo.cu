@@ -1,6 +1,6 @@
-// conv_halo.cu -- forward (stride 1 and 2), stride-1 data-gradient and
-// weight-gradient (stride 1 and 2) convolutions that decode every packed
-// input block once per tile and reuse it for all taps.
+// conv_halo.cu -- forward, data-gradient and weight-gradient convolutions
+// (stride 1 and 2) that decode every packed input block once per tile and
+// reuse it for all taps.
 //
 // MicroQonv §IV-A builds the channel-batch-first im2col X' on chip: each
 // contiguous CBF block crosses the off-chip/on-chip boundary once and is then
@@ -24,7 +24,11 @@
 // The data gradient of a stride-1 layer is the same correlation run on dY
 // with the taps mirrored and the weight blocks read transposed
 // (MN-major descriptor), padding Kh - 1 - pad: dX = col2im(W^T G_Y) of
-// MicroQonv §IV-A without any col2im buffer.
+// MicroQonv §IV-A without any col2im buffer.  At stride 2 a tile covers
+// output quads (2 x 2 dX pixels): dX[2i + a] sums W[kh] dY[i + (a + pad -
+// kh) / 2] over the taps kh of parity a + pad, so each output phase (a, b)
+// is a stride-1 correlation over dY with its own taps; the tile keeps one
+// accumulator per (row, phase) and feeds each decoded tap to its phase.
 //
 // GEMM per tile: rows = (output row s, position p, batch group j, n), columns
 // = output channels (BN), K = (chunk, tap, 16 channels).  One accumulator of
@@ -33,14 +37,14 @@
 // the epilogue drains one tile the next tile's rows already accumulate in
 // the spare slots and in the slots drained first.
 //
-// Warp roles: warps 0-7 decode, warps 8-15 drain the accumulators
-// (tcgen05.ld; warps w and w+4 share TMEM lane quadrant w % 4 and take
-// alternate 16-column chunks) into fp32 HWCN outputs or requantized CBF
-// blocks, warp 16 copies block scales and issues the TMA loads (lane 0),
-// lane 0 of warps 17 and 18 issue tcgen05.mma (the conv kernel splits the
-// output rows between the two issuers: the issue loop of one thread, not
-// the tensor pipe, bounds the MMA rate of a single issuer here; the
-// weight-gradient kernel has one).  Every wait is
+// Warp roles (conv kernel): warps 0-7 decode, warps 8-15 drain the
+// accumulators (tcgen05.ld; warps w and w+4 share TMEM lane quadrant w % 4
+// and take alternate 16- or 32-column chunks) into fp32 HWCN outputs or
+// requantized CBF blocks, warp 16 copies block scales and issues the TMA
+// loads (lane 0), lane 0 of warps 17 and 18 issue tcgen05.mma (the two
+// issuers split a tile's accumulators: the issue loop of one thread, not
+// the tensor pipe, bounds the MMA rate of a single issuer here).  The
+// weight-gradient kernel has ten decode warps and one issuer.  Every wait is
 // bounded; on expiry the CTA records MQ_ERR_TIMEOUT, stops, lets its copies
 // and MMAs in flight finish and frees its TMEM.
 #include <cuda.h>
