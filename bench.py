@@ -682,13 +682,13 @@ TRAFFIC = {
         "sources_sha1": "5df95795b2ec964a749f526e18051c440709cd37"},
 }
 
-def kernel_sources_sha1():
+def kernel_sources_sha1(root=None):
     """SHA-1 of the library sources with comments and blank space removed
     (editing a comment does not invalidate a capture, editing code does)."""
     import glob
     import hashlib
     import re
-    here = os.path.dirname(os.path.abspath(__file__))
+    here = root or os.path.dirname(os.path.abspath(__file__))
     files = sorted(glob.glob(os.path.join(here, "microscaling_quantized_convolution_only_b300", "csrc", "*")))
     files.append(os.path.join(here, "include", "mqconv.h"))
     h = hashlib.sha1()
