@@ -224,6 +224,96 @@ def conv_wgrad_at(dY, X, layer, idx):
     return _sampled(lib().orc_conv_wgrad_at, dY, X, layer, idx)
 
 
+# ------------------------------------- explicit-im2col GEMM form (full tensors)
+#
+# The same three convolutions written as the paper's GEMMs on an explicit
+# im2col matrix (MicroQonv §II-C, Fig. 2: each receptive field unrolled into a
+# column; §IV-A: Y = W_f X', G_W = G_Y X'^T, G_X' = W_f^T G_Y followed by the
+# reordering back to the input positions, which sums the copies of one input
+# that several receptive fields share).  A library matmul does each fp64
+# product; the im2col matrix is built per slice of `nb` batch entries, so the
+# full tensors of a large layer fit in host memory.  sum |a*b| (the scale of
+# the rounding tolerance) is the same product on |W|, |X'| in fp32.  Slower
+# layers are checked with these on the whole output; the 7-loop functions
+# above pin them on small layers.
+
+def _im2col(Xn: np.ndarray, layer) -> np.ndarray:
+    """X' for a slice of the batch: rows (ci, kh, kw) (the order of W.reshape
+    (Cout, -1) for OIHW weights), columns (n, ho, wo).  Zero padding."""
+    L = layer
+    nb = Xn.shape[0]
+    Xp = np.zeros((nb, L.Cin, L.H + 2 * L.pad, L.W + 2 * L.pad), dtype=Xn.dtype)
+    Xp[:, :, L.pad:L.pad + L.H, L.pad:L.pad + L.W] = Xn
+    cols = np.empty((L.Cin, L.k, L.k, nb, L.Ho, L.Wo), dtype=Xn.dtype)
+    for kh in range(L.k):
+        for kw in range(L.k):
+            win = Xp[:, :, kh:kh + L.stride * (L.Ho - 1) + 1:L.stride, kw:kw + L.stride * (L.Wo - 1) + 1:L.stride]
+            cols[:, kh, kw] = win.transpose(1, 0, 2, 3)
+    return cols.reshape(L.Cin * L.k * L.k, nb * L.Ho * L.Wo)
+
+
+def _col2im_add(dXp: np.ndarray, T: np.ndarray, layer) -> None:
+    """The reordering of G_X' back to input positions: row (ci, kh, kw),
+    column (n, ho, wo) of T adds into padded input (n, ci, ho s + kh,
+    wo s + kw)."""
+    L = layer
+    nb = dXp.shape[0]
+    T = T.reshape(L.Cin, L.k, L.k, nb, L.Ho, L.Wo)
+    for kh in range(L.k):
+        for kw in range(L.k):
+            dXp[:, :, kh:kh + L.stride * (L.Ho - 1) + 1:L.stride, kw:kw + L.stride * (L.Wo - 1) + 1:L.stride] += \
+                T[:, kh, kw].transpose(1, 0, 2, 3)
+
+
+def conv_fwd_gemm(X: np.ndarray, W: np.ndarray, layer, nb: int = 8):
+    """Y (N, Cout, Ho, Wo) = W_f X' per batch slice, fp64; and sum |a*b| (fp32)."""
+    L = layer
+    Wf = np.asarray(W, dtype=np.float64).reshape(L.Cout, -1)
+    Wa = np.abs(Wf).astype(np.float32)
+    Y = np.empty(L.y_shape(), dtype=np.float64)
+    Ya = np.empty(L.y_shape(), dtype=np.float64)
+    for n0 in range(0, L.N, nb):
+        Xc = _im2col(np.asarray(X[n0:n0 + nb], dtype=np.float64), L)
+        m = Xc.shape[1] // (L.Ho * L.Wo)
+        Y[n0:n0 + m] = (Wf @ Xc).reshape(L.Cout, m, L.Ho, L.Wo).transpose(1, 0, 2, 3)
+        Ya[n0:n0 + m] = (Wa @ np.abs(Xc).astype(np.float32)).reshape(L.Cout, m, L.Ho, L.Wo).transpose(1, 0, 2, 3)
+    return Y, Ya
+
+
+def conv_dgrad_gemm(W: np.ndarray, dY: np.ndarray, layer, nb: int = 8):
+    """dX (N, Cin, H, W): G_X' = W_f^T G_Y per batch slice, then the
+    reordering (col2im sum) into input positions, fp64; and sum |a*b|."""
+    L = layer
+    Wf = np.asarray(W, dtype=np.float64).reshape(L.Cout, -1)
+    Wa = np.abs(Wf).astype(np.float32)
+    dX = np.empty(L.x_shape(), dtype=np.float64)
+    dXa = np.empty(L.x_shape(), dtype=np.float64)
+    P = L.pad
+    for n0 in range(0, L.N, nb):
+        G = np.asarray(dY[n0:n0 + nb], dtype=np.float64)
+        m = G.shape[0]
+        Gm = G.transpose(1, 0, 2, 3).reshape(L.Cout, m * L.Ho * L.Wo)
+        for out, T in ((dX, Wf.T @ Gm), (dXa, (Wa.T @ np.abs(Gm).astype(np.float32)).astype(np.float64))):
+            acc = np.zeros((m, L.Cin, L.H + 2 * P + L.stride, L.W + 2 * P + L.stride), dtype=np.float64)
+            _col2im_add(acc, T, L)
+            out[n0:n0 + m] = acc[:, :, P:P + L.H, P:P + L.W]
+    return dX, dXa
+
+
+def conv_wgrad_gemm(dY: np.ndarray, X: np.ndarray, layer, nb: int = 8):
+    """dW (Cout, Cin, Kh, Kw) = sum over batch slices of G_Y X'^T, fp64; and sum |a*b|."""
+    L = layer
+    dW = np.zeros((L.Cout, L.Cin * L.k * L.k), dtype=np.float64)
+    dWa = np.zeros_like(dW)
+    for n0 in range(0, L.N, nb):
+        Xc = _im2col(np.asarray(X[n0:n0 + nb], dtype=np.float64), L)
+        G = np.asarray(dY[n0:n0 + nb], dtype=np.float64)
+        Gm = G.transpose(1, 0, 2, 3).reshape(L.Cout, -1)
+        dW += Gm @ Xc.T
+        dWa += np.abs(Gm).astype(np.float32) @ np.abs(Xc).astype(np.float32).T
+    return dW.reshape(L.w_shape()), dWa.reshape(L.w_shape())
+
+
 # ------------------------------------------------- instrumented naive flows
 #
 # These follow MicroQonv §III-C and the Table I comparison: quantization

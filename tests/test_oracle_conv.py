@@ -101,3 +101,19 @@ def test_sampled_equals_full(orc, L):
         v, va = at(A, B, L, idx)
         np.testing.assert_array_equal(v, ref.ravel()[idx])
         np.testing.assert_array_equal(va, refa.ravel()[idx])
+
+
+@pytest.mark.parametrize("nb", [8, 3])
+@pytest.mark.parametrize("L", GEOMS + [Layer(16, 24, 7, 6, 16, 3, 2, 2), Layer(8, 16, 11, 12, 16, 5, 2, 2)],
+                         ids=lambda L: L.name() if hasattr(L, "name") else str(L))
+def test_explicit_im2col_gemm_checker_matches_7_loop(orc, L, nb):
+    """The full-tensor checker (explicit im2col + library fp64 matmul, batch
+    slices of nb entries, the last one ragged for nb = 3) equals the direct
+    7-loop oracle; its sum |a*b|, formed in fp32, is within fp32 rounding."""
+    X, W, dY = rand(L.x_shape(), 21), rand(L.w_shape(), 22), rand(L.y_shape(), 23)
+    for gemm, loop, A, B in ((orc.conv_fwd_gemm, orc.conv_fwd, X, W), (orc.conv_dgrad_gemm, orc.conv_dgrad, W, dY),
+                             (orc.conv_wgrad_gemm, orc.conv_wgrad, dY, X)):
+        v, va = gemm(A, B, L, nb=nb)
+        ref, refa = loop(A, B, L)
+        np.testing.assert_allclose(v, ref, rtol=1e-11, atol=1e-11 * np.abs(ref).max())
+        np.testing.assert_allclose(va, refa, rtol=1e-5, atol=1e-6 * refa.max())

@@ -129,3 +129,63 @@ def test_square_blocks_of_cbf_im2col_are_microqonv_blocks(orc):
     idx = orc.im2col_index(LAYER, "cbf")
     M = np.where(idx >= 0, X.astype(np.float64).ravel()[np.maximum(idx, 0)], 0.0)
     np.testing.assert_array_equal(orc._fake_quantize_blocks(M, "e2m1", 8, 8), vals)
+
+
+def _line_block_matrix(fmt, rows, cols, br, bc, seed):
+    """A matrix whose br x bc blocks each hold grid values c * 448 * 2^(j - k)
+    (k = 0..3 varying from block to block) and one element of magnitude
+    maxB_ef * 448 * 2^(j - k).  With T_scale = 2^j (the largest block has
+    k = 0) every block's scale is 448 * 2^-k exactly and every code is c, so
+    fake quantization in exactly these blocks returns the matrix unchanged;
+    in blocks of another shape the block amax mixes different k, the small
+    values lose bits and the round trip breaks."""
+    import oracle
+    grid = oracle.format_grid(fmt)
+    emax, j = grid[-1], -3
+    rng = np.random.default_rng(seed)
+    M = np.zeros((rows, cols))
+    for b, (r0, c0) in enumerate((r, c) for r in range(0, rows, br) for c in range(0, cols, bc)):
+        k = (b * 7 + 1) % 4 if b else 0
+        vals = rng.choice(grid, size=(br, bc)) * rng.choice([-1.0, 1.0], size=(br, bc))
+        vals.flat[rng.integers(br * bc)] = emax
+        M[r0:r0 + br, c0:c0 + bc] = vals * 448.0 * 2.0 ** (j - k)
+    return M
+
+
+@pytest.mark.parametrize("fmt", ["e2m1", "e2m3", "e4m3"])
+@pytest.mark.parametrize("br,bc", [(64, 1), (1, 64), (8, 8)])
+def test_line_block_round_trip(orc, fmt, br, bc):
+    """DaCapo's line blocks of 64 along either GEMM direction (MicroQonv
+    §III-C) and the 8x8 squares: lossless round trip in the right blocks,
+    lossy in the transposed ones."""
+    M = _line_block_matrix(fmt, 128, 128, br, bc, 7 + br)
+    np.testing.assert_array_equal(orc._fake_quantize_blocks(M, fmt, br, bc), M)
+    if br != bc:
+        assert not np.array_equal(orc._fake_quantize_blocks(M, fmt, bc, br), M)
+
+
+def test_dacapo_flow_blocks_follow_each_gemm_direction(orc):
+    """flow_dacapo quantizes X' = im2col(X) twice from full precision: along
+    K (its rows, 64-line blocks in a column) for the forward GEMM and along
+    the (N Ho Wo) axis (64-line blocks in a row) for the weight gradient
+    (MicroQonv §III-C).  A constant activation tensor on the grid round-trips
+    exactly in both (every line block holds the constant or padding zeros);
+    with random activations both are valid fake quantizations of X' whose
+    copies of one activation differ between the two directions."""
+    L = Layer(8, 64, 8, 8, 16, 3, 1, 1)       # K = 576 and Ho Wo N = 512: both multiples of 64
+    X = np.full(L.x_shape(), 1.5 * 448 * 2.0 ** -4, dtype=np.float32)
+    Qf, Qb, idx = orc.flow_dacapo(X, L, "e2m1")
+    M = np.where(idx >= 0, X.astype(np.float64).ravel()[np.maximum(idx, 0)], 0.0)
+    np.testing.assert_array_equal(Qf, M)
+    np.testing.assert_array_equal(Qb, M)
+    X = S.draw_x(S.WORKLOADS[0], 0, L.x_shape())
+    Qf, Qb, idx = orc.flow_dacapo(X, L, "e2m1")
+    M = np.where(idx >= 0, X.astype(np.float64).ravel()[np.maximum(idx, 0)], 0.0)
+    assert Qf.shape == Qb.shape == M.shape == (576, 512)
+    assert np.all((idx >= 0) | (Qf == 0)) and np.all((idx >= 0) | (Qb == 0))
+    # the two directions agree with 64-line blocks computed column by column / row by row
+    np.testing.assert_array_equal(Qf[:, :1], orc._fake_quantize_blocks(M, "e2m1", 64, 1)[:, :1])
+    rel_f = np.abs(Qf - M).sum() / np.abs(M).sum()
+    rel_b = np.abs(Qb - M).sum() / np.abs(M).sum()
+    assert 0 < rel_f < 0.2 and 0 < rel_b < 0.2
+    assert not np.array_equal(Qf, Qb)
