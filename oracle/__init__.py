@@ -63,6 +63,10 @@ def lib() -> ctypes.CDLL:
         L.orc_num_blocks.argtypes = [ctypes.c_int, P]
         L.orc_num_blocks.restype = i64
         L.orc_quantize.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P]
+        L.orc_quantize_sr.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_uint64,
+                                      P, P, P, P]
+        L.orc_philox4x32_10.argtypes = [P, P, P]
+        L.orc_philox4x32_10.restype = None
         L.orc_dequantize.argtypes = [P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int, P, P]
         for name in ("orc_conv_fwd", "orc_conv_dgrad", "orc_conv_wgrad"):
             getattr(L, name).argtypes = [P, P, P, P, P]
@@ -123,12 +127,14 @@ def packed_sizes(fmt: str, role: str, dims) -> Dict[str, int]:
 
 
 def quantize(src: np.ndarray, fmt: str, role: str, layout: str,
-             amax_in: Optional[float] = None) -> Dict[str, object]:
+             amax_in: Optional[float] = None, sr_seed: Optional[int] = None) -> Dict[str, object]:
     """Quantize a dense fp32 tensor once into packed 8x8 blocks.
 
     dims are read from the logical shape: act/grad (N, C, H, W) whatever the
     memory layout; weight (Cout, Cin, Kh, Kw).  For layout "hwcn" `src` must
-    have memory shape (H, W, C, N).
+    have memory shape (H, W, C, N).  sr_seed: None for round-to-nearest
+    element codes, else stochastic rounding with that 64-bit Philox key
+    (mqoracle.c, "stochastic rounding").
     """
     src = np.ascontiguousarray(src, dtype=np.float32)
     if layout == "hwcn":
@@ -143,12 +149,28 @@ def quantize(src: np.ndarray, fmt: str, role: str, layout: str,
     s_t = ctypes.c_float(0.0)
     amax = ctypes.c_float(0.0)
     ain = ctypes.c_float(amax_in) if amax_in is not None else None
-    rc = lib().orc_quantize(_p(src), LAYOUTS[layout], ROLES[role], FORMATS[fmt], _p(d),
-                            ctypes.byref(ain) if ain is not None else None,
-                            _p(codes), _p(scales), ctypes.byref(s_t), ctypes.byref(amax))
+    if sr_seed is None:
+        rc = lib().orc_quantize(_p(src), LAYOUTS[layout], ROLES[role], FORMATS[fmt], _p(d),
+                                ctypes.byref(ain) if ain is not None else None,
+                                _p(codes), _p(scales), ctypes.byref(s_t), ctypes.byref(amax))
+    else:
+        rc = lib().orc_quantize_sr(_p(src), LAYOUTS[layout], ROLES[role], FORMATS[fmt], _p(d),
+                                   ctypes.byref(ain) if ain is not None else None,
+                                   ctypes.c_uint64(sr_seed & 0xFFFFFFFFFFFFFFFF),
+                                   _p(codes), _p(scales), ctypes.byref(s_t), ctypes.byref(amax))
     _check(rc, "quantize")
     return {"codes": codes, "scales": scales, "s_t": float(s_t.value), "amax": float(amax.value),
             "fmt": fmt, "role": role, "dims": tuple(int(x) for x in dims)}
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    """The four 32-bit output words of Philox4x32-10 for a counter (4 words)
+    and key (2 words)."""
+    c = np.asarray(ctr, dtype=np.uint32)
+    k = np.asarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_p(c), _p(k), _p(out))
+    return out
 
 
 def dequantize(q: Dict[str, object]) -> np.ndarray:

@@ -229,9 +229,12 @@ static int valid_dims(int role, const int64_t d[4]) {
  * in the Hindsight scheme the paper uses in §VII).  Writes codes, one E4M3
  * scale byte per block, T_scale, and the tensor's measured amax.
  */
-int orc_quantize(const float *src, int layout, int role, int fmt, const int64_t d[4],
-                 const float *amax_in, uint8_t *codes, uint8_t *scales,
-                 float *s_t_out, float *amax_out) {
+static unsigned sr_round_mag(const double *grid, int n, float ax, float bs, float s_t, uint32_t word);
+static uint32_t philox_word(uint64_t seed, int64_t index);
+
+static int quantize_impl(const float *src, int layout, int role, int fmt, const int64_t d[4],
+                         const float *amax_in, uint8_t *codes, uint8_t *scales,
+                         float *s_t_out, float *amax_out, int stochastic, uint64_t seed) {
   fmt_t f, f8;
   if (!fmt_get(fmt, &f) || !fmt_get(ORC_E4M3, &f8) || !valid_dims(role, d)) return ORC_ERR_ARG;
   if ((role == ORC_ROLE_WEIGHT) != (layout == ORC_OIHW)) return ORC_ERR_ARG;
@@ -279,15 +282,102 @@ int orc_quantize(const float *src, int layout, int role, int fmt, const int64_t 
     if (s_t > 0.0f) bs_code = round_mag(grid8, cnt8, (double)amax_b / (emax * (double)s_t));
     double bs = grid8[bs_code];
     scales[blk] = (uint8_t)bs_code;
-    /* step 4: element codes, nearest grid value to x / (B_scale * T_scale) */
+    /* step 4: element codes, nearest grid value to x / (B_scale * T_scale)
+     * (stochastic: one of the two grid values around it, see sr_round_mag) */
     uint8_t *out = codes + blk * bb;
     for (int i = 0; i < 64; ++i) {
       unsigned mag = 0;
-      if (bs > 0.0) mag = round_mag(grid, cnt, fabs((double)x[i]) / (bs * (double)s_t));
+      if (bs > 0.0) {
+        if (stochastic)
+          mag = sr_round_mag(grid, cnt, fabsf(x[i]), (float)bs, s_t, philox_word(seed, blk * 64 + i));
+        else
+          mag = round_mag(grid, cnt, fabs((double)x[i]) / (bs * (double)s_t));
+      }
       put_code(fmt, out, i, mag | (signbit(x[i]) ? sbit : 0u));
     }
   }
   return ORC_OK;
+}
+
+int orc_quantize(const float *src, int layout, int role, int fmt, const int64_t d[4],
+                 const float *amax_in, uint8_t *codes, uint8_t *scales,
+                 float *s_t_out, float *amax_out) {
+  return quantize_impl(src, layout, role, fmt, d, amax_in, codes, scales, s_t_out, amax_out, 0, 0);
+}
+
+/* ----------------------------------------------------- stochastic rounding */
+/*
+ * MicroQonv §III-A lets Round be round-to-nearest or stochastic, and uses
+ * stochastic rounding for gradients (paperlayer summary, §III-A).  The pages
+ * fix neither the random source nor the precision of the decision; these are
+ * the readings taken (the kernels implement the same steps):
+ *
+ *   random source  Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel
+ *                  random numbers: as easy as 1, 2, 3", SC 2011), keyed by a
+ *                  64-bit seed (low word k0, high word k1); element e of the
+ *                  packed tensor (e = block * 64 + in-block index) takes
+ *                  output word e % 4 of the counter (e / 4 low, e / 4 high,
+ *                  0, 0), and its top 24 bits r.
+ *   quotient       q = fl32(|x| / fl32(B_scale * T_scale)): one fp32 product
+ *                  and one IEEE fp32 division (the kernel's precision).
+ *   decision       q >= maxB_ef: the largest code.  Otherwise lo <= q < hi
+ *                  are adjacent grid values (hi - lo is a power of two) and
+ *                  the code is hi when r < ((q - lo) / (hi - lo)) * 2^24,
+ *                  else lo -- every step exact in fp32, so the probability of
+ *                  hi is ceil(2^24 (q - lo) / (hi - lo)) / 2^24: the expected
+ *                  code value is q to within 2^-24 of the grid spacing.
+ * The block scale stays round-to-nearest (CastE4M3 of §III-A).
+ */
+
+/* one Philox4x32 round: two 32x32 -> 64-bit products, then the bijection */
+static void philox_round(uint32_t c[4], const uint32_t k[2]) {
+  const uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+  const uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+  const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+  const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+  uint32_t n0 = hi1 ^ c[1] ^ k[0], n1 = lo1, n2 = hi0 ^ c[3] ^ k[1], n3 = lo0;
+  c[0] = n0; c[1] = n1; c[2] = n2; c[3] = n3;
+}
+
+/* Philox4x32-10: ten rounds, the key bumped by the Weyl constants between them */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]}, k[2] = {key[0], key[1]};
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) { k[0] += 0x9E3779B9u; k[1] += 0xBB67AE85u; }
+    philox_round(c, k);
+  }
+  for (int i = 0; i < 4; ++i) out[i] = c[i];
+}
+
+static uint32_t philox_word(uint64_t seed, int64_t index) {
+  const uint64_t q = (uint64_t)index >> 2;
+  const uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32), 0u, 0u};
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  orc_philox4x32_10(ctr, key, out);
+  return out[index & 3];
+}
+
+/* Stochastic magnitude code of |x| for block scale bs and T_scale s_t, from
+ * one 32-bit random word (steps above; fp32 arithmetic throughout). */
+static unsigned sr_round_mag(const double *grid, int n, float ax, float bs, float s_t, uint32_t word) {
+  volatile float d = bs * s_t;   /* fl32 product */
+  volatile float q = ax / d;     /* IEEE fp32 division */
+  if (!(q > 0.0f)) return 0u;
+  if ((double)q >= grid[n - 1]) return (unsigned)(n - 1);
+  int lo = 0;
+  while ((double)q >= grid[lo + 1]) ++lo;            /* grid[lo] <= q < grid[lo + 1] */
+  const float g_lo = (float)grid[lo], g_hi = (float)grid[lo + 1];
+  volatile float frac = (q - g_lo) / (g_hi - g_lo);  /* exact: Sterbenz, then a power of two */
+  volatile float scaled = frac * 16777216.0f;        /* x 2^24, exact */
+  const uint32_t r = word >> 8;                      /* top 24 bits */
+  return ((float)r < scaled) ? (unsigned)(lo + 1) : (unsigned)lo;
+}
+
+int orc_quantize_sr(const float *src, int layout, int role, int fmt, const int64_t d[4],
+                    const float *amax_in, uint64_t seed, uint8_t *codes, uint8_t *scales,
+                    float *s_t_out, float *amax_out) {
+  return quantize_impl(src, layout, role, fmt, d, amax_in, codes, scales, s_t_out, amax_out, 1, seed);
 }
 
 /* Fake-quantized (dequantized) values, dense fp64: NCHW for activations and
