@@ -381,28 +381,28 @@ def im2col_index(layer, order: str = "cbf") -> np.ndarray:
 
 def _fake_quantize_blocks(M: np.ndarray, fmt: str, br: int, bc: int):
     """Two-level microscaling of a 2-D fp64 matrix in br x bc blocks (the same
-    steps as the quantizer: tensor scale, per-block E4M3 scale, element codes),
-    returning fake-quantized values.  Rows/cols must divide by br/bc."""
+    steps as the quantizer: tensor scale from the whole matrix, per-block E4M3
+    scale, element codes; quotients in fp64 as in mqoracle.c), returning
+    fake-quantized values.  A ragged last block row / column is a partial
+    block (the same as padding it with zeros, which change no block amax and
+    quantize to zero)."""
+    M = np.asarray(M, dtype=np.float64)
     grid = format_grid(fmt)
     emax = grid[-1]
     amax = float(np.max(np.abs(M))) if M.size else 0.0
     s_t = tensor_scale(fmt, np.float32(amax))
     R, C = M.shape
-    out = np.zeros_like(M)
-    for r0 in range(0, R, br):
-        for c0 in range(0, C, bc):
-            blk = M[r0:r0 + br, c0:c0 + bc]
-            ab = float(np.max(np.abs(blk)))
-            if s_t > 0:
-                bs = decode("e4m3", round_codes("e4m3", np.array([ab / (emax * s_t)])))[0]
-            else:
-                bs = 0.0
-            if bs > 0:
-                q = decode(fmt, round_codes(fmt, blk / (bs * s_t)))
-            else:
-                q = np.zeros_like(blk)
-            out[r0:r0 + br, c0:c0 + bc] = q * bs * s_t
-    return out
+    Rp, Cp = -(-R // br) * br, -(-C // bc) * bc
+    P = np.zeros((Rp, Cp))
+    P[:R, :C] = M
+    B = P.reshape(Rp // br, br, Cp // bc, bc)            # block (i, j) is B[i, :, j, :]
+    ab = np.abs(B).max(axis=(1, 3))
+    bs = decode("e4m3", round_codes("e4m3", ab / (emax * s_t))) if s_t > 0 else np.zeros_like(ab)
+    d = (bs * s_t)[:, None, :, None]
+    q = np.zeros_like(B)
+    np.divide(B, d, out=q, where=np.broadcast_to(d > 0, B.shape))
+    out = decode(fmt, round_codes(fmt, q)) * d
+    return out.reshape(Rp, Cp)[:R, :C]
 
 
 def flow_quantize_after_im2col(X: np.ndarray, layer, fmt: str):
@@ -423,9 +423,7 @@ def flow_dacapo(X: np.ndarray, layer, fmt: str):
     idx = im2col_index(layer, "standard")
     Xf = np.asarray(X, dtype=np.float64).ravel()
     M = np.where(idx >= 0, Xf[np.maximum(idx, 0)], 0.0)
-    Qf = _fake_quantize_blocks(M, fmt, 64, 1) if M.shape[0] % 64 == 0 else None
-    Qb = _fake_quantize_blocks(M, fmt, 1, 64) if M.shape[1] % 64 == 0 else None
-    return Qf, Qb, idx
+    return _fake_quantize_blocks(M, fmt, 64, 1), _fake_quantize_blocks(M, fmt, 1, 64), idx
 
 
 def flow_quantization_counts(layer, flow: str) -> Dict[str, np.ndarray]:
@@ -509,3 +507,74 @@ def unpack_codes(q: Dict[str, object]) -> np.ndarray:
         bits = np.unpackbits(raw, axis=1, bitorder="little").reshape(-1, 64, 6)
         return (bits * (1 << np.arange(6, dtype=np.uint8))).sum(axis=2).astype(np.uint8)
     return raw.copy()
+
+
+# ------------------------------------------------- quantization error (Table II)
+#
+# MicroQonv §IV-D measures the average per-element quantization MSE of the
+# weights (W), activations (A) and output gradients (G), normalized by
+# MicroQonv's (Table II: DaCapo 0.891 / 0.982 / 0.827, Cuyckens et al.
+# 0.875 / 0.992 / 0.996, MicroQonv+ 0.236 / 1.0 / 1.0 for A / W / G).  The
+# pages do not spell the averaging out; the readings taken here:
+#   * A is averaged over the valid entries of the standard im2col X' (every
+#     copy an operand of the GEMMs; padding excluded) for every flow --
+#     MicroQonv's copies all carry their source element's one error;
+#   * a flow that quantizes a tensor twice (DaCapo, once per GEMM it feeds)
+#     contributes the mean of its two MSEs;
+#   * the GEMM matrices are X' (rows (ci, kh, kw), columns (n, ho, wo)),
+#     W_f = W.reshape(Cout, Cin Kh Kw) and G_Y as (Cout, N Ho Wo):
+#       microqonv  X, W, G quantized once in the CBF 8x8 blocks (§IV-B);
+#       cuyckens   8x8 squares of X', W_f and G_Y (§III-C, extrapolated);
+#       dacapo     64-line blocks along each GEMM's reduction: X' along K
+#                  (fwd) and along (n, ho, wo) (wgrad), W_f along K (fwd) and
+#                  along Cout (dgrad), G_Y along Cout (dgrad) and along
+#                  (n, ho, wo) (wgrad) (§III-C);
+#       microqonv+ as microqonv with the activations in a 6-bit format.
+
+def quantization_mse(X: np.ndarray, W: np.ndarray, G: np.ndarray, layer, fmt: str = "e2m1",
+                     fmt_plus: str = "e2m3") -> Dict[str, Dict[str, float]]:
+    """Per-element quantization MSE {flow: {"A", "W", "G"}} of one layer's
+    tensors (fp32 values; X NCHW, W OIHW, G NCHW) under the flows above."""
+    L = layer
+    X64, W64, G64 = (np.asarray(a, dtype=np.float64) for a in (X, W, G))
+    idx = im2col_index(L, "standard")
+    valid = idx >= 0
+    Xp = np.where(valid, X64.ravel()[np.maximum(idx, 0)], 0.0)
+    Wf = W64.reshape(L.Cout, -1)
+    Gm = G64.transpose(1, 0, 2, 3).reshape(L.Cout, -1)
+
+    def mse(Q, R, mask=None):
+        e = (Q - R) ** 2
+        return float(e[mask].mean() if mask is not None else e.mean())
+
+    def cbf(a, f, role, layout):
+        return dequantize(quantize(np.asarray(a, dtype=np.float32), f, role, layout))
+
+    def a_from_x(xhat):      # error of each X' copy = error of its source element
+        return mse(np.where(valid, xhat.ravel()[np.maximum(idx, 0)], 0.0), Xp, valid)
+
+    fq = _fake_quantize_blocks
+    out = {
+        "microqonv": {"A": a_from_x(cbf(X, fmt, "act", "nchw")), "W": mse(cbf(W, fmt, "weight", "oihw"), W64),
+                      "G": mse(cbf(G, fmt, "grad", "nchw"), G64)},
+        "cuyckens": {"A": mse(fq(Xp, fmt, 8, 8), Xp, valid), "W": mse(fq(Wf, fmt, 8, 8), Wf),
+                     "G": mse(fq(Gm, fmt, 8, 8), Gm)},
+        "dacapo": {"A": 0.5 * (mse(fq(Xp, fmt, 64, 1), Xp, valid) + mse(fq(Xp, fmt, 1, 64), Xp, valid)),
+                   "W": 0.5 * (mse(fq(Wf, fmt, 1, 64), Wf) + mse(fq(Wf, fmt, 64, 1), Wf)),
+                   "G": 0.5 * (mse(fq(Gm, fmt, 64, 1), Gm) + mse(fq(Gm, fmt, 1, 64), Gm))},
+    }
+    out["microqonv+"] = {"A": a_from_x(cbf(X, fmt_plus, "act", "nchw")), "W": out["microqonv"]["W"],
+                         "G": out["microqonv"]["G"]}
+    return out
+
+
+def normalized_mse(per_layer, weights=None) -> Dict[str, Dict[str, float]]:
+    """Element-weighted mean over layers of each flow's MSE, divided by
+    MicroQonv's (Table II's normalization).  weights: {tensor: [count per layer]}."""
+    flows, tensors = per_layer[0].keys(), ("A", "W", "G")
+    tot = {f: {t: 0.0 for t in tensors} for f in flows}
+    for i, m in enumerate(per_layer):
+        for f in flows:
+            for t in tensors:
+                tot[f][t] += m[f][t] * (weights[t][i] if weights else 1.0)
+    return {f: {t: tot[f][t] / tot["microqonv"][t] for t in tensors} for f in flows}

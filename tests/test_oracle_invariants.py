@@ -146,19 +146,21 @@ def _line_block_matrix(fmt, rows, cols, br, bc, seed):
     M = np.zeros((rows, cols))
     for b, (r0, c0) in enumerate((r, c) for r in range(0, rows, br) for c in range(0, cols, bc)):
         k = (b * 7 + 1) % 4 if b else 0
-        vals = rng.choice(grid, size=(br, bc)) * rng.choice([-1.0, 1.0], size=(br, bc))
-        vals.flat[rng.integers(br * bc)] = emax
-        M[r0:r0 + br, c0:c0 + bc] = vals * 448.0 * 2.0 ** (j - k)
+        h, w = min(br, rows - r0), min(bc, cols - c0)     # partial blocks at ragged edges
+        vals = rng.choice(grid, size=(h, w)) * rng.choice([-1.0, 1.0], size=(h, w))
+        vals.flat[rng.integers(h * w)] = emax
+        M[r0:r0 + h, c0:c0 + w] = vals * 448.0 * 2.0 ** (j - k)
     return M
 
 
 @pytest.mark.parametrize("fmt", ["e2m1", "e2m3", "e4m3"])
 @pytest.mark.parametrize("br,bc", [(64, 1), (1, 64), (8, 8)])
-def test_line_block_round_trip(orc, fmt, br, bc):
+@pytest.mark.parametrize("rows,cols", [(128, 128), (100, 72)], ids=["whole-blocks", "ragged"])
+def test_line_block_round_trip(orc, fmt, br, bc, rows, cols):
     """DaCapo's line blocks of 64 along either GEMM direction (MicroQonv
-    §III-C) and the 8x8 squares: lossless round trip in the right blocks,
-    lossy in the transposed ones."""
-    M = _line_block_matrix(fmt, 128, 128, br, bc, 7 + br)
+    §III-C) and the 8x8 squares: lossless round trip in the right blocks
+    (partial ones at ragged edges included), lossy in the transposed ones."""
+    M = _line_block_matrix(fmt, rows, cols, br, bc, 7 + br)
     np.testing.assert_array_equal(orc._fake_quantize_blocks(M, fmt, br, bc), M)
     if br != bc:
         assert not np.array_equal(orc._fake_quantize_blocks(M, fmt, bc, br), M)
@@ -172,7 +174,7 @@ def test_dacapo_flow_blocks_follow_each_gemm_direction(orc):
     exactly in both (every line block holds the constant or padding zeros);
     with random activations both are valid fake quantizations of X' whose
     copies of one activation differ between the two directions."""
-    L = Layer(8, 64, 8, 8, 16, 3, 1, 1)       # K = 576 and Ho Wo N = 512: both multiples of 64
+    L = Layer(8, 64, 8, 8, 16, 3, 1, 1)       # K = 576, Ho Wo N = 512
     X = np.full(L.x_shape(), 1.5 * 448 * 2.0 ** -4, dtype=np.float32)
     Qf, Qb, idx = orc.flow_dacapo(X, L, "e2m1")
     M = np.where(idx >= 0, X.astype(np.float64).ravel()[np.maximum(idx, 0)], 0.0)
