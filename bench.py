@@ -408,6 +408,129 @@ def barrier(world):
         dist.barrier()
 
 
+def time_quantizer(mq, torch, src, layout, role, fmt, dims, flush, reps=8):
+    """Median CUDA-event time (ms) of quantizing `src` in single-pass mode
+    (statistic supplied: the tensor's own amax) and in exact two-pass mode,
+    L2 flushed before each rep; returns {mode: ms}."""
+    dev = src.device
+    p = mq.Packed(fmt, role, dims, device=dev)
+    stat = torch.zeros(1, device=dev)
+    aout = torch.zeros(1, device=dev)
+    mq.quantize_cbf(src, layout, p, amax_out=stat)
+    out = {}
+    for mode in ("single_pass", "two_pass"):
+        ts = []
+        for i in range(reps + 2):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            if mode == "single_pass":
+                mq.quantize_cbf(src, layout, p, amax_in=stat, amax_out=aout)
+            else:
+                mq.quantize_cbf(src, layout, p, amax_out=aout)
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 2:
+                ts.append(e0.elapsed_time(e1))
+        out[mode] = statistics.median(ts)
+    return out
+
+
+def quantizer_entry(ms, in_bytes, fmt, elems, peaks):
+    """GB/s and fraction of the HBM copy peak on the one-read byte count
+    (input + packed output); the two-pass figure also on its two-read count."""
+    one = in_bytes + packed_bytes(fmt, elems)
+    d = {"bytes_one_read": one}
+    for mode, t in ms.items():
+        gbs = one / (t * 1e-3) / 1e9
+        d[mode] = {"us": t * 1e3, "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
+    d["two_pass"]["frac_hbm_two_reads"] = (one + in_bytes) / (ms["two_pass"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
+    return d
+
+
+def layer_rows(wl, per_layer, peaks, launch_bound_us=5.0):
+    """Per layer and op: time, TFLOP/s and fraction of the roofline (burst
+    bf16 and the HBM copy); ops whose roofline time is below launch_bound_us
+    are labelled launch-bound (their time is launch and pipeline latency)."""
+    rows = []
+    for li, L in enumerate(wl.layers):
+        if (li, "fwd") not in per_layer:
+            break
+        row = {"layer": L.name()}
+        xe, we, ye = (int(np.prod(sh)) for sh in (L.x_shape(), L.w_shape(), L.y_shape()))
+        fb = packed_bytes(wl.fmt, 1)
+        byts = {"fwd": fb * (xe + we) + 4 * ye, "dgrad": fb * (we + ye) + 4 * xe, "wgrad": fb * (ye + xe) + 4 * we}
+        for op in ("fwd", "dgrad", "wgrad"):
+            v = per_layer[(li, op)]
+            t = sum(v) / len(v)
+            t_flop = L.flops / (peaks["bf16_tflops"] * 1e12)
+            t_byte = byts[op] / (peaks["hbm_gbs"] * 1e9)
+            row[op] = {"ms": t, "tflops": L.flops / (t * 1e-3) / 1e12, "frac_roofline": max(t_flop, t_byte) / (t * 1e-3),
+                       "bound": "tensor" if t_flop >= t_byte else "hbm"}
+            if max(t_flop, t_byte) * 1e6 < launch_bound_us:
+                row[op]["launch_bound"] = True
+        rows.append(row)
+    return rows
+
+
+def extra_workload(name, device, peaks, steps, flush):
+    """One more workload after the headline: its whole step as a CUDA graph
+    (per-op and per-layer CUDA-event times), and the quantizer alone on each
+    of its activation and output-gradient tensors of 8 MB or more."""
+    import torch
+    import microscaling_quantized_convolution_only_b300 as mq
+    wl = S.WORKLOADS[WORKLOADS[name]]
+    step = make_step(wl, device)
+    for _ in range(3):
+        step.run()
+    torch.cuda.synchronize()
+    graph, tm = torch.cuda.CUDAGraph(), OpTimer()
+    with torch.cuda.graph(graph):
+        step.run(tm)
+    per_op, per_layer, step_ms = {}, {}, []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+        for g, v in tm.times().items():
+            per_op.setdefault(g, []).extend(v)
+        for k, v in tm.layer_times().items():
+            per_layer.setdefault(k, []).extend(v)
+    mq.check_device_status()
+    ms = statistics.median(step_ms)
+    flops = sum(step.flops.values())
+    ops = {}
+    for op in ("fwd", "dgrad", "wgrad"):
+        t = sum(per_op[op]) / steps
+        ops[op] = {"ms_per_step": t, "tflops": step.flops[op] / (t * 1e-3) / 1e12}
+    quant = {}
+    in_b = 2 if wl.dtype == "bf16" else 4
+    tensors = []
+    if wl.chained:
+        L = wl.layers[0]
+        tensors = [("X0", step.x0, "act", L.x_shape()), ("dY3", step.dy, "grad", L.y_shape())]
+    else:
+        for li, d in enumerate(step.layers):
+            L = d["L"]
+            tensors += [(f"L{li}.X", d["x"], "act", L.x_shape()), (f"L{li}.dY", d["dy"], "grad", L.y_shape())]
+    for tname, t, role, dims in tensors:
+        if t.numel() * in_b < 8e6:
+            continue
+        qms = time_quantizer(mq, torch, t, "nchw", role, wl.fmt, dims, flush)
+        quant[tname] = quantizer_entry(qms, t.numel() * in_b, wl.fmt, t.numel(), peaks)
+    out = {"ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12, "conv_flops_per_step": flops,
+           "element_format": wl.fmt, "input_dtype": wl.dtype, "steps": steps, "ops": ops,
+           "layers": layer_rows(wl, per_layer, peaks), "quantizer_per_tensor": quant,
+           "execution": "one CUDA graph per step, L2 flushed (256 MB write) before each; quantizer timed alone"}
+    del graph, step
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import torch
     import microscaling_quantized_convolution_only_b300 as mq
@@ -533,19 +656,12 @@ def run_gpu(args):
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "traffic_kind": traffic_kind, "peak_source": f"{peaks['source']} HBM copy"}
 
-    layers_out = []
-    for li, L in enumerate(wl.layers):
-        if (li, "fwd") not in per_layer:
-            break
-        row = {"layer": L.name()}
-        xe, we, ye = (int(np.prod(sh)) for sh in (L.x_shape(), L.w_shape(), L.y_shape()))
-        fb = packed_bytes(wl.fmt, 1)
-        byts = {"fwd": fb * (xe + we) + 4 * ye, "dgrad": fb * (we + ye) + 4 * xe, "wgrad": fb * (ye + xe) + 4 * we}
-        for op in ("fwd", "dgrad", "wgrad"):
-            t = mean(per_layer[(li, op)])
-            t_roof = max(L.flops / (pk_t * 1e12), byts[op] / (peaks["hbm_gbs"] * 1e9))
-            row[op] = {"ms": t, "tflops": L.flops / (t * 1e-3) / 1e12, "frac_roofline": t_roof / (t * 1e-3)}
-        layers_out.append(row)
+    layers_out = layer_rows(wl, per_layer, peaks)
+    # the quantizer alone on the headline's largest input, single-pass and exact two-pass
+    if wl.chained:
+        in_b = 2 if wl.dtype == "bf16" else 4
+        qms = time_quantizer(mq, torch, step.x0, "nchw", "act", wl.fmt, wl.layers[0].x_shape(), flush)
+        ops["quantize_x0"] = quantizer_entry(qms, step.x0.numel() * in_b, wl.fmt, step.x0.numel(), peaks)
 
     # ---- end to end through the public API with host buffers
     pinned = step.pinned()
@@ -631,6 +747,15 @@ def run_gpu(args):
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": step.h2d_bytes,
                 "d2h_bytes_per_step": step.d2h_bytes, "ms_per_step": e2e_max / len(e2e_ms)},
     }
+    if world == 1 and not args.no_extra_workloads and not args.batch:
+        # every other workload after the headline (per-layer fractions, quantizer per tensor)
+        del step, pinned
+        torch.cuda.empty_cache()
+        extras = {}
+        for name in ("tiny-3x3", "resnet32-cifar", "resnet18-224", "yolov8n-640-fp8", "stack4-fp6"):
+            if WORKLOADS[name] != WORKLOADS[args.workload]:
+                extras[S.WORKLOADS[WORKLOADS[name]].name] = extra_workload(name, device, peaks, 3, flush)
+        result["workloads"] = extras
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     if rank == 0:
@@ -773,6 +898,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of one CUDA graph per step")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="time only the headline workload (the default also times the other workloads after it)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch N (multiple of 8) for small profiling captures; "
                          "the default runs the workload as specified")

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define MQCONV_ABI_VERSION 1
+#define MQCONV_ABI_VERSION 2
 
 /* cudaStream_t without including CUDA headers */
 typedef struct CUstream_st *mq_stream;
@@ -74,6 +74,19 @@ typedef enum { MQ_FMT_E2M1 = 4, MQ_FMT_E2M3 = 6, MQ_FMT_E4M3 = 8 } mq_format;
 typedef enum { MQ_ROLE_ACT = 0, MQ_ROLE_WEIGHT = 1, MQ_ROLE_GRAD = 2 } mq_role;
 typedef enum { MQ_DT_F32 = 0, MQ_DT_BF16 = 1 } mq_dtype;
 typedef enum { MQ_LAYOUT_NCHW = 0, MQ_LAYOUT_HWCN = 1, MQ_LAYOUT_OIHW = 2 } mq_layout;
+
+/* Rounding of the element codes (MicroQonv §III-A: Round is round-to-nearest
+ * or stochastic; the paper rounds gradients stochastically).  Block scales
+ * are always round-to-nearest (CastE4M3).  Stochastic rounding, as read
+ * here:  q = fl32(|x| / fl32(B_scale * T_scale)) (IEEE fp32 division);
+ * q >= maxB_ef gives the largest code; otherwise lo <= q < hi are the grid
+ * values around q and the code is hi when r < 2^24 (q - lo) / (hi - lo),
+ * else lo, with r the top 24 bits of word e % 4 of Philox4x32-10 (Salmon et
+ * al., SC 2011) under key (seed low, seed high) at counter (e / 4 low,
+ * e / 4 high, 0, 0), e = block * 64 + in-block index in packed order.  Every
+ * step is exact, so a seed determines the codes bit for bit; the expected
+ * code value is q to within 2^-24 of the grid spacing. */
+typedef enum { MQ_ROUND_RN = 0, MQ_ROUND_SR = 1 } mq_rounding;
 
 /* A tensor quantized once into packed 8x8 blocks (layout above). */
 typedef struct {
@@ -104,6 +117,8 @@ typedef struct {
   const float *amax_in;   /* device, 1 float: statistic T_scale is built from */
   const mq_packed *out;   /* packed Y (its fmt/role/dims must match) */
   float *amax_out;        /* device, 1 float or NULL: receives max|Y| */
+  int32_t rounding;       /* mq_rounding of the element codes (MQ_ROUND_RN: 0) */
+  uint64_t sr_seed;       /* Philox key of MQ_ROUND_SR; ignored otherwise */
 } mq_requant;
 
 int32_t mqconv_abi_version(void);
@@ -128,6 +143,15 @@ size_t mqconv_packed_scale_bytes(const int64_t dims[4]);
  */
 mq_status mqconv_quantize_cbf(const void *src, int32_t dtype, int32_t layout, const mq_packed *dst,
                               const float *amax_in, float *amax_out, mq_stream stream);
+
+/*
+ * mqconv_quantize_cbf with stochastically rounded element codes (mq_rounding
+ * above; MicroQonv §III-A, the paper's rounding of gradients), Philox key
+ * `seed`.  T_scale, block scales, layouts, statistic modes and errors as for
+ * mqconv_quantize_cbf.
+ */
+mq_status mqconv_quantize_cbf_sr(const void *src, int32_t dtype, int32_t layout, const mq_packed *dst,
+                                 const float *amax_in, float *amax_out, uint64_t seed, mq_stream stream);
 
 /*
  * Forward convolution on packed operands: Y = W_f * X' with X' the on-chip
@@ -214,6 +238,27 @@ mq_status mqconv_wgrad_noalloc(const mq_conv_desc *desc, const mq_packed *dyq, c
 /* Synchronize `stream`, copy the device status word (an OR of mq_status bit
  * flags 1 << MQ_ERR_*) to *host_status, and clear it. */
 mq_status mqconv_device_status(mq_stream stream, int32_t *host_status);
+
+/*
+ * Test support for the failure detection (not part of the method; the paper
+ * describes no runtime).  Every wait inside the convolution kernels is
+ * bounded (2 s): when one expires, the kernel ORs 1 << MQ_ERR_TIMEOUT into
+ * the device status word, lets the copies and MMAs it already issued land,
+ * frees its tensor memory and returns, so the CUDA context stays usable and
+ * the host learns of it from mqconv_device_status().
+ *   what  MQ_INJECT_NONE, or MQ_INJECT_WITHHOLD_ACC_RELEASE: in every later
+ *         launch of the halo forward / data-gradient kernel, one epilogue
+ *         warp of CTA 0 skips its release of the first accumulator slot, so
+ *         the MMA issuer's wait for that slot (on a second tile of CTA 0) can
+ *         only expire.  Nothing traps or faults; only a plain barrier
+ *         arrival is withheld.
+ * The setting is process-wide and applies until changed; MQ_ERR_INVALID_ARG
+ * for an unknown value.  Call with MQ_INJECT_NONE to restore normal
+ * operation.
+ */
+#define MQ_INJECT_NONE 0
+#define MQ_INJECT_WITHHOLD_ACC_RELEASE 1
+mq_status mqconv_test_fault_inject(int32_t what);
 
 #ifdef __cplusplus
 }

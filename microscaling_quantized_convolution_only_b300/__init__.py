@@ -4,9 +4,10 @@ Argument marshalling only: every step of quantization and convolution runs in
 the library's CUDA kernels.  PyTorch supplies device memory and streams.  There
 is no fallback: if libmqconv.so is missing or a call fails, this module raises.
 
-Entry points mirror the C names: quantize_cbf, fwd, dgrad (and, with rq_out,
-dgrad_requant), wgrad, wgrad_noalloc, wgrad_workspace_bytes,
-packed_code_bytes, packed_scale_bytes, device_status.
+Entry points mirror the C names: quantize_cbf (and, with sr_seed,
+quantize_cbf_sr), fwd, dgrad (and, with rq_out, dgrad_requant), wgrad,
+wgrad_noalloc, wgrad_workspace_bytes, packed_code_bytes, packed_scale_bytes,
+device_status, test_fault_inject.
 """
 from __future__ import annotations
 
@@ -42,7 +43,15 @@ class _Desc(ctypes.Structure):
 
 class _Requant(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("amax_in", ctypes.c_void_p), ("out", ctypes.POINTER(_Packed)),
-                ("amax_out", ctypes.c_void_p)]
+                ("amax_out", ctypes.c_void_p), ("rounding", ctypes.c_int32), ("sr_seed", ctypes.c_uint64)]
+
+
+def _requant(rq_out, rq_amax_in, rq_amax_out, sr_seed):
+    out_c = rq_out.c()
+    rq = _Requant(FMT[rq_out.fmt], _ptr(rq_amax_in), ctypes.pointer(out_c), _ptr(rq_amax_out),
+                  0 if sr_seed is None else 1, 0 if sr_seed is None else sr_seed & 0xFFFFFFFFFFFFFFFF)
+    rq._keep = out_c
+    return rq
 
 
 _lib = None
@@ -64,6 +73,7 @@ def lib() -> ctypes.CDLL:
         L.mqconv_packed_scale_bytes.argtypes = [P]
         L.mqconv_packed_scale_bytes.restype = ctypes.c_size_t
         L.mqconv_quantize_cbf.argtypes = [P, i32, i32, ctypes.POINTER(_Packed), P, P, P]
+        L.mqconv_quantize_cbf_sr.argtypes = [P, i32, i32, ctypes.POINTER(_Packed), P, P, ctypes.c_uint64, P]
         L.mqconv_fwd.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P,
                                  ctypes.POINTER(_Requant), P]
         L.mqconv_dgrad.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P, P]
@@ -76,8 +86,9 @@ def lib() -> ctypes.CDLL:
         L.mqconv_device_status.argtypes = [P, ctypes.POINTER(i32)]
         L.mqconv_wgrad_noalloc.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P,
                                            P]
-        for f in ("mqconv_quantize_cbf", "mqconv_fwd", "mqconv_dgrad", "mqconv_dgrad_requant", "mqconv_wgrad",
-                  "mqconv_device_status", "mqconv_wgrad_noalloc"):
+        L.mqconv_test_fault_inject.argtypes = [i32]
+        for f in ("mqconv_quantize_cbf", "mqconv_quantize_cbf_sr", "mqconv_fwd", "mqconv_dgrad", "mqconv_dgrad_requant", "mqconv_wgrad",
+                  "mqconv_device_status", "mqconv_wgrad_noalloc", "mqconv_test_fault_inject"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -144,40 +155,49 @@ def desc(layer) -> _Desc:
 
 
 def quantize_cbf(src: torch.Tensor, layout: str, dst: Packed, amax_in: Optional[torch.Tensor] = None,
-                 amax_out: Optional[torch.Tensor] = None, stream=None) -> None:
-    """mqconv_quantize_cbf: quantize `src` (fp32/bf16, dense in `layout`) once into `dst`."""
+                 amax_out: Optional[torch.Tensor] = None, stream=None, sr_seed: Optional[int] = None) -> None:
+    """mqconv_quantize_cbf: quantize `src` (fp32/bf16, dense in `layout`) once into `dst`;
+    with sr_seed, mqconv_quantize_cbf_sr (stochastic element codes, Philox key sr_seed)."""
     if not src.is_contiguous():
         raise MQError("src must be contiguous")
     c = dst.c()
-    rc = lib().mqconv_quantize_cbf(src.data_ptr(), DTYPE[src.dtype], LAYOUT[layout], ctypes.byref(c),
-                                   _ptr(amax_in), _ptr(amax_out), _stream(stream))
-    _check(rc, "mqconv_quantize_cbf")
+    if sr_seed is None:
+        rc = lib().mqconv_quantize_cbf(src.data_ptr(), DTYPE[src.dtype], LAYOUT[layout], ctypes.byref(c),
+                                       _ptr(amax_in), _ptr(amax_out), _stream(stream))
+        _check(rc, "mqconv_quantize_cbf")
+    else:
+        rc = lib().mqconv_quantize_cbf_sr(src.data_ptr(), DTYPE[src.dtype], LAYOUT[layout], ctypes.byref(c),
+                                          _ptr(amax_in), _ptr(amax_out), ctypes.c_uint64(sr_seed & 0xFFFFFFFFFFFFFFFF),
+                                          _stream(stream))
+        _check(rc, "mqconv_quantize_cbf_sr")
 
 
 def fwd(layer, xq: Packed, wq: Packed, y: Optional[torch.Tensor], rq_out: Optional[Packed] = None,
-        rq_amax_in: Optional[torch.Tensor] = None, rq_amax_out: Optional[torch.Tensor] = None, stream=None) -> None:
-    """mqconv_fwd: Y (fp32, [Ho][Wo][Cout][N]) and/or the fused requantization of Y into rq_out."""
+        rq_amax_in: Optional[torch.Tensor] = None, rq_amax_out: Optional[torch.Tensor] = None, stream=None,
+        rq_sr_seed: Optional[int] = None) -> None:
+    """mqconv_fwd: Y (fp32, [Ho][Wo][Cout][N]) and/or the fused requantization of Y into rq_out
+    (stochastic element codes with Philox key rq_sr_seed when given)."""
     d, x, w = desc(layer), xq.c(), wq.c()
     rq_p = None
     if rq_out is not None:
-        out_c = rq_out.c()
-        rq = _Requant(FMT[rq_out.fmt], _ptr(rq_amax_in), ctypes.pointer(out_c), _ptr(rq_amax_out))
+        rq = _requant(rq_out, rq_amax_in, rq_amax_out, rq_sr_seed)
         rq_p = ctypes.byref(rq)
     rc = lib().mqconv_fwd(ctypes.byref(d), ctypes.byref(x), ctypes.byref(w), _ptr(y), rq_p, _stream(stream))
     _check(rc, "mqconv_fwd")
 
 
 def dgrad(layer, wq: Packed, dyq: Packed, dx: Optional[torch.Tensor], rq_out: Optional[Packed] = None,
-          rq_amax_in: Optional[torch.Tensor] = None, rq_amax_out: Optional[torch.Tensor] = None, stream=None) -> None:
+          rq_amax_in: Optional[torch.Tensor] = None, rq_amax_out: Optional[torch.Tensor] = None, stream=None,
+          rq_sr_seed: Optional[int] = None) -> None:
     """mqconv_dgrad: dX (fp32, [H][W][Cin][N]); with rq_out, mqconv_dgrad_requant: dX (optional) and its
-    fused requantization into rq_out (role grad, dims (N, Cin, H, W))."""
+    fused requantization into rq_out (role grad, dims (N, Cin, H, W); stochastic element codes with Philox
+    key rq_sr_seed when given)."""
     d, w, g = desc(layer), wq.c(), dyq.c()
     if rq_out is None:
         rc = lib().mqconv_dgrad(ctypes.byref(d), ctypes.byref(w), ctypes.byref(g), _ptr(dx), _stream(stream))
         _check(rc, "mqconv_dgrad")
         return
-    out_c = rq_out.c()
-    rq = _Requant(FMT[rq_out.fmt], _ptr(rq_amax_in), ctypes.pointer(out_c), _ptr(rq_amax_out))
+    rq = _requant(rq_out, rq_amax_in, rq_amax_out, rq_sr_seed)
     rc = lib().mqconv_dgrad_requant(ctypes.byref(d), ctypes.byref(w), ctypes.byref(g), _ptr(dx), ctypes.byref(rq),
                                     _stream(stream))
     _check(rc, "mqconv_dgrad_requant")
@@ -202,6 +222,15 @@ def wgrad_noalloc(layer, dyq: Packed, xq: Packed, dw: torch.Tensor, stream=None)
     d, g, x = desc(layer), dyq.c(), xq.c()
     rc = lib().mqconv_wgrad_noalloc(ctypes.byref(d), ctypes.byref(g), ctypes.byref(x), _ptr(dw), _stream(stream))
     _check(rc, "mqconv_wgrad_noalloc")
+
+
+INJECT = {"none": 0, "withhold_acc_release": 1}
+
+
+def test_fault_inject(what: str = "none") -> None:
+    """mqconv_test_fault_inject: test support for the failure detection (see
+    include/mqconv.h).  "none" restores normal operation."""
+    _check(lib().mqconv_test_fault_inject(INJECT[what]), "mqconv_test_fault_inject")
 
 
 def device_status(stream=None) -> int:

@@ -14,8 +14,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmqconv.so")
-SOURCES = ["api.cu", "quantize.cu", "conv.cu", "conv_halo.cu"]
-HEADERS = ["common.cuh", "kernels.h", os.path.join("..", "..", "include", "mqconv.h")]
+SOURCES = ["api.cu", "quantize.cu", "conv.cu", "conv_halo.cu", "conv_halo_fwd_a.cu", "conv_halo_fwd_b.cu", "conv_halo_dgrad_a.cu",
+           "conv_halo_dgrad_b.cu", "conv_halo_wide.cu"]
+HEADERS = ["common.cuh", "conv_halo.cuh", "kernels.h", os.path.join("..", "..", "include", "mqconv.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -71,7 +72,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     os.makedirs(OBJ, exist_ok=True)
     todo = [s for s in SOURCES if force or _obj_stale(s)]
-    with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         for f in [ex.submit(_compile, s, verbose) for s in todo]:
             f.result()
     cmd = [_nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-Xcompiler", "-fPIC",

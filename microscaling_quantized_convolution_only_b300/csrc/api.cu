@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/mqconv.h: argument checks, launch
 // planning and launches.  The library never allocates device memory.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstring>
 #include <mutex>
@@ -40,6 +41,9 @@ mq_status dev_info(DevInfo **out) {
   *out = &d;
   return MQ_OK;
 }
+
+// Fault injection of the failure-detection tests (mqconv_test_fault_inject).
+std::atomic<int> g_inject{0};
 
 bool fmt_ok(int32_t f) { return f == MQ_FMT_E2M1 || f == MQ_FMT_E2M3 || f == MQ_FMT_E4M3; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -90,6 +94,7 @@ mq::ConvParams base_params(const mq_conv_desc *d, int op, uint32_t *status) {
   p.CIG = p.Cin / 8;
   p.COG = p.Cout / 8;
   p.status = status;
+  p.inject = g_inject.load();
   return p;
 }
 
@@ -148,7 +153,7 @@ mq_status run_wgrad(mq::ConvParams &p, float *partials, size_t bytes, int max_sp
     mq::conv_plan(p);
     if (max_splits > 0 && p.k_splits > max_splits) {
       int per = (p.kg_total + max_splits - 1) / max_splits;
-      per = (per + 7) / 8 * 8;
+      per = (per + mq::CONV_KCH - 1) / mq::CONV_KCH * mq::CONV_KCH;
       p.kg_per_split = per;
       p.k_splits = (p.kg_total + per - 1) / per;
     }
@@ -208,6 +213,7 @@ mq_status conv_fwd_or_dgrad(int op, const mq_conv_desc *desc, const mq_packed *a
   if (out && !aligned16(out)) return MQ_ERR_ALIGNMENT;
   if (rq) {
     if (!rq->amax_in || !fmt_ok(rq->fmt) || !rq->out || rq->out->fmt != rq->fmt) return MQ_ERR_INVALID_ARG;
+    if (rq->rounding != MQ_ROUND_RN && rq->rounding != MQ_ROUND_SR) return MQ_ERR_INVALID_ARG;
     st = fwd ? check_packed(rq->out, MQ_ROLE_ACT, desc->N, desc->Cout, Ho, Wo)
              : check_packed(rq->out, MQ_ROLE_GRAD, desc->N, desc->Cin, desc->H, desc->W);
     if (st != MQ_OK) return st;
@@ -230,6 +236,8 @@ mq_status conv_fwd_or_dgrad(int op, const mq_conv_desc *desc, const mq_packed *a
     p.rq.amax_in = rq->amax_in;
     p.rq.amax_out_bits = reinterpret_cast<uint32_t *>(rq->amax_out);
     p.rq.fmt = rq->fmt;
+    p.rq.sr = rq->rounding == MQ_ROUND_SR ? 1 : 0;
+    p.rq.sr_seed = rq->sr_seed;
     if (rq->amax_out && cudaMemsetAsync(rq->amax_out, 0, sizeof(float), s) != cudaSuccess) return MQ_ERR_CUDA;
   }
   return run_conv(p, di->num_sms, s);
@@ -268,8 +276,9 @@ size_t mqconv_packed_scale_bytes(const int64_t dims[4]) {
   return (size_t)(dims[0] / 8) * (size_t)(dims[1] / 8) * (size_t)dims[2] * (size_t)dims[3];
 }
 
-mq_status mqconv_quantize_cbf(const void *src, int32_t dtype, int32_t layout, const mq_packed *dst,
-                              const float *amax_in, float *amax_out, mq_stream stream) {
+namespace {
+mq_status quantize_cbf(const void *src, int32_t dtype, int32_t layout, const mq_packed *dst, const float *amax_in,
+                       float *amax_out, int sr, uint64_t seed, mq_stream stream) {
   if (!src || !dst || !dst->codes || !dst->scales || !dst->s_t) return MQ_ERR_INVALID_ARG;
   if (!fmt_ok(dst->fmt) || (dtype != MQ_DT_F32 && dtype != MQ_DT_BF16)) return MQ_ERR_INVALID_ARG;
   if (dst->role != MQ_ROLE_ACT && dst->role != MQ_ROLE_WEIGHT && dst->role != MQ_ROLE_GRAD) return MQ_ERR_INVALID_ARG;
@@ -300,6 +309,8 @@ mq_status mqconv_quantize_cbf(const void *src, int32_t dtype, int32_t layout, co
   p.scales = dst->scales;
   p.s_t_out = dst->s_t;
   p.status = di->status;
+  p.sr = sr;
+  p.sr_seed = seed;
   if (!amax_in) {
     uint32_t *bits = reinterpret_cast<uint32_t *>(amax_out);
     if (cudaMemsetAsync(bits, 0, sizeof(uint32_t), s) != cudaSuccess) return MQ_ERR_CUDA;
@@ -313,6 +324,17 @@ mq_status mqconv_quantize_cbf(const void *src, int32_t dtype, int32_t layout, co
   }
   if (mq::launch_quantize(src, dtype, layout, dst->fmt, p, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
   return MQ_OK;
+}
+}  // namespace
+
+mq_status mqconv_quantize_cbf(const void *src, int32_t dtype, int32_t layout, const mq_packed *dst,
+                              const float *amax_in, float *amax_out, mq_stream stream) {
+  return quantize_cbf(src, dtype, layout, dst, amax_in, amax_out, 0, 0, stream);
+}
+
+mq_status mqconv_quantize_cbf_sr(const void *src, int32_t dtype, int32_t layout, const mq_packed *dst,
+                                 const float *amax_in, float *amax_out, uint64_t seed, mq_stream stream) {
+  return quantize_cbf(src, dtype, layout, dst, amax_in, amax_out, 1, seed, stream);
 }
 
 mq_status mqconv_fwd(const mq_conv_desc *desc, const mq_packed *xq, const mq_packed *wq, float *y,
@@ -383,6 +405,13 @@ mq_status mqconv_wgrad_noalloc(const mq_conv_desc *desc, const mq_packed *dyq, c
   if ((st = scratch_addr(&scratch)) != MQ_OK) return st;
   return run_wgrad(p, scratch, MQCONV_WGRAD_NOALLOC_SCRATCH_BYTES, (int)std::min<size_t>(max_splits, 1 << 20), dw,
                    di->num_sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mq_status mqconv_test_fault_inject(int32_t what) {
+  if (what != MQ_INJECT_NONE && what != MQ_INJECT_WITHHOLD_ACC_RELEASE) return MQ_ERR_INVALID_ARG;
+  static_assert(MQ_INJECT_WITHHOLD_ACC_RELEASE == mq::INJECT_WITHHOLD_ACC_RELEASE, "injection codes");
+  g_inject.store(what);
+  return MQ_OK;
 }
 
 mq_status mqconv_device_status(mq_stream stream, int32_t *host_status) {

@@ -96,6 +96,24 @@ template <int FMT> __device__ __forceinline__ float code_value(uint32_t mag) {
 // contain the exact quotient when q is computed with a few fp32 roundings.
 constexpr float QEPS = 9.5367431640625e-07f;   // 2^-20
 
+// Tiny tensor scales.  The bracket and tie-test arguments below need
+// B_scale * T_scale and maxB_ef * T_scale to be normal fp32 numbers, and the
+// exact difference in the fma tie test to be a multiple of 2^-149.  Both hold
+// for T_scale >= 2^-62 (the products are then >= 2^-71, and every term of the
+// difference is a multiple of 2^-107 or finer than 2^-149 only below
+// T_scale = 2^-107).  A tensor whose T_scale lies below 2^-62 (amax below
+// about 1.2e-15) -- including a subnormal T_scale, amax below about 3e-35 --
+// is encoded from x * 2^64 and T_scale * 2^64 instead: both products are exact
+// powers-of-two shifts, so every quotient x / (B_scale * T_scale) is the same
+// real number, and every intermediate is back in the range the arguments
+// cover.  An input beyond 2^64 (only possible with a supplied statistic far
+// below the data) would overflow; it is clamped to the largest finite value,
+// whose quotient saturates all the same.
+constexpr float TINY_ST = 0x1p-62f;
+constexpr float TINY_MULT = 0x1p64f;
+__device__ __forceinline__ bool is_tiny_scale(float s_t) { return s_t > 0.0f && s_t < TINY_ST; }
+__device__ __forceinline__ float up64(float x) { return fminf(fmaxf(x * TINY_MULT, -3.4028234663852886e38f), 3.4028234663852886e38f); }
+
 // Exact RN-even of the real quotient a / (k * s_t) onto the format grid, given
 // the codes c_lo, c_hi of the bracket ends.  When they differ, the two are
 // adjacent grid points and the one whose side of their midpoint `a` lies on
@@ -431,7 +449,7 @@ __device__ __forceinline__ void quot_bracket(float bs, float s_t, float &inv_lo,
   }
 }
 
-template <int F>
+template <int F, bool PLACE = true>
 __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs, float s_t, float inv_lo, float inv_hi);
 
 template <int F> __device__ __forceinline__ uint64_t encode_row8(const float (&v)[8], float bs, float s_t) {
@@ -513,7 +531,9 @@ __device__ __forceinline__ uint64_t cvt_row_e2m3(const float (&q)[8]) {
   return r;
 }
 
-template <int F>
+// PLACE = false: E2M3 codes are returned in byte containers (element j in
+// byte j) instead of the packed 6-bit stream; other formats are unaffected.
+template <int F, bool PLACE>
 __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs, float s_t, float inv_lo, float inv_hi) {
   float ql[8], qh[8];
 #pragma unroll
@@ -530,13 +550,22 @@ __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs,
   uint32_t lo[4], hi[4];
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) lo[jj] = (uint32_t)((row_lo >> (SH * jj)) & M);
-  if (row_lo == row_hi) return F == 6 ? place_row<F>(lo) : row_lo;   // common case: no element near a midpoint
+  if (row_lo == row_hi) return F == 6 && PLACE ? place_row<F>(lo) : row_lo;   // common case: no element near a midpoint
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) hi[jj] = (uint32_t)((row_hi >> (SH * jj)) & M);
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj)
     if (lo[jj] != hi[jj]) lo[jj] = fix_pair<F>(lo[jj], hi[jj], v[2 * jj], v[2 * jj + 1], bs, s_t);
+  if (F == 6 && !PLACE)
+    return (uint64_t)lo[0] | ((uint64_t)lo[1] << 16) | ((uint64_t)lo[2] << 32) | ((uint64_t)lo[3] << 48);
   return place_row<F>(lo);
+}
+
+// E2M3 codes in byte containers (element j in byte j) -> the packed 6-bit row
+__device__ __forceinline__ uint64_t place_row_e2m3_bytes(uint64_t b) {
+  const uint32_t pr[4] = {(uint32_t)(b & 0xFFFFu), (uint32_t)((b >> 16) & 0xFFFFu), (uint32_t)((b >> 32) & 0xFFFFu),
+                          (uint32_t)(b >> 48)};
+  return place_row<6>(pr);
 }
 
 // store one packed row (8 codes) at byte offset 4r / 6r / 8r of its block
@@ -551,6 +580,75 @@ template <int F> __device__ __forceinline__ void store_row8(uint8_t *blk, int r,
   } else {
     reinterpret_cast<uint64_t *>(blk)[r] = bits;
   }
+}
+
+}  // namespace mq
+
+namespace mq {
+
+// ------------------------------------------------------ stochastic rounding
+// MicroQonv §III-A lets Round be stochastic (the paper's choice for
+// gradients).  Random words come from Philox4x32-10 (Salmon, Moraes, Dror,
+// Shaw, SC 2011) keyed by a 64-bit seed; element e of a packed tensor
+// (e = block * 64 + in-block index) takes word e % 4 of counter
+// (e / 4 low, e / 4 high, 0, 0).  The decision is taken in fp32, exactly at
+// every step: q = fl32(|x| / fl32(B_scale T_scale)) (IEEE division, so
+// subnormal and tiny scales need no rescaling here); q >= maxB_ef gives the
+// largest code; otherwise, with lo <= q < hi the grid values around q, the
+// code is hi when (top 24 bits of the word) < 2^24 (q - lo) / (hi - lo).
+// q - lo is exact (lo <= q <= 2 lo, or lo = 0) and hi - lo is a power of two.
+
+// Philox4x32-10 of counter c (in place) under key (k0, k1)
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c[0], hi0 = __umulhi(0xD2511F53u, c[0]);
+    const uint32_t lo1 = 0xCD9E8D57u * c[2], hi1 = __umulhi(0xCD9E8D57u, c[2]);
+    const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+}
+
+// stochastic magnitude code of ax = |x| >= 0 for d = fl32(B_scale T_scale)
+template <int F> __device__ __forceinline__ uint32_t sr_mag(float ax, float d, uint32_t word) {
+  const float q = __fdiv_rn(ax, d);
+  if (!(q > 0.0f)) return 0u;
+  constexpr uint32_t MAXC = F == 8 ? 0x7Eu : Fmt<F>::MAG;   // largest finite magnitude code
+  if (q >= Fmt<F>::EMAX) return MAXC;
+  const uint32_t c = cvt2<F>(q, 0.0f) & Fmt<F>::MAG;        // nearest grid value (q below the largest)
+  const uint32_t lo = code_value<F>(c) > q ? c - 1u : c;
+  const float g_lo = code_value<F>(lo), g_hi = code_value<F>(lo + 1u);
+  const float frac = __fmul_rn(__fsub_rn(q, g_lo), __frcp_rn(__fsub_rn(g_hi, g_lo)));   // exact
+  const float scaled = __fmul_rn(frac, 16777216.0f);
+  return __uint2float_rn(word >> 8) < scaled ? lo + 1u : lo;
+}
+
+// Codes of one block row v[0..7] (elements 8r .. 8r+7 of block blk), packed
+// like encode_row8's result; d = fl32(B_scale T_scale), 0 for a zero scale.
+template <int F>
+__device__ __forceinline__ uint64_t encode_row8_sr(const float (&v)[8], float d, uint64_t seed, int64_t blk, int r) {
+  uint64_t bits = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint64_t ctr = (uint64_t)blk * 16u + (uint64_t)(2 * r + h);   // element index / 4
+    uint32_t w[4] = {(uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u};
+    philox4x32_10(w, (uint32_t)seed, (uint32_t)(seed >> 32));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float x = v[4 * h + j];
+      const uint32_t mag = d > 0.0f ? sr_mag<F>(fabsf(x), d, w[j]) : 0u;
+      const uint32_t code = mag | (signbit(x) ? Fmt<F>::SBIT : 0u);
+      bits |= (uint64_t)code << ((F == 4 ? 4 : F == 6 ? 6 : 8) * (4 * h + j));
+    }
+  }
+  return bits;
 }
 
 }  // namespace mq

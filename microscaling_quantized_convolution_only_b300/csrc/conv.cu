@@ -35,7 +35,7 @@
 
 namespace mq {
 
-constexpr int KCH = 8;                    // k-groups (8 reduction elements each) per stage: K = 64
+constexpr int KCH = CONV_KCH;             // k-groups (8 reduction elements each) per stage: K = 64
 constexpr int PROD_WARPS = 8;
 constexpr int EPI_WARPS = 4;
 constexpr int MMA_WARP = PROD_WARPS + EPI_WARPS;
@@ -227,28 +227,35 @@ __device__ __forceinline__ int64_t b_blk(const ConvParams &p, const Tile &T, con
 // activations for the forward pass, the lower layer's output gradient for the
 // data gradient; nc channels, ncg = nc / 8 groups).  Lanes 8q..8q+7 of a warp
 // hold the eight batch rows of one block: the block amax is their shuffle-max.
-template <int F>
+// TINY: T_scale below 2^-62, encoded from y 2^64 and T_scale 2^64 (s_t is
+// then the scaled one; see up64).  RARE: compile the stochastic-rounding
+// branch (p.rq.sr; only the out-of-line copy below has it).
+template <int F, bool TINY, bool RARE = true>
 __device__ __forceinline__ void requant_chunk(const ConvParams &p, const float (&y)[16], int pos, int ng, int n_in,
-                                              int co0, bool row_ok, float s_t, int nc, int ncg, uint32_t &amax_acc) {
+                                              int co0, bool row_ok, float s_t, float s_true, int nc, int ncg,
+                                              uint32_t &amax_acc) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int co = co0 + 8 * h;
-    float v[8];
+    float v[8], v_true[8];
     uint32_t m = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      v[j] = y[8 * h + j];
-      m = max(m, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+      m = max(m, __float_as_uint(y[8 * h + j]) & 0x7FFFFFFFu);
+      v_true[j] = y[8 * h + j];
+      v[j] = TINY ? up64(y[8 * h + j]) : y[8 * h + j];
     }
     if (!row_ok) m = 0;
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     amax_acc = max(amax_acc, m);
     if (!row_ok || co >= nc) continue;
-    const uint32_t bsc = block_scale_code<F>(__uint_as_float(m), s_t);
+    const uint32_t bsc = block_scale_code<F>(TINY ? up64(__uint_as_float(m)) : __uint_as_float(m), s_t);
     const float bs = code_value<8>(bsc);
-    const uint64_t bits = encode_row8<F>(v, bs, s_t);
     const int64_t blk = ((int64_t)pos * p.NG + ng) * ncg + co / 8;
+    // stochastic codes (MicroQonv §III-A, see encode_row8_sr) from the unscaled T_scale s_true
+    const uint64_t bits = RARE && p.rq.sr ? encode_row8_sr<F>(v_true, __fmul_rn(bs, s_true), p.rq.sr_seed, blk, n_in)
+                                          : encode_row8<F>(v, bs, s_t);
     uint8_t *dst = p.rq.codes + blk * Fmt<F>::BLOCK_BYTES;
     if (F == 4) {
       reinterpret_cast<uint32_t *>(dst)[n_in] = (uint32_t)bits;
@@ -262,6 +269,16 @@ __device__ __forceinline__ void requant_chunk(const ConvParams &p, const float (
     }
     if (n_in == 0) p.rq.scales[blk] = (uint8_t)bsc;
   }
+}
+
+// The tiny-T_scale and stochastic requantizations, kept out of line (rare;
+// inlined they would raise the register pressure of every requantizing kernel).
+template <int F>
+__device__ __noinline__ void requant_chunk_rare(const ConvParams &p, const float (&y)[16], int pos, int ng, int n_in,
+                                                int co0, bool row_ok, float s_t, float s_true, int nc, int ncg,
+                                                bool tiny, uint32_t &amax_acc) {
+  if (tiny) requant_chunk<F, true>(p, y, pos, ng, n_in, co0, row_ok, s_t, s_true, nc, ncg, amax_acc);
+  else requant_chunk<F, false>(p, y, pos, ng, n_in, co0, row_ok, s_t, s_true, nc, ncg, amax_acc);
 }
 
 // --------------------------------------------------------------- kernel
@@ -422,7 +439,8 @@ __global__ void __launch_bounds__(CONV_THREADS, 1) conv_kernel(const ConvParams 
       }
       // every MMA issued above has completed once `done` flips
       umma_commit(&ctl->done);
-      wait_or_abort(&ctl->done, 0, p, ctl);
+      // every MMA issued so far completes before the TMEM is freed, whatever the abort flag says
+      mbar_wait(&ctl->done, 0, p.status);
     }
     __syncwarp();
   } else {
@@ -433,6 +451,8 @@ __global__ void __launch_bounds__(CONV_THREADS, 1) conv_kernel(const ConvParams 
     const float f = (*p.a.s_t) * (*p.b.s_t) * pre;
     float rq_st = 0.0f;
     if (FR) rq_st = __fdiv_rn(*p.rq.amax_in, Fmt<FR ? FR : 4>::DENOM);
+    const bool rq_tiny = FR && is_tiny_scale(rq_st);
+    const float rq_stq = rq_tiny ? rq_st * TINY_MULT : rq_st;   // the T_scale quotients are formed with
     uint32_t amax_acc = 0;
     int tc = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
@@ -500,7 +520,12 @@ __global__ void __launch_bounds__(CONV_THREADS, 1) conv_kernel(const ConvParams 
           }
           if (FR) {
             const int nc = OP == OP_FWD ? p.Cout : p.Cin;
-            requant_chunk<FR ? FR : 4>(p, y, pos, ng, n_in, col0 + c0, obase >= 0, rq_st, nc, nc / 8, amax_acc);
+            if (rq_tiny || p.rq.sr)
+              requant_chunk_rare<FR ? FR : 4>(p, y, pos, ng, n_in, col0 + c0, obase >= 0, rq_stq, rq_st, nc,
+                                              nc / 8, rq_tiny, amax_acc);
+            else
+              requant_chunk<FR ? FR : 4, false, false>(p, y, pos, ng, n_in, col0 + c0, obase >= 0, rq_stq, rq_st,
+                                                       nc, nc / 8, amax_acc);
           }
         }
       }

@@ -1,6 +1,7 @@
 // kernels.h -- host-side launch interface between the C ABI (api.cu) and the kernels.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mq {
@@ -16,9 +17,16 @@ struct QuantParams {
   const uint32_t *amax_src_bits;   // statistic T_scale is built from (fp32 bits)
   uint32_t *amax_meas_bits;        // nullable: receives max |x| (atomic max of fp32 bits)
   uint32_t *status;
+  int sr;                          // element codes: 0 round-to-nearest, 1 stochastic (Philox key sr_seed)
+  uint64_t sr_seed;
 };
 
 enum ConvOp : int { OP_FWD = 0, OP_DGRAD = 1, OP_WGRAD = 2 };
+
+// k-groups (8 reduction elements each) per pipeline stage of the generic
+// implicit-im2col kernel (conv.cu); its weight-gradient splits are whole
+// multiples of it
+constexpr int CONV_KCH = 8;
 
 struct Operand {
   const uint8_t *codes;
@@ -34,6 +42,8 @@ struct Requant {                   // fused requantizing epilogue of the forward
   const float *amax_in;
   uint32_t *amax_out_bits;         // nullable
   int fmt;
+  int sr;                          // element codes: 0 round-to-nearest, 1 stochastic (Philox key sr_seed)
+  uint64_t sr_seed;
 };
 
 struct ConvParams {
@@ -55,7 +65,14 @@ struct ConvParams {
   int wg_rows;                     // wgrad: Cout rounded to 128 (partial-sum row pitch = Cout)
   int ncols;                       // wgrad: Kh*Kw*Cin
   uint32_t *status;
+  int inject;                      // fault injection for the failure-detection tests (0: none)
 };
+
+// Fault injections (test support): INJECT_WITHHOLD_ACC_RELEASE makes one
+// epilogue warp of CTA 0 of the halo forward / data-gradient kernel skip its
+// release of the first accumulator slot, so the MMA issuer's bounded wait for
+// that slot expires (no copy or MMA is left waiting on it).
+constexpr int INJECT_WITHHOLD_ACC_RELEASE = 1;
 
 // Forward / data-gradient convolution (stride 1 or 2) with per-tile halo
 // reuse (conv_halo.cu).  Filled by halo_plan() from a ConvParams.
@@ -72,6 +89,8 @@ struct HaloConv {
   int PHP;                       // halo positions per phase: RH * WP, padded so that every phase's
                                  // packed box starts 128-byte aligned
   int HKh, HKw;                  // halo extent in taps (Kh, Kw except for QD)
+  int wide;                      // wide form: MMAs of M = 128 output channels x N = 256 positions x batch
+                                 // (stride 1; P G = 32, BN = 128, two 256-column accumulators)
   int QD;                        // stride-2 data gradient: a tile covers R rows x P positions of output
                                  // quads (2 x 2 dX pixels), one accumulator per (row, output phase)
   int NPHS, RT;                  // accumulator phases per row (4 with QD, else 1); accumulators per tile R NPHS
@@ -91,6 +110,7 @@ struct HaloConv {
   float *out;                    // fp32 HWCN, nullable with rq
   Requant rq;
   uint32_t *status;
+  int inject;                    // fault injection (INJECT_*; 0: none)
   // shared-memory carve-up (bytes from the 1 KB-aligned base)
   uint32_t off_dec, dec_stage, dec_b_off;
   uint32_t off_pk, pk_stage, pk_b_off, pk_bytes;
@@ -132,6 +152,21 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms);
 bool halo_wgrad_plan(const ConvParams &cp, HaloWgrad &h, int max_splits);
 cudaError_t halo_wgrad_launch(const ConvParams &cp, HaloWgrad &h, int num_sms, cudaStream_t s);
 cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStream_t s);
+// launches of the forward / data-gradient halo kernel for operand formats fa
+// (input), fb (weights) and requantized-output format fr (0: none), split
+// over translation units by fr (conv_halo_{fwd,dgrad}_{a,b}.cu)
+#define MQ_HALO_DISPATCH(name)                                                                            \
+  cudaError_t name(int fa, int fb, int fr, const CUtensorMap &a, const CUtensorMap &b, const HaloConv &h, \
+                   int grid, cudaStream_t st);
+MQ_HALO_DISPATCH(halo_dispatch_fwd_04)
+MQ_HALO_DISPATCH(halo_dispatch_fwd_68)
+MQ_HALO_DISPATCH(halo_dispatch_dgrad_04)
+MQ_HALO_DISPATCH(halo_dispatch_dgrad_68)
+#undef MQ_HALO_DISPATCH
+// the wide form (conv_halo_wide.cu): op OP_FWD / OP_DGRAD, operand format f,
+// requantized-output format fr (0 or f)
+cudaError_t halo_dispatch_wide(int op, int f, int fr, const CUtensorMap &a, const CUtensorMap &b, const HaloConv &h,
+                               int grid, cudaStream_t st);
 
 // Tiled TMA descriptor of a row-major tensor (dims[0] innermost, elements of
 // esize bytes) with box `box`, zero fill outside; `map` is a 64-byte aligned

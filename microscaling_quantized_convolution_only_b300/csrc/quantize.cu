@@ -167,7 +167,7 @@ __device__ __forceinline__ void encode_block(const float (&x)[64], float bs, flo
 
 // -------------------------------------------------------------- quantize
 // Thread order: NCHW/OIHW -- spatial position fastest; HWCN -- n-group fastest.
-template <int FMT, typename T, int LAYOUT>
+template <int FMT, typename T, int LAYOUT, bool SR>
 __global__ void __launch_bounds__(256) quantize_kernel(const T *__restrict__ src, QuantParams p) {
   const int64_t GA = p.d0 / 8, GB = p.d1 / 8, HW = p.d2 * p.d3;
   const int64_t nblk = GA * GB * HW;
@@ -226,15 +226,36 @@ __global__ void __launch_bounds__(256) quantize_kernel(const T *__restrict__ src
     for (int i = 0; i < 64; ++i) mb = max(mb, __float_as_uint(x[i]) & 0x7FFFFFFFu);
     my_amax = mb;
     if (mb >= 0x7F800000u) atomicOr(p.status, ST_NONFINITE);
-    const float amax_b = __uint_as_float(mb);
-
-    const uint32_t bs_code = block_scale_code<FMT>(amax_b, s_t);
-    const float bs = code_value<8>(bs_code);
-    Packer<FMT> pk;
-    encode_block<FMT>(x, bs, s_t, pk);
+    float amax_b = __uint_as_float(mb);
     const int64_t b = (hw * GA + ga) * GB + gb;
-    pk.store(p.codes + b * Fmt<FMT>::BLOCK_BYTES);
-    p.scales[b] = (uint8_t)bs_code;
+    if (SR) {   // stochastic element codes (the block scale is round-to-nearest)
+      const uint32_t bs_code = is_tiny_scale(s_t) ? block_scale_code<FMT>(up64(amax_b), s_t * TINY_MULT)
+                                                  : block_scale_code<FMT>(amax_b, s_t);
+      const float d = __fmul_rn(code_value<8>(bs_code), s_t);
+      uint8_t *blkp = p.codes + b * Fmt<FMT>::BLOCK_BYTES;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        float v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = x[8 * r + c];
+        store_row8<FMT>(blkp, r, encode_row8_sr<FMT>(v, d, p.sr_seed, b, r));
+      }
+      p.scales[b] = (uint8_t)bs_code;
+    } else {
+      float st = s_t;
+      if (is_tiny_scale(s_t)) {   // T_scale below 2^-62: encode from x 2^64, T_scale 2^64 (see up64)
+        st = s_t * TINY_MULT;
+        amax_b = up64(amax_b);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[i] = up64(x[i]);
+      }
+      const uint32_t bs_code = block_scale_code<FMT>(amax_b, st);
+      const float bs = code_value<8>(bs_code);
+      Packer<FMT> pk;
+      encode_block<FMT>(x, bs, st, pk);
+      pk.store(p.codes + b * Fmt<FMT>::BLOCK_BYTES);
+      p.scales[b] = (uint8_t)bs_code;
+    }
   }
 
   if (p.amax_meas_bits) {
@@ -255,6 +276,66 @@ template <typename T> __device__ __forceinline__ uint32_t to_bits32(uint32_t raw
   return sizeof(T) == 2 ? raw << 16 : raw;
 }
 
+// Block scale and codes of one block whose 64 inputs are held as raw bits
+// (bf16 inputs two to a register, element 2k in the low half), row a of the
+// block (8 consecutive b) at raw[8a / PK ...]; `mb` is the block amax (fp32
+// bits).  The packed rows go to `ob`; returns the E4M3 scale code.  TINY:
+// T_scale below 2^-62, encoded from x 2^64 and T_scale 2^64 (see up64).
+template <int FMT, typename T, bool TINY>
+__device__ __forceinline__ uint32_t encode_raw_block(const uint32_t (&raw)[sizeof(T) == 2 ? 32 : 64], uint32_t mb,
+                                                     float s_t, uint8_t *ob) {
+  const float st = TINY ? s_t * TINY_MULT : s_t;
+  const float amax_b = TINY ? up64(__uint_as_float(mb)) : __uint_as_float(mb);
+  const uint32_t bs_code = block_scale_code<FMT>(amax_b, st);
+  const float bs = code_value<8>(bs_code);
+  float inv_lo, inv_hi;
+  quot_bracket(bs, st, inv_lo, inv_hi);
+#pragma unroll
+  for (int a = 0; a < 8; ++a) {
+    float x[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (sizeof(T) == 2) {
+        const uint32_t w = raw[((a * 8 + b) / 2) & 31];
+        x[b] = __uint_as_float((b & 1) ? (w & 0xFFFF0000u) : (w << 16));
+      } else {
+        x[b] = __uint_as_float(raw[(a * 8 + b) & 63]);
+      }
+      if (TINY) x[b] = up64(x[b]);
+    }
+    store_row8<FMT>(ob, a, encode_row8_b<FMT>(x, bs, st, inv_lo, inv_hi));
+  }
+  return bs_code;
+}
+
+// The same block with stochastically rounded element codes (block `blk` of
+// the packed tensor, Philox key `seed`; see encode_row8_sr).  The block scale
+// is the round-to-nearest one.
+template <int FMT, typename T>
+__device__ __forceinline__ uint32_t encode_raw_block_sr(const uint32_t (&raw)[sizeof(T) == 2 ? 32 : 64], uint32_t mb,
+                                                        float s_t, uint8_t *ob, int64_t blk, uint64_t seed) {
+  const bool tiny = is_tiny_scale(s_t);
+  const float amax_b = __uint_as_float(mb);
+  const uint32_t bs_code = tiny ? block_scale_code<FMT>(up64(amax_b), s_t * TINY_MULT)
+                                : block_scale_code<FMT>(amax_b, s_t);
+  const float d = __fmul_rn(code_value<8>(bs_code), s_t);
+#pragma unroll
+  for (int a = 0; a < 8; ++a) {
+    float x[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (sizeof(T) == 2) {
+        const uint32_t w = raw[((a * 8 + b) / 2) & 31];
+        x[b] = __uint_as_float((b & 1) ? (w & 0xFFFF0000u) : (w << 16));
+      } else {
+        x[b] = __uint_as_float(raw[(a * 8 + b) & 63]);
+      }
+    }
+    store_row8<FMT>(ob, a, encode_row8_sr<FMT>(x, d, seed, blk, a));
+  }
+  return bs_code;
+}
+
 // ------------------------------------------------------ NCHW / OIHW path
 // Dense NCHW (or OIHW: a = Cout, b = Cin, hw = tap) input is contiguous along
 // hw; the packed output is contiguous along the b-groups of one (hw, a-group).
@@ -267,11 +348,12 @@ constexpr int QN_HW = 32, QN_GB = 8;
 
 // CTA shape: GBT b-groups (one warp each) x (8 / GBT) chunks of 32 positions;
 // GBT = min(8, B / 8) so that narrow tensors keep all warps busy.
-template <int FMT, typename T>
-__global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2) quantize_nchw_kernel(const T *__restrict__ src, QuantParams p) {
+// The work of one quantize_nchw_kernel CTA after T_scale is known (TINY:
+// T_scale below 2^-62).
+template <int FMT, typename T, bool SR, bool TINY>
+__device__ __forceinline__ void nchw_body(const T *__restrict__ src, const QuantParams &p, uint8_t *obuf,
+                                          uint8_t *sbuf, float s_t) {
   constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
-  __shared__ __align__(16) uint8_t obuf[QN_HW * QN_GB * BB + QN_HW * QN_GB * 16];   // HWT * opitch at most
-  __shared__ uint8_t sbuf[QN_HW * QN_GB];
   const int GA = (int)(p.d0 / 8), GB = (int)(p.d1 / 8);
   const int GBT = GB < QN_GB ? GB : QN_GB, HWT = QN_HW * (QN_GB / GBT);
   const int64_t HW = p.d2 * p.d3;
@@ -287,13 +369,6 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2) quantize_nchw_ker
   const int warp = threadIdx.x >> 5;
   const int wl = warp % GBT, hl = (warp / GBT) * 32 + (threadIdx.x & 31);
   const int opitch = GBT * BB + 16;    // staged bytes per position
-  const float amax_src = __uint_as_float(*p.amax_src_bits);
-  const float s_t = __fdiv_rn(amax_src, Fmt<FMT>::DENOM);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    *p.s_t_out = s_t;
-    if (!(amax_src <= 3.4028234663852886e38f)) atomicOr(p.status, ST_NONFINITE);
-  }
-
   uint32_t my_amax = 0;
   if (wl < ngb && hl < nhw) {
     // the block's 64 inputs, row a = 8 consecutive b; rows and columns are
@@ -324,24 +399,13 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2) quantize_nchw_ker
     }
     my_amax = mb;
     if (mb >= 0x7F800000u) atomicOr(p.status, ST_NONFINITE);
-    const uint32_t bs_code = block_scale_code<FMT>(__uint_as_float(mb), s_t);
-    const float bs = code_value<8>(bs_code);
-    float inv_lo, inv_hi;
-    quot_bracket(bs, s_t, inv_lo, inv_hi);
     uint8_t *ob = obuf + hl * opitch + wl * BB;
-#pragma unroll
-    for (int a = 0; a < 8; ++a) {
-      float x[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        if (PK == 2) {
-          const uint32_t w = raw[(a * 8 + b) / 2];
-          x[b] = __uint_as_float((b & 1) ? (w & 0xFFFF0000u) : (w << 16));
-        } else {
-          x[b] = __uint_as_float(raw[a * 8 + b]);
-        }
-      }
-      store_row8<FMT>(ob, a, encode_row8_b<FMT>(x, bs, s_t, inv_lo, inv_hi));
+    uint32_t bs_code;
+    if (SR) {
+      const int64_t blk = ((hw0 + hl) * GA + ga) * (int64_t)GB + gb0 + wl;
+      bs_code = encode_raw_block_sr<FMT, T>(raw, mb, s_t, ob, blk, p.sr_seed);
+    } else {
+      bs_code = encode_raw_block<FMT, T, TINY>(raw, mb, s_t, ob);
     }
     sbuf[hl * GBT + wl] = (uint8_t)bs_code;
   }
@@ -366,6 +430,29 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2) quantize_nchw_ker
   }
 }
 
+template <int FMT, typename T>
+__device__ __noinline__ void nchw_body_tiny(const T *__restrict__ src, const QuantParams &p, uint8_t *obuf,
+                                            uint8_t *sbuf, float s_t) {
+  nchw_body<FMT, T, false, true>(src, p, obuf, sbuf, s_t);
+}
+
+template <int FMT, typename T, bool SR>
+__global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2) quantize_nchw_kernel(const T *__restrict__ src, QuantParams p) {
+  constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
+  __shared__ __align__(16) uint8_t obuf[QN_HW * QN_GB * BB + QN_HW * QN_GB * 16];   // HWT * opitch at most
+  __shared__ uint8_t sbuf[QN_HW * QN_GB];
+  const float amax_src = __uint_as_float(*p.amax_src_bits);
+  const float s_t = __fdiv_rn(amax_src, Fmt<FMT>::DENOM);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *p.s_t_out = s_t;
+    if (!(amax_src <= 3.4028234663852886e38f)) atomicOr(p.status, ST_NONFINITE);
+  }
+  // stochastic codes decide from the unscaled T_scale; the tiny-T_scale
+  // round-to-nearest encode runs in an out-of-line copy
+  if (!SR && is_tiny_scale(s_t)) nchw_body_tiny<FMT, T>(src, p, obuf, sbuf, s_t);
+  else nchw_body<FMT, T, SR, false>(src, p, obuf, sbuf, s_t);
+}
+
 
 // ------------------------------------------------- NCHW / OIHW, TMA path
 // Same tiling and arithmetic as quantize_nchw_kernel, but the input tile
@@ -385,7 +472,8 @@ struct QtCtl {
 // bounded wait: gives up after 2 s, or at once when another warp has given
 // up, so that every warp leaves its loop and the CTA still meets at its
 // barriers
-__device__ __forceinline__ bool qt_wait(uint64_t *bar, uint32_t parity, QtCtl *ctl, uint32_t *status) {
+template <class Ctl>
+__device__ __forceinline__ bool qt_wait(uint64_t *bar, uint32_t parity, Ctl *ctl, uint32_t *status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
@@ -399,59 +487,18 @@ __device__ __forceinline__ bool qt_wait(uint64_t *bar, uint32_t parity, QtCtl *c
   }
 }
 
-template <int FMT, typename T, int GBT>
-__global__ void __launch_bounds__(QT_THREADS, 2)
-    quantize_tma_kernel(const __grid_constant__ CUtensorMap tm, QuantParams p, int ntiles, int hw_tiles, int gb_tiles) {
+// The quantizing warps' loop over the CTA's tiles (see quantize_tma_kernel);
+// returns the largest |x| seen (fp32 bits).  TINY: T_scale below 2^-62.
+template <int FMT, typename T, int GBT, bool TINY>
+__device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl, uint8_t *ring, uint8_t *obuf,
+                                                uint8_t *sbuf, int ntiles, int hw_tiles, int gb_tiles, float s_t) {
   constexpr int HWT = QN_HW * (QN_GB / GBT);
   constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
   constexpr int STAGE = HWT * GBT * 64 * (int)sizeof(T);
   constexpr int OPITCH = GBT * BB + 16;
-  extern __shared__ __align__(1024) uint8_t qraw[];
-  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(qraw) + 1023) & ~uintptr_t(1023));
-  uint8_t *obuf = ring + QT_STAGES * STAGE;
-  uint8_t *sbuf = obuf + HWT * OPITCH;
-  QtCtl *ctl = reinterpret_cast<QtCtl *>(sbuf + ((HWT * GBT + 15) / 16) * 16);
   const int GA = (int)(p.d0 / 8), GB = (int)(p.d1 / 8);
   const int64_t HW = p.d2 * p.d3;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const float amax_src = __uint_as_float(*p.amax_src_bits);
-  const float s_t = __fdiv_rn(amax_src, Fmt<FMT>::DENOM);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < QT_STAGES; ++s) {
-      mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], QT_CWARPS);
-    }
-    ctl->abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (blockIdx.x == 0) {
-      *p.s_t_out = s_t;
-      if (!(amax_src <= 3.4028234663852886e38f)) atomicOr(p.status, ST_NONFINITE);
-    }
-  }
-  __syncthreads();
-
-  if (warp == QT_CWARPS) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int it = 0;
-      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-        const int s = it % QT_STAGES;
-        if (!qt_wait(&ctl->empty[s], ((it / QT_STAGES) & 1) ^ 1, ctl, p.status)) break;
-        const int hwt = t % hw_tiles, rest = t / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
-        mbar_expect_tx(&ctl->full[s], STAGE);
-        tma_load_3d(ring + s * STAGE, &tm, &ctl->full[s], hwt * HWT, gbt * GBT * 8, ga * 8);
-      }
-      for (int i = 0; i < QT_STAGES && i < it; ++i) {   // copies in flight land before exit
-        const int q = it - 1 - i;
-        mbar_wait(&ctl->full[q % QT_STAGES], (q / QT_STAGES) & 1, p.status);   // ignores the abort flag
-      }
-    }
-    __syncwarp();
-    return;
-  }
-
-  // --------------------------------------------------------------- compute
   const int wl = warp % GBT, hl = (warp / GBT) * 32 + lane;
   uint32_t my_amax = 0;
   int it = 0;
@@ -499,25 +546,8 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
       }
       my_amax = max(my_amax, mb);
       if (mb >= 0x7F800000u) atomicOr(p.status, ST_NONFINITE);
-      const uint32_t bs_code = block_scale_code<FMT>(__uint_as_float(mb), s_t);
-      const float bs = code_value<8>(bs_code);
-      float inv_lo, inv_hi;
-      quot_bracket(bs, s_t, inv_lo, inv_hi);
       uint8_t *ob = obuf + hl * OPITCH + wl * BB;
-#pragma unroll
-      for (int a = 0; a < 8; ++a) {
-        float x[8];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          if (sizeof(T) == 2) {
-            const uint32_t w = raw[((a * 8 + b) / 2) & 31];
-            x[b] = __uint_as_float((b & 1) ? (w & 0xFFFF0000u) : (w << 16));
-          } else {
-            x[b] = __uint_as_float(raw[(a * 8 + b) & 63]);
-          }
-        }
-        store_row8<FMT>(ob, a, encode_row8_b<FMT>(x, bs, s_t, inv_lo, inv_hi));
-      }
+      const uint32_t bs_code = encode_raw_block<FMT, T, TINY>(raw, mb, s_t, ob);
       sbuf[hl * GBT + wl] = (uint8_t)bs_code;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(QT_CWARPS * 32) : "memory");
@@ -535,6 +565,71 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
     }
     asm volatile("bar.sync 1, %0;" ::"n"(QT_CWARPS * 32) : "memory");
   }
+  return my_amax;
+}
+
+// the tiny-T_scale loop, kept out of line (rare; inlined beside the common
+// loop it would raise the register pressure of every launch)
+template <int FMT, typename T, int GBT>
+__device__ __noinline__ uint32_t tma_compute_tiny(const QuantParams &p, QtCtl *ctl, uint8_t *ring, uint8_t *obuf,
+                                                  uint8_t *sbuf, int ntiles, int hw_tiles, int gb_tiles, float s_t) {
+  return tma_compute<FMT, T, GBT, true>(p, ctl, ring, obuf, sbuf, ntiles, hw_tiles, gb_tiles, s_t);
+}
+
+template <int FMT, typename T, int GBT>
+__global__ void __launch_bounds__(QT_THREADS, 2)
+    quantize_tma_kernel(const __grid_constant__ CUtensorMap tm, QuantParams p, int ntiles, int hw_tiles, int gb_tiles) {
+  constexpr int HWT = QN_HW * (QN_GB / GBT);
+  constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
+  constexpr int STAGE = HWT * GBT * 64 * (int)sizeof(T);
+  constexpr int OPITCH = GBT * BB + 16;
+  extern __shared__ __align__(1024) uint8_t qraw[];
+  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(qraw) + 1023) & ~uintptr_t(1023));
+  uint8_t *obuf = ring + QT_STAGES * STAGE;
+  uint8_t *sbuf = obuf + HWT * OPITCH;
+  QtCtl *ctl = reinterpret_cast<QtCtl *>(sbuf + ((HWT * GBT + 15) / 16) * 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const float amax_src = __uint_as_float(*p.amax_src_bits);
+  const float s_t = __fdiv_rn(amax_src, Fmt<FMT>::DENOM);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < QT_STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], QT_CWARPS);
+    }
+    ctl->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (blockIdx.x == 0) {
+      *p.s_t_out = s_t;
+      if (!(amax_src <= 3.4028234663852886e38f)) atomicOr(p.status, ST_NONFINITE);
+    }
+  }
+  __syncthreads();
+
+  if (warp == QT_CWARPS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int s = it % QT_STAGES;
+        if (!qt_wait(&ctl->empty[s], ((it / QT_STAGES) & 1) ^ 1, ctl, p.status)) break;
+        const int hwt = t % hw_tiles, rest = t / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
+        mbar_expect_tx(&ctl->full[s], STAGE);
+        tma_load_3d(ring + s * STAGE, &tm, &ctl->full[s], hwt * HWT, gbt * GBT * 8, ga * 8);
+      }
+      for (int i = 0; i < QT_STAGES && i < it; ++i) {   // copies in flight land before exit
+        const int q = it - 1 - i;
+        mbar_wait(&ctl->full[q % QT_STAGES], (q / QT_STAGES) & 1, p.status);   // ignores the abort flag
+      }
+    }
+    __syncwarp();
+    return;
+  }
+
+  // --------------------------------------------------------------- compute
+  const uint32_t my_amax =
+      is_tiny_scale(s_t) ? tma_compute_tiny<FMT, T, GBT>(p, ctl, ring, obuf, sbuf, ntiles, hw_tiles, gb_tiles, s_t)
+                         : tma_compute<FMT, T, GBT, false>(p, ctl, ring, obuf, sbuf, ntiles, hw_tiles, gb_tiles, s_t);
   if (p.amax_meas_bits) {
     uint32_t m = my_amax;
 #pragma unroll
@@ -590,16 +685,18 @@ static cudaError_t launch_q(const void *src, int layout, const QuantParams &p, i
   const T *x = static_cast<const T *>(src);
   if (layout == 1) {
     const unsigned grid = (unsigned)((nblk + 255) / 256);
-    quantize_kernel<FMT, T, 1><<<grid, 256, 0, s>>>(x, p);
+    if (p.sr) quantize_kernel<FMT, T, 1, true><<<grid, 256, 0, s>>>(x, p);
+    else quantize_kernel<FMT, T, 1, false><<<grid, 256, 0, s>>>(x, p);
     return cudaGetLastError();
   }
   cudaError_t err = cudaSuccess;
-  if (try_tma_q<FMT, T>(x, p, num_sms, s, err)) return err;
+  if (!p.sr && try_tma_q<FMT, T>(x, p, num_sms, s, err)) return err;   // stochastic codes: direct-load kernel
   // NCHW / OIHW: GBT b-groups x 256 / GBT positions per CTA, contiguous output runs
   const int64_t HW = p.d2 * p.d3, GB = p.d1 / 8;
   const int64_t GBT = GB < QN_GB ? GB : QN_GB, HWT = QN_HW * (QN_GB / GBT);
   const int64_t grid = (p.d0 / 8) * ((GB + GBT - 1) / GBT) * ((HW + HWT - 1) / HWT);
-  quantize_nchw_kernel<FMT, T><<<(unsigned)grid, 256, 0, s>>>(x, p);
+  if (p.sr) quantize_nchw_kernel<FMT, T, true><<<(unsigned)grid, 256, 0, s>>>(x, p);
+  else quantize_nchw_kernel<FMT, T, false><<<(unsigned)grid, 256, 0, s>>>(x, p);
   return cudaGetLastError();
 }
 

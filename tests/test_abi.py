@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert mq.abi_version() == 1
+    assert mq.abi_version() == 2
     assert mq.status_string(0) == "ok"
     assert "multiples of 8" in mq.status_string(2)
 
@@ -87,3 +87,10 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mq, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(mq.MQError):
         mq.lib()
+
+
+def test_fault_inject_validates_its_arguments(lib):
+    """mqconv_test_fault_inject only sets a host-side launch setting."""
+    assert lib.mqconv_test_fault_inject(7) == 1               # unknown injection
+    assert lib.mqconv_test_fault_inject(1) == 0
+    assert lib.mqconv_test_fault_inject(0) == 0               # back to normal operation

@@ -20,7 +20,7 @@ def _copy_sources(dst):
     shutil.copytree(src_csrc, os.path.join(dst, "microscaling_quantized_convolution_only_b300", "csrc"))
     os.makedirs(os.path.join(dst, "include"))
     shutil.copy(os.path.join(ROOT, "include", "mqconv.h"), os.path.join(dst, "include", "mqconv.h"))
-    return os.path.join(dst, "microscaling_quantized_convolution_only_b300", "csrc", "conv_halo.cu")
+    return os.path.join(dst, "microscaling_quantized_convolution_only_b300", "csrc", "conv_halo.cuh")
 
 
 def test_sources_key_ignores_comments_not_code(tmp_path):

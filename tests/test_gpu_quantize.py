@@ -116,3 +116,54 @@ def test_full_size_activation(cuda_device, wl_layer):
     ref = oracle.quantize(x, wl.fmt, "act", "nchw")
     assert amax == ref["amax"]
     assert_packed_equal(p, ref, f"{wl.name} X")
+
+
+def _tiny(shape, seed, amax):
+    """A tensor scaled so that its amax is `amax` (fp32, subnormal values
+    included when amax is small enough), with exact zeros, negative zeros and
+    a few of the smallest subnormals mixed in."""
+    x = np.random.default_rng(seed).standard_normal(shape)
+    x = (x / np.abs(x).max() * amax).astype(np.float32)
+    x.ravel()[::11] = 0.0
+    x.ravel()[3::13] = -0.0
+    x.ravel()[5::17] = np.float32(1.4e-45)            # 2^-149
+    x.ravel()[7::19] = -np.float32(2.8e-45)
+    x.ravel()[0] = np.float32(amax)
+    return x
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("amax", [1e-20, 1e-36, 1e-40], ids=["Tscale-below-2^-62", "Tscale-subnormal",
+                                                              "Tscale-deep-subnormal"])
+@pytest.mark.parametrize("layout", ["nchw", "hwcn"])
+def test_tiny_tensor_scale(cuda_device, fmt, amax, layout):
+    """T_scale below 2^-62 and subnormal T_scale (amax ~1e-36, 1e-40), with
+    subnormal inputs: codes and scales still bit-exact against the oracle."""
+    shape = (16, 24, 6, 8)
+    x = _tiny(shape, 11, amax)
+    if layout == "hwcn":
+        xs = np.ascontiguousarray(x.transpose(2, 3, 1, 0))
+        p, a = gpu_quantize(to_dev(xs, "f32", cuda_device), fmt, "grad", layout, shape)
+        ref = oracle.quantize(xs, fmt, "grad", layout)
+    else:
+        p, a = gpu_quantize(to_dev(x, "f32", cuda_device), fmt, "act", layout, shape)
+        ref = oracle.quantize(x, fmt, "act", layout)
+    assert a == ref["amax"]
+    assert_packed_equal(p, ref, f"tiny T_scale amax={amax} {fmt} {layout}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("data_amax,stat", [(1.0, 1e-36), (1e20, 1e-30), (1e-30, 1e-38), (3e38, 1e-20)],
+                         ids=["unit-data-subnormal-stat", "huge-data-tiny-stat", "tiny-data-subnormal-stat",
+                              "max-data-tiny-stat"])
+def test_supplied_statistic_far_below_data(cuda_device, fmt, data_amax, stat):
+    """A supplied statistic far below the data: T_scale tiny or subnormal,
+    most quotients saturate (some beyond 2^64 x T_scale); bit-exact against
+    the oracle for both the bf16-pair and the fp32 code paths."""
+    for dtype in ("f32", "bf16"):
+        x = _tiny((16, 16, 4, 8), 21, data_amax)
+        if dtype == "bf16":
+            x = S.to_bf16_rne(x)
+        p, _ = gpu_quantize(to_dev(x, dtype, cuda_device), fmt, "act", "nchw", x.shape, amax_in=stat)
+        ref = oracle.quantize(x, fmt, "act", "nchw", amax_in=stat)
+        assert_packed_equal(p, ref, f"data {data_amax} statistic {stat} {fmt} {dtype}")

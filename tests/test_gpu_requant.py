@@ -16,7 +16,7 @@ import torch
 import microscaling_quantized_convolution_only_b300 as mq
 import oracle
 import synthetic as S
-from mqtest import LayerRun, assert_packed_equal
+from mqtest import LayerRun, assert_packed_equal, check_close, hwcn_to_nchw
 from synthetic import Layer
 
 pytestmark = pytest.mark.gpu
@@ -120,3 +120,69 @@ def test_requant_rejects_wrong_role(cuda_device):
     ain = torch.ones(1, device=cuda_device)
     with pytest.raises(mq.MQError, match="invalid argument"):
         mq.dgrad(L, run.wq, run.gq, None, rq_out=out, rq_amax_in=ain)
+
+
+@pytest.mark.parametrize("fmt", ["e2m1", "e2m3", "e4m3"])
+@pytest.mark.parametrize("L", [LAYERS[0], LAYERS[2]], ids=["halo", "generic"])
+@pytest.mark.parametrize("stat_factor", [1.0, 1e-16], ids=["Tscale-below-2^-62", "Tscale-subnormal"])
+def test_requant_tiny_tensor_scale(cuda_device, fmt, L, stat_factor):
+    """Activations scaled by 1e-20: Y ~ 1e-20, so its T_scale (from a
+    statistic of max|Y|, or that times 1e-16 -- subnormal) is below 2^-62 and
+    the fused epilogues encode through their tiny-scale path.  Bit-exact
+    against the oracle quantizer on the unfused fp32 output."""
+    X, W, dY = _inputs(L, 5 + L.N)
+    run = LayerRun(L, fmt, "f32", (X * np.float32(1e-20)).astype(np.float32), W,
+                   (dY * np.float32(1e-20)).astype(np.float32), cuda_device, check_quant=True)
+    for op, role, shape in (("fwd", "act", L.y_shape()), ("dgrad", "grad", L.x_shape())):
+        ref = run.fwd() if op == "fwd" else run.dgrad()
+        ref_np = ref.cpu().numpy()
+        stat = float(np.float32(np.max(np.abs(ref_np)) * stat_factor))
+        assert 0.0 < stat < 1e-18
+        out = mq.Packed(fmt, role, shape, device=cuda_device)
+        ain = torch.tensor([stat], device=cuda_device)
+        aout = torch.zeros(1, device=cuda_device)
+        if op == "fwd":
+            mq.fwd(L, run.xq, run.wq, None, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
+        else:
+            mq.dgrad(L, run.wq, run.gq, None, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
+        mq.check_device_status()
+        _check(out, ref_np, fmt, role, stat, aout, f"{op} requant tiny T_scale x{stat_factor} {fmt} {L.name()}")
+
+
+WIDE_LAYERS = [
+    Layer(16, 128, 9, 7, 128, 3, 1, 1),    # wide form both ways, ragged positions (7 of 8 / 32-row tiles)
+    Layer(8, 128, 6, 10, 256, 3, 1, 1),    # two output-channel tiles forward, one batch group
+    Layer(32, 256, 5, 5, 128, 1, 1, 0),    # 1x1, four batch groups, more input channels than a tile
+]
+
+
+@pytest.mark.parametrize("fmt", ["e2m1", "e2m3", "e4m3"])
+@pytest.mark.parametrize("L", WIDE_LAYERS, ids=lambda L: L.name())
+@pytest.mark.parametrize("scale", [1.0, 1e-20], ids=["unit", "tiny-Tscale"])
+def test_wide_requant(cuda_device, fmt, L, scale):
+    """Layers with at least 128 output channels at stride 1 run through the
+    wide form (MMAs of 128 channels x 256 positions x batch, channels on the
+    accumulator lanes): fp32 outputs against the oracle, and the fused
+    requantizations (codes transposed across lanes before they are stored)
+    bit-exact against the oracle quantizer on the unfused fp32 outputs."""
+    X, W, dY = _inputs(L, 11 + L.N)
+    run = LayerRun(L, fmt, "f32", (X * np.float32(scale)).astype(np.float32), W,
+                   (dY * np.float32(scale)).astype(np.float32), cuda_device, check_quant=True)
+    Xd, Wd, Gd = run.oracle_operands()
+    for op, role, shape in (("fwd", "act", L.y_shape()), ("dgrad", "grad", L.x_shape())):
+        ref = run.fwd() if op == "fwd" else run.dgrad()
+        want, wanta = oracle.conv_fwd(Xd, Wd, L) if op == "fwd" else oracle.conv_dgrad(Wd, Gd, L)
+        check_close(hwcn_to_nchw(ref), want, wanta, f"{op} {fmt} {L.name()} x{scale}")
+        ref_np = ref.cpu().numpy()
+        stat = float(np.float32(np.max(np.abs(ref_np)) * 1.3))
+        out = mq.Packed(fmt, role, shape, device=cuda_device)
+        ain = torch.tensor([stat], device=cuda_device)
+        aout = torch.zeros(1, device=cuda_device)
+        y2 = torch.full_like(ref, float("nan"))
+        if op == "fwd":
+            mq.fwd(L, run.xq, run.wq, y2, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
+        else:
+            mq.dgrad(L, run.wq, run.gq, y2, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
+        mq.check_device_status()
+        assert torch.equal(y2, ref), f"{op}: fp32 output beside the fused epilogue differs from the unfused one"
+        _check(out, ref_np, fmt, role, stat, aout, f"wide {op} requant {fmt} {L.name()} x{scale}")
