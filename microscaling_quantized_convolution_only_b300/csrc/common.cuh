@@ -459,24 +459,26 @@ template <int F> __device__ __forceinline__ uint64_t encode_row8(const float (&v
 }
 
 // encode_row8 with the bracket multipliers of quot_bracket precomputed.  The
-// codes of both bracket ends are formed a pair at a time; when a pair agrees
-// (the common case) it is placed as is, otherwise each element of the pair is
-// settled by resolve_tie.
-template <int F>
-__device__ __forceinline__ uint32_t fix_pair(uint32_t lo, uint32_t hi, float v0, float v1, float bs, float s_t) {
-  constexpr uint32_t cmask = F == 4 ? 0xFu : 0xFFu;
-  constexpr int sh = F == 4 ? 4 : 8;
-  uint32_t pair = 0;
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const uint32_t cl = (lo >> (e * sh)) & cmask, ch = (hi >> (e * sh)) & cmask;
-    const float x = e ? v1 : v0;
-    const uint32_t c = cl == ch ? cl
-                                : resolve_tie<F>(fabsf(x), bs, s_t, cl & Fmt<F>::MAG, ch & Fmt<F>::MAG) |
-                                      (signbit(x) ? Fmt<F>::SBIT : 0u);
-    pair |= c << (e * sh);
-  }
-  return pair;
+// codes of both bracket ends are formed for the whole row at once; when they
+// agree (the common case) the row is placed as is, otherwise every element is
+// converted again from the quotient tie_quotient picks, without a branch.
+//
+// tie_quotient: a value whose RN-even conversion is the exact RN-even code of
+// the quotient x / (bs * s_t), given the bracket ends ql, qh around it
+// (signed like x; |ql| <= |qh|).  m = ql rounded to 5 significant bits is the
+// rounding midpoint inside the bracket when there is one: every midpoint of
+// the three grids has at most 5 significant bits, and the bracket is 2^-19
+// wide.  The fma rounds the exact |x| - (|m| * bs) * s_t once (|m| * bs is
+// exact: at most 9 significant bits), so its sign is the side of m on which
+// the exact quotient lies (the argument of resolve_tie): above m the code of
+// qh is right, below it the code of ql, and on it the exact quotient is m
+// itself, which the conversion rounds to even.  Without a midpoint in the
+// bracket both ends convert to the same code, and so does m when the sign is
+// zero (m is then the exact quotient).
+__device__ __forceinline__ float tie_quotient(float ql, float qh, float x, float bs, float s_t) {
+  const float m = __uint_as_float((__float_as_uint(ql) + 0x40000u) & 0xFFF80000u);
+  const float r = fmaf(-(fabsf(m) * bs), s_t, fabsf(x));
+  return r > 0.0f ? qh : (r < 0.0f ? ql : m);
 }
 
 // four code pairs (containers as cvt2 returns them) -> one packed row
@@ -547,17 +549,17 @@ __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs,
   const uint64_t row_hi = F == 4 ? (uint64_t)cvt_row_e2m1(qh) : F == 8 ? cvt_row_e4m3(qh) : cvt_row_e2m3(qh);
   constexpr int SH = F == 4 ? 8 : 16;
   constexpr uint64_t M = F == 4 ? 0xFFu : 0xFFFFu;
-  uint32_t lo[4], hi[4];
+  uint32_t lo[4];
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) lo[jj] = (uint32_t)((row_lo >> (SH * jj)) & M);
   if (row_lo == row_hi) return F == 6 && PLACE ? place_row<F>(lo) : row_lo;   // common case: no element near a midpoint
+  float q[8];
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) hi[jj] = (uint32_t)((row_hi >> (SH * jj)) & M);
+  for (int j = 0; j < 8; ++j) q[j] = tie_quotient(ql[j], qh[j], v[j], bs, s_t);
+  const uint64_t row = F == 4 ? (uint64_t)cvt_row_e2m1(q) : F == 8 ? cvt_row_e4m3(q) : cvt_row_e2m3(q);
+  if (F != 6 || !PLACE) return row;
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj)
-    if (lo[jj] != hi[jj]) lo[jj] = fix_pair<F>(lo[jj], hi[jj], v[2 * jj], v[2 * jj + 1], bs, s_t);
-  if (F == 6 && !PLACE)
-    return (uint64_t)lo[0] | ((uint64_t)lo[1] << 16) | ((uint64_t)lo[2] << 32) | ((uint64_t)lo[3] << 48);
+  for (int jj = 0; jj < 4; ++jj) lo[jj] = (uint32_t)((row >> (SH * jj)) & M);
   return place_row<F>(lo);
 }
 

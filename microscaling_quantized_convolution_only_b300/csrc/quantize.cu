@@ -66,104 +66,63 @@ __global__ void __launch_bounds__(256) amax_kernel(const T *__restrict__ src, in
 }
 
 // ------------------------------------------------------------- codes
-// Pack 64 codes of one block into its payload (layout in mqconv.h).
-template <int FMT> struct Packer;
-
-template <> struct Packer<4> {   // two codes per byte, element 2j in the low nibble
-  uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  __device__ __forceinline__ void put_pair(int j, uint32_t pair) {   // pair = c(2j) | c(2j+1) << 4
-    const int word = j >> 2, sh = (j & 3) * 8;
-    w[word] = (w[word] & ~(0xFFu << sh)) | (pair << sh);
-  }
-  __device__ __forceinline__ void store(uint8_t *dst) const {
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  }
+// Row sinks of the block encoders: packed rows written to a staging buffer
+// in shared memory, or collected in registers and written to the block's place
+// in global memory with 32- or 16-byte stores (block payload layout in
+// mqconv.h).
+template <int F> struct SmemRows {
+  uint8_t *ob;
+  __device__ __forceinline__ void put(int r, uint64_t bits) { store_row8<F>(ob, r, bits); }
 };
 
-template <> struct Packer<6> {   // little-endian stream of 6-bit codes
-  uint32_t p[32];                // pair j: c(2j) | c(2j+1) << 8 (8-bit containers)
-  __device__ __forceinline__ void put_pair(int j, uint32_t pair) { p[j] = pair; }
-  __device__ __forceinline__ void store(uint8_t *dst) const {
-    uint32_t w[12];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {     // 16 codes -> 96 bits -> 3 words
-      uint32_t t[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t a = p[g * 8 + 2 * k], b = p[g * 8 + 2 * k + 1];
-        t[k] = (a & 0x3Fu) | (((a >> 8) & 0x3Fu) << 6) | ((b & 0x3Fu) << 12) | (((b >> 8) & 0x3Fu) << 18);
-      }
-      w[g * 3 + 0] = t[0] | (t[1] << 24);
-      w[g * 3 + 1] = (t[1] >> 8) | (t[2] << 16);
-      w[g * 3 + 2] = (t[2] >> 16) | (t[3] << 8);
-    }
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    d[2] = make_uint4(w[8], w[9], w[10], w[11]);
-  }
-};
-
-template <> struct Packer<8> {   // one byte per code
-  uint32_t w[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-  __device__ __forceinline__ void put_pair(int j, uint32_t pair) {   // pair = c(2j) | c(2j+1) << 8
-    const int word = j >> 1, sh = (j & 1) * 16;
-    w[word] = (w[word] & ~(0xFFFFu << sh)) | (pair << sh);
-  }
-  __device__ __forceinline__ void store(uint8_t *dst) const {
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) d[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-  }
-};
-
-template <int FMT> __device__ __forceinline__ uint32_t pair_shift() { return FMT == 4 ? 4u : 8u; }
-
-// Codes of one block whose inputs are x[0..63] (in-block order), given its
-// scale value bs (fp32) and T_scale.  Returns nothing; fills the packer.
-template <int FMT>
-__device__ __forceinline__ void encode_block(const float (&x)[64], float bs, float s_t, Packer<FMT> &pk) {
-  float inv_lo = 0.0f, inv_hi = 0.0f;
-  if (bs > 0.0f) {
-    const float inv = __frcp_rn(bs * s_t);
-    inv_lo = inv * (1.0f - QEPS);
-    inv_hi = inv * (1.0f + QEPS);
-  }
-  uint32_t diff = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const uint32_t lo = cvt2<FMT>(x[2 * j] * inv_lo, x[2 * j + 1] * inv_lo);
-    const uint32_t hi = cvt2<FMT>(x[2 * j] * inv_hi, x[2 * j + 1] * inv_hi);
-    diff |= lo ^ hi;
-    pk.put_pair(j, lo);
-  }
-  if (diff) {   // some quotient lies within the bracket of a rounding midpoint
-    const float k = bs;
-    const uint32_t cmask = (FMT == 4) ? 0xFu : 0xFFu;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t lo = cvt2<FMT>(x[2 * j] * inv_lo, x[2 * j + 1] * inv_lo);
-      const uint32_t hi = cvt2<FMT>(x[2 * j] * inv_hi, x[2 * j + 1] * inv_hi);
-      if (lo == hi) continue;
-      uint32_t pair = 0;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const uint32_t sh = e * pair_shift<FMT>();
-        uint32_t cl = (lo >> sh) & cmask, ch = (hi >> sh) & cmask;
-        uint32_t c = cl;
-        if (cl != ch) {
-          const float v = x[2 * j + e];
-          c = resolve_tie<FMT>(fabsf(v), k, s_t, cl & Fmt<FMT>::MAG, ch & Fmt<FMT>::MAG) |
-              (signbit(v) ? Fmt<FMT>::SBIT : 0u);
-        }
-        pair |= c << sh;
-      }
-      pk.put_pair(j, pair);
+template <int F> struct RegRows {
+  static constexpr int NW = Fmt<F>::BLOCK_BYTES / 4;
+  uint32_t w[NW];
+  // r is a constant after unrolling; E2M3 rows are 48 bits, so an odd row
+  // starts in the upper half of a word that the row before it began
+  __device__ __forceinline__ void put(int r, uint64_t bits) {
+    if (F == 4) {
+      w[r] = (uint32_t)bits;
+    } else if (F == 8) {
+      w[2 * r] = (uint32_t)bits;
+      w[2 * r + 1] = (uint32_t)(bits >> 32);
+    } else if ((r & 1) == 0) {
+      w[3 * r / 2] = (uint32_t)bits;
+      w[3 * r / 2 + 1] = (uint32_t)(bits >> 32);
+    } else {
+      w[(3 * r - 1) / 2] |= (uint32_t)bits << 16;
+      w[(3 * r + 1) / 2] = (uint32_t)(bits >> 16);
     }
   }
-}
+  // 32-byte stores where the payload starts on a 32-byte boundary (every
+  // sector written whole in one request), else 16-byte stores
+  __device__ __forceinline__ void st32(uint8_t *d, int k) const {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(d), "r"(w[k]), "r"(w[k + 1]),
+                 "r"(w[k + 2]), "r"(w[k + 3]), "r"(w[k + 4]), "r"(w[k + 5]), "r"(w[k + 6]), "r"(w[k + 7])
+                 : "memory");
+  }
+  __device__ __forceinline__ void st16(uint8_t *d, int k) const {
+    *reinterpret_cast<uint4 *>(d) = make_uint4(w[k], w[k + 1], w[k + 2], w[k + 3]);
+  }
+  __device__ __forceinline__ void store(uint8_t *dst) const {
+    const bool a32 = (reinterpret_cast<uintptr_t>(dst) & 31u) == 0;
+    if (F == 6) {                                  // 48 bytes: 32 + 16 or 16 + 32
+      if (a32) {
+        st32(dst, 0);
+        st16(dst + 32, 8);
+      } else {
+        st16(dst, 0);
+        st32(dst + 16, 4);
+      }
+    } else if (a32) {
+#pragma unroll
+      for (int k = 0; k < NW / 8; ++k) st32(dst + 32 * k, 8 * k);
+    } else {
+#pragma unroll
+      for (int k = 0; k < NW / 4; ++k) st16(dst + 16 * k, 4 * k);
+    }
+  }
+};
 
 // -------------------------------------------------------------- quantize
 // Thread order: NCHW/OIHW -- spatial position fastest; HWCN -- n-group fastest.
@@ -251,9 +210,17 @@ __global__ void __launch_bounds__(256) quantize_kernel(const T *__restrict__ src
       }
       const uint32_t bs_code = block_scale_code<FMT>(amax_b, st);
       const float bs = code_value<8>(bs_code);
-      Packer<FMT> pk;
-      encode_block<FMT>(x, bs, st, pk);
-      pk.store(p.codes + b * Fmt<FMT>::BLOCK_BYTES);
+      float inv_lo, inv_hi;
+      quot_bracket(bs, st, inv_lo, inv_hi);
+      RegRows<FMT> rows;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        float v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = x[8 * r + c];
+        rows.put(r, encode_row8_b<FMT>(v, bs, st, inv_lo, inv_hi));
+      }
+      rows.store(p.codes + b * Fmt<FMT>::BLOCK_BYTES);
       p.scales[b] = (uint8_t)bs_code;
     }
   }
@@ -279,11 +246,12 @@ template <typename T> __device__ __forceinline__ uint32_t to_bits32(uint32_t raw
 // Block scale and codes of one block whose 64 inputs are held as raw bits
 // (bf16 inputs two to a register, element 2k in the low half), row a of the
 // block (8 consecutive b) at raw[8a / PK ...]; `mb` is the block amax (fp32
-// bits).  The packed rows go to `ob`; returns the E4M3 scale code.  TINY:
+// bits).  The packed rows go to the sink `ob` (SmemRows or RegRows); returns
+// the E4M3 scale code.  TINY:
 // T_scale below 2^-62, encoded from x 2^64 and T_scale 2^64 (see up64).
-template <int FMT, typename T, bool TINY>
+template <int FMT, typename T, bool TINY, class Sink>
 __device__ __forceinline__ uint32_t encode_raw_block(const uint32_t (&raw)[sizeof(T) == 2 ? 32 : 64], uint32_t mb,
-                                                     float s_t, uint8_t *ob) {
+                                                     float s_t, Sink &ob) {
   const float st = TINY ? s_t * TINY_MULT : s_t;
   const float amax_b = TINY ? up64(__uint_as_float(mb)) : __uint_as_float(mb);
   const uint32_t bs_code = block_scale_code<FMT>(amax_b, st);
@@ -303,7 +271,7 @@ __device__ __forceinline__ uint32_t encode_raw_block(const uint32_t (&raw)[sizeo
       }
       if (TINY) x[b] = up64(x[b]);
     }
-    store_row8<FMT>(ob, a, encode_row8_b<FMT>(x, bs, st, inv_lo, inv_hi));
+    ob.put(a, encode_row8_b<FMT>(x, bs, st, inv_lo, inv_hi));
   }
   return bs_code;
 }
@@ -311,9 +279,9 @@ __device__ __forceinline__ uint32_t encode_raw_block(const uint32_t (&raw)[sizeo
 // The same block with stochastically rounded element codes (block `blk` of
 // the packed tensor, Philox key `seed`; see encode_row8_sr).  The block scale
 // is the round-to-nearest one.
-template <int FMT, typename T>
+template <int FMT, typename T, class Sink>
 __device__ __forceinline__ uint32_t encode_raw_block_sr(const uint32_t (&raw)[sizeof(T) == 2 ? 32 : 64], uint32_t mb,
-                                                        float s_t, uint8_t *ob, int64_t blk, uint64_t seed) {
+                                                        float s_t, Sink &ob, int64_t blk, uint64_t seed) {
   const bool tiny = is_tiny_scale(s_t);
   const float amax_b = __uint_as_float(mb);
   const uint32_t bs_code = tiny ? block_scale_code<FMT>(up64(amax_b), s_t * TINY_MULT)
@@ -331,7 +299,7 @@ __device__ __forceinline__ uint32_t encode_raw_block_sr(const uint32_t (&raw)[si
         x[b] = __uint_as_float(raw[(a * 8 + b) & 63]);
       }
     }
-    store_row8<FMT>(ob, a, encode_row8_sr<FMT>(x, d, seed, blk, a));
+    ob.put(a, encode_row8_sr<FMT>(x, d, seed, blk, a));
   }
   return bs_code;
 }
@@ -341,9 +309,9 @@ __device__ __forceinline__ uint32_t encode_raw_block_sr(const uint32_t (&raw)[si
 // hw; the packed output is contiguous along the b-groups of one (hw, a-group).
 // A CTA of 8 warps takes one a-group, 8 b-groups (one per warp) and 32
 // positions (one per lane): each thread quantizes one block from 64 loads that
-// are coalesced across the warp (consecutive positions), parks the packed
-// block in shared memory, and the CTA writes each position's 8 blocks out as
-// one contiguous run.
+// are coalesced across the warp (consecutive positions) and writes the packed
+// block and its scale straight to global memory; the eight warps write
+// neighbouring blocks, so lines fill in L2 before they are written back.
 constexpr int QN_HW = 32, QN_GB = 8;
 
 // CTA shape: GBT b-groups (one warp each) x (8 / GBT) chunks of 32 positions;
@@ -351,8 +319,7 @@ constexpr int QN_HW = 32, QN_GB = 8;
 // The work of one quantize_nchw_kernel CTA after T_scale is known (TINY:
 // T_scale below 2^-62).
 template <int FMT, typename T, bool SR, bool TINY>
-__device__ __forceinline__ void nchw_body(const T *__restrict__ src, const QuantParams &p, uint8_t *obuf,
-                                          uint8_t *sbuf, float s_t) {
+__device__ __forceinline__ void nchw_body(const T *__restrict__ src, const QuantParams &p, float s_t) {
   constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
   const int GA = (int)(p.d0 / 8), GB = (int)(p.d1 / 8);
   const int GBT = GB < QN_GB ? GB : QN_GB, HWT = QN_HW * (QN_GB / GBT);
@@ -368,7 +335,6 @@ __device__ __forceinline__ void nchw_body(const T *__restrict__ src, const Quant
   const int nhw = (int)(HW - hw0 < (int64_t)HWT ? HW - hw0 : (int64_t)HWT);
   const int warp = threadIdx.x >> 5;
   const int wl = warp % GBT, hl = (warp / GBT) * 32 + (threadIdx.x & 31);
-  const int opitch = GBT * BB + 16;    // staged bytes per position
   uint32_t my_amax = 0;
   if (wl < ngb && hl < nhw) {
     // the block's 64 inputs, row a = 8 consecutive b; rows and columns are
@@ -399,28 +365,12 @@ __device__ __forceinline__ void nchw_body(const T *__restrict__ src, const Quant
     }
     my_amax = mb;
     if (mb >= 0x7F800000u) atomicOr(p.status, ST_NONFINITE);
-    uint8_t *ob = obuf + hl * opitch + wl * BB;
-    uint32_t bs_code;
-    if (SR) {
-      const int64_t blk = ((hw0 + hl) * GA + ga) * (int64_t)GB + gb0 + wl;
-      bs_code = encode_raw_block_sr<FMT, T>(raw, mb, s_t, ob, blk, p.sr_seed);
-    } else {
-      bs_code = encode_raw_block<FMT, T, TINY>(raw, mb, s_t, ob);
-    }
-    sbuf[hl * GBT + wl] = (uint8_t)bs_code;
-  }
-  __syncthreads();
-  {
-    const int units = ngb * BB / 16;
-    for (int w = threadIdx.x; w < nhw * units; w += 256) {
-      const int h = w / units, u = w - h * units;
-      const int64_t blk0 = ((hw0 + h) * GA + ga) * (int64_t)GB + gb0;
-      reinterpret_cast<uint4 *>(p.codes + blk0 * BB)[u] = reinterpret_cast<const uint4 *>(obuf + h * opitch)[u];
-    }
-    for (int w = threadIdx.x; w < nhw * ngb; w += 256) {
-      const int h = w / ngb, b = w - h * ngb;
-      p.scales[((hw0 + h) * GA + ga) * (int64_t)GB + gb0 + b] = sbuf[h * GBT + b];
-    }
+    const int64_t blk = ((hw0 + hl) * GA + ga) * (int64_t)GB + gb0 + wl;
+    RegRows<FMT> rows;
+    const uint32_t bs_code = SR ? encode_raw_block_sr<FMT, T>(raw, mb, s_t, rows, blk, p.sr_seed)
+                                : encode_raw_block<FMT, T, TINY>(raw, mb, s_t, rows);
+    rows.store(p.codes + blk * BB);
+    p.scales[blk] = (uint8_t)bs_code;
   }
   if (p.amax_meas_bits) {
     uint32_t m = my_amax;
@@ -431,16 +381,12 @@ __device__ __forceinline__ void nchw_body(const T *__restrict__ src, const Quant
 }
 
 template <int FMT, typename T>
-__device__ __noinline__ void nchw_body_tiny(const T *__restrict__ src, const QuantParams &p, uint8_t *obuf,
-                                            uint8_t *sbuf, float s_t) {
-  nchw_body<FMT, T, false, true>(src, p, obuf, sbuf, s_t);
+__device__ __noinline__ void nchw_body_tiny(const T *__restrict__ src, const QuantParams &p, float s_t) {
+  nchw_body<FMT, T, false, true>(src, p, s_t);
 }
 
 template <int FMT, typename T, bool SR>
-__global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2) quantize_nchw_kernel(const T *__restrict__ src, QuantParams p) {
-  constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
-  __shared__ __align__(16) uint8_t obuf[QN_HW * QN_GB * BB + QN_HW * QN_GB * 16];   // HWT * opitch at most
-  __shared__ uint8_t sbuf[QN_HW * QN_GB];
+__global__ void __launch_bounds__(256, 2) quantize_nchw_kernel(const T *__restrict__ src, QuantParams p) {
   const float amax_src = __uint_as_float(*p.amax_src_bits);
   const float s_t = __fdiv_rn(amax_src, Fmt<FMT>::DENOM);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -449,8 +395,8 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2) quantize_nchw_ker
   }
   // stochastic codes decide from the unscaled T_scale; the tiny-T_scale
   // round-to-nearest encode runs in an out-of-line copy
-  if (!SR && is_tiny_scale(s_t)) nchw_body_tiny<FMT, T>(src, p, obuf, sbuf, s_t);
-  else nchw_body<FMT, T, SR, false>(src, p, obuf, sbuf, s_t);
+  if (!SR && is_tiny_scale(s_t)) nchw_body_tiny<FMT, T>(src, p, s_t);
+  else nchw_body<FMT, T, SR, false>(src, p, s_t);
 }
 
 
@@ -488,14 +434,17 @@ __device__ __forceinline__ bool qt_wait(uint64_t *bar, uint32_t parity, Ctl *ctl
 }
 
 // The quantizing warps' loop over the CTA's tiles (see quantize_tma_kernel);
-// returns the largest |x| seen (fp32 bits).  TINY: T_scale below 2^-62.
+// returns the largest |x| seen (fp32 bits).  Each thread encodes one block
+// and writes its payload and scale straight to global memory (16-byte
+// stores; the eight warps of a tile write neighbouring blocks, so lines fill
+// in L2 before they are written back), so the warps never wait on one
+// another.  TINY: T_scale below 2^-62.
 template <int FMT, typename T, int GBT, bool TINY>
-__device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl, uint8_t *ring, uint8_t *obuf,
-                                                uint8_t *sbuf, int ntiles, int hw_tiles, int gb_tiles, float s_t) {
+__device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl, uint8_t *ring, int ntiles,
+                                                int hw_tiles, int gb_tiles, float s_t) {
   constexpr int HWT = QN_HW * (QN_GB / GBT);
   constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
   constexpr int STAGE = HWT * GBT * 64 * (int)sizeof(T);
-  constexpr int OPITCH = GBT * BB + 16;
   const int GA = (int)(p.d0 / 8), GB = (int)(p.d1 / 8);
   const int64_t HW = p.d2 * p.d3;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -504,8 +453,7 @@ __device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl
   int it = 0;
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int s = it % QT_STAGES;
-    // a failed wait still takes part in the named barriers below
-    const bool ok = qt_wait(&ctl->full[s], (it / QT_STAGES) & 1, ctl, p.status);
+    if (!qt_wait(&ctl->full[s], (it / QT_STAGES) & 1, ctl, p.status)) break;
     const int hwt = t % hw_tiles, rest = t / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
     const int64_t hw0 = (int64_t)hwt * HWT;
     const int gb0 = gbt * GBT;
@@ -513,7 +461,7 @@ __device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl
     const int nhw = (int)(HW - hw0 < (int64_t)HWT ? HW - hw0 : (int64_t)HWT);
     // tile in shared memory: [a (8)][b (GBT*8)][hw (HWT)], hw fastest
     const T *tile = reinterpret_cast<const T *>(ring + s * STAGE) + (wl * 8) * HWT + hl;
-    const bool mine = ok && wl < ngb && hl < nhw;
+    const bool mine = wl < ngb && hl < nhw;
     uint32_t raw[sizeof(T) == 2 ? 32 : 64];
     if (mine) {
 #pragma unroll
@@ -546,24 +494,12 @@ __device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl
       }
       my_amax = max(my_amax, mb);
       if (mb >= 0x7F800000u) atomicOr(p.status, ST_NONFINITE);
-      uint8_t *ob = obuf + hl * OPITCH + wl * BB;
-      const uint32_t bs_code = encode_raw_block<FMT, T, TINY>(raw, mb, s_t, ob);
-      sbuf[hl * GBT + wl] = (uint8_t)bs_code;
+      const int64_t blk = ((hw0 + hl) * GA + ga) * (int64_t)GB + gb0 + wl;
+      RegRows<FMT> rows;
+      const uint32_t bs_code = encode_raw_block<FMT, T, TINY>(raw, mb, s_t, rows);
+      rows.store(p.codes + blk * BB);
+      p.scales[blk] = (uint8_t)bs_code;
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(QT_CWARPS * 32) : "memory");
-    if (!*reinterpret_cast<volatile int *>(&ctl->abort)) {
-      const int units = ngb * BB / 16;
-      for (int w = threadIdx.x; w < nhw * units; w += QT_CWARPS * 32) {
-        const int h = w / units, u = w - h * units;
-        const int64_t blk0 = ((hw0 + h) * GA + ga) * (int64_t)GB + gb0;
-        reinterpret_cast<uint4 *>(p.codes + blk0 * BB)[u] = reinterpret_cast<const uint4 *>(obuf + h * OPITCH)[u];
-      }
-      for (int w = threadIdx.x; w < nhw * ngb; w += QT_CWARPS * 32) {
-        const int h = w / ngb, b = w - h * ngb;
-        p.scales[((hw0 + h) * GA + ga) * (int64_t)GB + gb0 + b] = sbuf[h * GBT + b];
-      }
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(QT_CWARPS * 32) : "memory");
   }
   return my_amax;
 }
@@ -571,23 +507,19 @@ __device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl
 // the tiny-T_scale loop, kept out of line (rare; inlined beside the common
 // loop it would raise the register pressure of every launch)
 template <int FMT, typename T, int GBT>
-__device__ __noinline__ uint32_t tma_compute_tiny(const QuantParams &p, QtCtl *ctl, uint8_t *ring, uint8_t *obuf,
-                                                  uint8_t *sbuf, int ntiles, int hw_tiles, int gb_tiles, float s_t) {
-  return tma_compute<FMT, T, GBT, true>(p, ctl, ring, obuf, sbuf, ntiles, hw_tiles, gb_tiles, s_t);
+__device__ __noinline__ uint32_t tma_compute_tiny(const QuantParams &p, QtCtl *ctl, uint8_t *ring, int ntiles,
+                                                  int hw_tiles, int gb_tiles, float s_t) {
+  return tma_compute<FMT, T, GBT, true>(p, ctl, ring, ntiles, hw_tiles, gb_tiles, s_t);
 }
 
 template <int FMT, typename T, int GBT>
 __global__ void __launch_bounds__(QT_THREADS, 2)
     quantize_tma_kernel(const __grid_constant__ CUtensorMap tm, QuantParams p, int ntiles, int hw_tiles, int gb_tiles) {
   constexpr int HWT = QN_HW * (QN_GB / GBT);
-  constexpr int BB = Fmt<FMT>::BLOCK_BYTES;
   constexpr int STAGE = HWT * GBT * 64 * (int)sizeof(T);
-  constexpr int OPITCH = GBT * BB + 16;
-  extern __shared__ __align__(1024) uint8_t qraw[];
-  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(qraw) + 1023) & ~uintptr_t(1023));
-  uint8_t *obuf = ring + QT_STAGES * STAGE;
-  uint8_t *sbuf = obuf + HWT * OPITCH;
-  QtCtl *ctl = reinterpret_cast<QtCtl *>(sbuf + ((HWT * GBT + 15) / 16) * 16);
+  extern __shared__ __align__(128) uint8_t qraw[];
+  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(qraw) + 127) & ~uintptr_t(127));
+  QtCtl *ctl = reinterpret_cast<QtCtl *>(ring + QT_STAGES * STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const float amax_src = __uint_as_float(*p.amax_src_bits);
@@ -628,8 +560,8 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
 
   // --------------------------------------------------------------- compute
   const uint32_t my_amax =
-      is_tiny_scale(s_t) ? tma_compute_tiny<FMT, T, GBT>(p, ctl, ring, obuf, sbuf, ntiles, hw_tiles, gb_tiles, s_t)
-                         : tma_compute<FMT, T, GBT, false>(p, ctl, ring, obuf, sbuf, ntiles, hw_tiles, gb_tiles, s_t);
+      is_tiny_scale(s_t) ? tma_compute_tiny<FMT, T, GBT>(p, ctl, ring, ntiles, hw_tiles, gb_tiles, s_t)
+                         : tma_compute<FMT, T, GBT, false>(p, ctl, ring, ntiles, hw_tiles, gb_tiles, s_t);
   if (p.amax_meas_bits) {
     uint32_t m = my_amax;
 #pragma unroll
@@ -649,8 +581,7 @@ static cudaError_t launch_tma_q(const T *src, const QuantParams &p, int num_sms,
   const int64_t hw_tiles = (HW + HWT - 1) / HWT, gb_tiles = (GB + GBT - 1) / GBT;
   const int64_t ntiles = GA * gb_tiles * hw_tiles;
   constexpr size_t STAGE = (size_t)HWT * GBT * 64 * sizeof(T);
-  const size_t smem = 1024 + QT_STAGES * STAGE + (size_t)HWT * (GBT * Fmt<FMT>::BLOCK_BYTES + 16) +
-                      ((HWT * GBT + 15) / 16) * 16 + sizeof(QtCtl);
+  const size_t smem = 128 + QT_STAGES * STAGE + sizeof(QtCtl);
   auto k = quantize_tma_kernel<FMT, T, GBT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -167,3 +167,53 @@ def test_supplied_statistic_far_below_data(cuda_device, fmt, data_amax, stat):
         p, _ = gpu_quantize(to_dev(x, dtype, cuda_device), fmt, "act", "nchw", x.shape, amax_in=stat)
         ref = oracle.quantize(x, fmt, "act", "nchw", amax_in=stat)
         assert_packed_equal(p, ref, f"data {data_amax} statistic {stat} {fmt} {dtype}")
+
+
+EMAXV = {"e2m1": 6.0, "e2m3": 7.5, "e4m3": 448.0}
+
+
+def tie_dense(shape, seed, fmt, exact):
+    """ReLU(N(0,1)) in bf16 whose amax puts many quotients on or next to a
+    rounding midpoint.  exact: amax = maxB_ef * 448 / 256, so T_scale = 2^-8
+    exactly and quotients of few-bit bf16 values land exactly on midpoints.
+    Otherwise amax = 5.46875 = 175/32, which shares factors with maxB_ef * 448
+    (2688 = 2^7 * 21, 3360 = 2^5 * 105, 200704 = 2^12 * 49): T_scale is a
+    short fraction rounded once to fp32, and quotients land within about
+    2^-24 of midpoints, inside the 2^-20 bracket, yet not on them."""
+    x = np.maximum(np.random.default_rng(seed).standard_normal(shape), 0).astype(np.float32)
+    top = np.float32(EMAXV[fmt] * 448 / 256) if exact else np.float32(5.46875)
+    x = S.to_bf16_rne(np.minimum(x * (top / np.float32(5.5) if exact else 1.0), top * 0.99).astype(np.float32))
+    x.ravel()[0] = top
+    return x
+
+
+def near_midpoint_blocks(x, fmt, role, layout, stat=None):
+    """Fraction of blocks whose oracle codes change when every input moves by
+    a relative 2^-20 either way (same statistic, by default the amax): blocks
+    with a quotient on or next to a rounding midpoint."""
+    a = float(np.abs(x).max()) if stat is None else stat
+    ends = [oracle.quantize((x.astype(np.float64) * (1 + d * 2.0 ** -20)).astype(np.float32), fmt, role, layout,
+                            amax_in=a) for d in (-1, 1)]
+    c0, c1 = (e["codes"].reshape(len(e["scales"]), -1) for e in ends)
+    return float((c0 != c1).any(axis=1).mean())
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("exact", [False, True], ids=["near-ties", "exact-ties"])
+@pytest.mark.parametrize("path", ["nchw-bf16-tma", "nchw-bf16-direct", "nchw-f32-tma", "hwcn-bf16"])
+def test_tie_dense_inputs(cuda_device, fmt, exact, path):
+    """Inputs with many quotients on, or within fp32 rounding of, a rounding
+    midpoint (5 % to 70 % of blocks): every encoder path settles them exactly
+    like the oracle, codes and scales bit for bit."""
+    layout, dtype, shape = {"nchw-bf16-tma": ("nchw", "bf16", (32, 64, 16, 16)),
+                            "nchw-bf16-direct": ("nchw", "bf16", (32, 64, 7, 7)),
+                            "nchw-f32-tma": ("nchw", "f32", (32, 16, 8, 8)),
+                            "hwcn-bf16": ("hwcn", "bf16", (6, 7, 64, 32))}[path]
+    x = tie_dense(shape, 3, fmt, exact)
+    role = "act" if layout == "nchw" else "grad"
+    dims = shape if layout == "nchw" else (shape[3], shape[2], shape[0], shape[1])
+    assert near_midpoint_blocks(x, fmt, role, layout) > 0.03
+    p, a = gpu_quantize(to_dev(x, dtype, cuda_device), fmt, role, layout, dims)
+    ref = oracle.quantize(x, fmt, role, layout)
+    assert a == ref["amax"]
+    assert_packed_equal(p, ref, f"tie-dense {path} {fmt} {'exact' if exact else 'near'}")

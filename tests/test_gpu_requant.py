@@ -186,3 +186,65 @@ def test_wide_requant(cuda_device, fmt, L, scale):
         mq.check_device_status()
         assert torch.equal(y2, ref), f"{op}: fp32 output beside the fused epilogue differs from the unfused one"
         _check(out, ref_np, fmt, role, stat, aout, f"wide {op} requant {fmt} {L.name()} x{scale}")
+
+
+EMAXV = {"e2m1": 6.0, "e2m3": 7.5, "e4m3": 448.0}
+
+
+def _single_product_inputs(L, fmt, seed):
+    """Sparse operands under which every output of fwd and dgrad is a single
+    product of two dequantized values (or zero): X nonzero only in channel 0,
+    dY only in channel 0, both only at rows and columns that are multiples of
+    4 (any three consecutive rows or columns hold at most one).  The amax of X,
+    W and dY are maxB_ef * 448 times powers of two, so their T_scale are exact
+    powers of two and each product has few significant bits: its quotients
+    land on, or next to, rounding midpoints of the requantized grid."""
+    rng = np.random.default_rng(seed)
+    e = np.float32(EMAXV[fmt] * 448)
+    X = np.zeros(L.x_shape(), np.float32)
+    X[:, 0, ::4, ::4] = np.maximum(rng.standard_normal(X[:, 0, ::4, ::4].shape), 0)
+    X = (X / X.max() * e * np.float32(2.0 ** -8)).astype(np.float32)
+    X[0, 0, 0, 0] = e * np.float32(2.0 ** -8)
+    W = rng.standard_normal(L.w_shape()).astype(np.float32)
+    W = (W / np.abs(W).max() * e * np.float32(0.9 * 2.0 ** -10)).astype(np.float32)
+    W[0, 0, 0, 0] = e * np.float32(2.0 ** -10)
+    dY = np.zeros(L.y_shape(), np.float32)
+    dY[:, 0, ::4, ::4] = rng.standard_normal(dY[:, 0, ::4, ::4].shape)
+    dY = (dY / np.abs(dY).max() * e * np.float32(0.9 * 2.0 ** -6)).astype(np.float32)
+    dY[0, 0, 0, 0] = e * np.float32(2.0 ** -6)
+    return X, W, dY
+
+
+def _tie_stat(amax, fmt, exact):
+    """maxB_ef * 448 times the power of two nearest amax / (maxB_ef * 448)
+    (T_scale exact: quotients exactly on midpoints), else 175/32 times a
+    power of two (T_scale a short fraction rounded once: quotients within
+    fp32 rounding of midpoints)."""
+    base = EMAXV[fmt] * 448 if exact else 5.46875
+    return float(np.float32(base * 2.0 ** round(np.log2(amax / base))))
+
+
+@pytest.mark.parametrize("fmt", ["e2m1", "e2m3", "e4m3"])
+@pytest.mark.parametrize("L", [LAYERS[1], LAYERS[3], LAYERS[5]], ids=["halo", "generic-1x1-s2", "halo-s2"])
+def test_requant_tie_dense(cuda_device, fmt, L):
+    """Fused fwd and dgrad epilogues on outputs whose quotients sit on, or
+    within fp32 rounding of, rounding midpoints: bit-exact against the oracle
+    quantizer on the unfused fp32 results with the same statistic."""
+    from test_gpu_quantize import near_midpoint_blocks
+    run = LayerRun(L, fmt, "f32", *_single_product_inputs(L, fmt, L.N + L.Cin), cuda_device, check_quant=True)
+    assert float(run.xq.s_t.item()) == 2.0 ** -8 and float(run.wq.s_t.item()) == 2.0 ** -10
+    for op, role, shape in (("fwd", "act", L.y_shape()), ("dgrad", "grad", L.x_shape())):
+        ref_np = (run.fwd() if op == "fwd" else run.dgrad()).cpu().numpy()
+        for exact in (True, False):
+            stat = _tie_stat(float(np.max(np.abs(ref_np))), fmt, exact)
+            if exact:
+                assert near_midpoint_blocks(ref_np, fmt, role, "hwcn", stat) > 0.005
+            out = mq.Packed(fmt, role, shape, device=cuda_device)
+            ain = torch.tensor([stat], device=cuda_device)
+            aout = torch.zeros(1, device=cuda_device)
+            if op == "fwd":
+                mq.fwd(L, run.xq, run.wq, None, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
+            else:
+                mq.dgrad(L, run.wq, run.gq, None, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
+            mq.check_device_status()
+            _check(out, ref_np, fmt, role, stat, aout, f"tie-dense {op} requant {fmt} {L.name()} exact={exact}")
