@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmqconv.so")
 SOURCES = ["api.cu", "quantize.cu", "conv.cu", "conv_halo.cu", "conv_halo_fwd_a.cu", "conv_halo_fwd_b.cu", "conv_halo_dgrad_a.cu",
-           "conv_halo_dgrad_b.cu", "conv_halo_wide.cu"]
+           "conv_halo_dgrad_b.cu"]
 HEADERS = ["common.cuh", "conv_halo.cuh", "kernels.h", os.path.join("..", "..", "include", "mqconv.h")]
 
 NVCC_FLAGS = [

@@ -406,58 +406,6 @@ int pow2_at_least32(int x) {
 
 }  // namespace
 
-// The wide form's tile: P positions x G batch groups with P G = 32 (least
-// padding waste), 128 output channels, R = 2 output rows (one when the output
-// has one row); two accumulators of 128 lanes x 256 columns fill the TMEM.
-// h arrives with the geometry fields of halo_plan set; false when the tile
-// does not fit (the caller then plans the narrow form).
-constexpr bool kWidePlanEnabled = false;
-
-static bool wide_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
-  (void)num_sms;
-  HaloConv c = h;
-  c.NPHS = 1;
-  c.outH = c.Hout;
-  c.outW = c.Wout;
-  c.NCG = c.NC / 8;
-  int best = -1;
-  double best_waste = 1e30;
-  for (int P = 32; P >= 1; P >>= 1) {
-    const int G = 32 / P;
-    if (G > c.NG || c.NG % G) continue;
-    const double waste = (double)((c.Wout + P - 1) / P * P) / c.Wout;
-    if (waste < best_waste - 1e-9) {
-      best_waste = waste;
-      best = P;
-    }
-  }
-  if (best < 0) return false;
-  c.P = best;
-  c.G = 32 / best;
-  c.BN = 128;
-  c.NB = 16;
-  c.acc_cols = 256;
-  c.NS = 2;
-  c.ns_log2 = 1;
-  c.R = c.Hout >= 2 ? 2 : 1;
-  c.RT = c.R;
-  const size_t sm = halo_smem(c, block_bytes(cp.a.fmt), block_bytes(cp.b.fmt));
-  if (!sm) return false;
-  c.smem = sm;
-  c.gran_h = pow2_part(c.G * c.CGin);
-  c.gran_w = c.op == OP_FWD ? pow2_part(c.CIG * std::gcd(c.COG, c.NB)) : pow2_part(std::gcd(c.CIG, c.NB));
-  c.tiles_g = c.NG / c.G;
-  c.tiles_w = (c.Wout + c.P - 1) / c.P;
-  c.tiles_h = (c.Hout + c.R - 1) / c.R;
-  c.tiles_n = (c.NC + c.BN - 1) / c.BN;
-  const int64_t nt = (int64_t)c.tiles_g * c.tiles_w * c.tiles_h * c.tiles_n;
-  if (nt <= 0 || nt > INT32_MAX) return false;
-  c.num_tiles = (int)nt;
-  c.wide = 1;
-  h = c;
-  return true;
-}
-
 // Plans the halo kernel for a forward (stride 1 or 2) or data-gradient
 // (stride 1, or stride 2 as output quads) convolution;
 // returns false when the layer does not fit its constraints (the caller then
@@ -527,14 +475,6 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
   if (h.CGin % CGC) return false;
   h.nchunks = h.CGin / CGC;
   if (!qd) { h.HKh = h.Kh; h.HKw = h.Kw; }
-  // the wide form would apply to stride 1, at least 128 output channels, one
-  // operand format, requantization (if any) into that format, not
-  // stochastic, at most 3 x 3 taps; it is not selected: on the 56x56 C128
-  // layer it measured 287 us against 219 us for this (narrow) form, the
-  // per-block decode rate, not the MMAs, bounding both
-  if (kWidePlanEnabled && !qd && h.S == 1 && h.NC >= 128 && cp.a.fmt == cp.b.fmt && h.Kh * h.Kw <= 9 &&
-      (!cp.rq.codes || (cp.rq.fmt == cp.a.fmt && !cp.rq.sr)) && wide_plan(cp, h, num_sms))
-    return true;
   // positions x batch groups = 16 row groups (M = 128); least padding waste
   int best = -1;
   double best_waste = 1e30;
@@ -663,7 +603,6 @@ cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStre
   }
   const int grid = std::min(h.num_tiles, num_sms);
   const int fr = cp.rq.codes ? cp.rq.fmt : 0;
-  if (h.wide) return halo_dispatch_wide(cp.op, cp.a.fmt, fr, ma, mb, h, grid, st);
   if (cp.op == OP_FWD)
     return fr == 0 || fr == 4 ? halo_dispatch_fwd_04(cp.a.fmt, cp.b.fmt, fr, ma, mb, h, grid, st)
                               : halo_dispatch_fwd_68(cp.a.fmt, cp.b.fmt, fr, ma, mb, h, grid, st);

@@ -488,222 +488,9 @@ __device__ __forceinline__ void hc_epilogue_entry(const HaloConv &p, HcCtl *ctl,
 }
 
 
-// ------------------------------------------------------------- wide form
-// For stride-1 layers with at least 128 output channels the same tile data
-// runs through MMAs of N = 256: the operand roles are swapped, A = the
-// decoded weights (M = 128 output channels, from the same shared-memory
-// layout the narrow form reads as its B operand) and B = the decoded halo
-// (N = 256 GEMM rows: one output row of P positions x G batch groups with
-// P G = 32).  A 128 x 256 x 16 MMA does twice the work of a 128 x 128 x 16
-// one for less than twice the operand traffic, and halves the MMA
-// instructions the issuers have to send.  The accumulator of an output row
-// is 128 lanes (channels) x 256 columns (positions x batch); two of them fill
-// the TMEM.  Producer and decoders are those of the narrow form.
-
-template <int OP>
-__device__ __forceinline__ void hc_issue_wide(const HaloConv &p, HcCtl *ctl, uint8_t *smem, uint32_t tmem, int warp,
-                                              int lane) {
-  const int issuer = warp - HC_MMA_WARP, NI = p.RT >= 2 ? 2 : 1;
-  if (lane == 0 && issuer < NI) {
-    const uint32_t idesc = idesc_f16(128, 256, OP == OP_DGRAD, false);
-    // descriptor low words step by (bytes >> 4) as in hc_issue
-    const uint64_t a_desc = OP == OP_FWD ? sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), 128, CGC * 128)
-                                         : sdesc(smem_u32(smem + p.off_dec + p.dec_b_off), p.NB * 128, 128);
-    const uint64_t b_desc = sdesc(smem_u32(smem + p.off_dec), 128, CGC * 128);
-    const uint32_t a_hi = (uint32_t)(a_desc >> 32), b_hi = (uint32_t)(b_desc >> 32);
-    const uint32_t d_row = (uint32_t)((p.WP * p.G * CGC * 128) >> 4);     // one halo row
-    const uint32_t d_col = (uint32_t)((p.G * CGC * 128) >> 4);            // one halo position
-    const uint32_t d_tap = (uint32_t)((p.NB * CGC * 128) >> 4);           // one weight tap
-    const uint32_t d_stage = p.dec_stage >> 4;
-    const int taps = p.Kh * p.Kw;
-    constexpr int UT = 9;
-    uint32_t w_off[UT], h_off[UT];
-#pragma unroll
-    for (int t = 0; t < UT; ++t) {
-      const int u = t / p.Kw, v = t - u * p.Kw;
-      h_off[t] = (uint32_t)u * d_row + (uint32_t)v * d_col;
-      w_off[t] = (uint32_t)(OP == OP_FWD ? t : taps - 1 - t) * d_tap;
-    }
-    int dit = 0, k = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
-      for (int c = 0; c < p.nchunks; ++c, ++dit) {
-        const int ds = dit % DSTAGES;
-        if (!hc_wait(&ctl->dfull[ds], (dit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t w_stage = (uint32_t)a_desc + (uint32_t)ds * d_stage;
-        const uint32_t h_stage = (uint32_t)b_desc + (uint32_t)ds * d_stage;
-        uint32_t wq[UT];
-#pragma unroll
-        for (int tp = 0; tp < UT; ++tp) wq[tp] = w_stage + w_off[tp];
-        for (int sl = issuer; sl < p.RT && ok; sl += NI) {
-          const int ring = k * p.RT + sl, slot = ring & (p.NS - 1), use = ring >> p.ns_log2;
-          if (c == 0) {
-            if (!hc_wait(&ctl->acc_empty[slot], (use & 1) ^ 1, p, ctl)) { ok = false; break; }
-            tc_fence_after();
-          }
-          const uint32_t d = tmem + slot * p.acc_cols;
-          const uint32_t h_s = h_stage + (uint32_t)sl * d_row;
-          if (taps == UT) {   // 3x3: no per-tap predicate
-            umma_f16(d, desc_of(a_hi, wq[0]), desc_of(b_hi, h_s + h_off[0]), idesc, c > 0 ? 1u : 0u);
-#pragma unroll
-            for (int tp = 1; tp < UT; ++tp) umma_f16_acc(d, desc_of(a_hi, wq[tp]), desc_of(b_hi, h_s + h_off[tp]), idesc);
-          } else {
-#pragma unroll
-            for (int tp = 0; tp < UT; ++tp)
-              if (tp < taps)
-                umma_f16(d, desc_of(a_hi, wq[tp]), desc_of(b_hi, h_s + h_off[tp]), idesc, (tp > 0 || c > 0) ? 1u : 0u);
-          }
-          if (c == p.nchunks - 1) umma_commit(&ctl->acc_full[slot]);
-        }
-        umma_commit(&ctl->dempty[ds]);
-      }
-    }
-    umma_commit(&ctl->done);
-    hc_drain(&ctl->done, 0, p.status);   // every MMA issued so far has completed
-  }
-  __syncwarp();
-}
-
-// One 8 x 8 block of the wide accumulator -- lanes 8k .. 8k+7 of the warp
-// hold its 8 channels, v[] the 8 batch entries of the lane's channel -- into
-// the packed output: block amax by shuffles, block scale, each lane's codes
-// for its channel (a block column), then an 8 x 8 transpose of the codes
-// across the 8 lanes (three butterfly stages), after which lane 8k + r holds
-// row r of the block (8 channels of batch entry r).  All 32 lanes take part;
-// `ok` says whether this group's block is in range.  TINY as in hc_requant.
-template <int F, bool TINY>
-__device__ __forceinline__ void wide_requant_block(const HaloConv &p, const float (&v)[8], int64_t blk, bool ok,
-                                                   float st_q, float inv_den, uint32_t &amax_acc) {
-  const int lane = threadIdx.x & 31, r = lane & 7;
-  uint32_t m = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) m = max(m, __float_as_uint(v[j]) & 0x7FFFFFFFu);
-  if (!ok) m = 0;
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  amax_acc = max(amax_acc, m);
-  const uint32_t bsc = block_scale_code_r<F>(TINY ? up64(__uint_as_float(m)) : __uint_as_float(m), st_q, inv_den);
-  const float bs = code_value<8>(bsc);
-  float inv_lo, inv_hi;
-  quot_bracket(bs, st_q, inv_lo, inv_hi);
-  float x[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) x[j] = TINY ? up64(v[j]) : v[j];
-  constexpr int W = F == 4 ? 4 : 8;                    // container width: nibbles, else bytes
-  uint64_t col = encode_row8_b<F, false>(x, bs, st_q, inv_lo, inv_hi);
-#pragma unroll
-  for (int sft = 1; sft < 8; sft <<= 1) {
-    // field n of every lane: element (n, channel lane) -> (channel n, element lane)
-    uint64_t mask = 0;
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-      if (!(n & sft)) mask |= ((1ull << W) - 1) << (W * n);
-    const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)col, sft);
-    const uint32_t hi = W == 8 ? __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)(col >> 32), sft) : 0u;
-    const uint64_t y = (uint64_t)lo | ((uint64_t)hi << 32);
-    col = (r & sft) ? ((col & ~mask) | ((y & ~mask) >> (sft * W))) : ((col & mask) | ((y & mask) << (sft * W)));
-    if (W == 4) col &= 0xFFFFFFFFull;
-  }
-  if (ok) {
-    const uint64_t row = F == 6 ? place_row_e2m3_bytes(col) : col;
-    store_row8<F>(p.rq.codes + blk * Fmt<F>::BLOCK_BYTES, r, row);
-    if (r == 0) p.rq.scales[blk] = (uint8_t)bsc;
-  }
-}
-
-// Epilogue warps of the wide form: warp w drains TMEM lanes 32 (w % 4) ..
-// (channels), its half of the 16-column chunks (two position x batch-group
-// pairs each).  fp32 output: the 8 batch entries of a pair are 32 contiguous
-// bytes of HWCN.  TINY as in hc_requant.
-template <int FR, bool TINY>
-__device__ __forceinline__ void hc_epilogue_wide(const HaloConv &p, HcCtl *ctl, uint32_t tmem, int warp, int lane) {
-  const int q = warp & 3;
-  const int half = (warp - HC_EPI_WARP0) >> 2;
-  const float f = (*p.sa) * (*p.sb) * p.pre_mult;
-  float rq_st = 0.0f, rq_stq = 0.0f, rq_inv = 0.0f;
-  if (FR) {
-    rq_st = __fdiv_rn(*p.rq.amax_in, Fmt<FR ? FR : 4>::DENOM);
-    rq_stq = TINY ? rq_st * TINY_MULT : rq_st;
-    rq_inv = __frcp_rn(Fmt<FR ? FR : 4>::EMAX * rq_stq);
-  }
-  const bool inject = p.inject == INJECT_WITHHOLD_ACC_RELEASE && blockIdx.x == 0 && warp == HC_EPI_WARP0;
-  uint32_t amax_acc = 0;
-  int k = 0;
-  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++k) {
-    const TileCoord tc = hc_tile(p, t);
-    const int ch = tc.n0 + q * 32 + lane;
-    const bool ch_ok = ch < p.NC;
-    bool stop = false;
-    for (int sl = 0; sl < p.RT; ++sl) {
-      const int ring = k * p.RT + sl, slot = ring & (p.NS - 1), use = ring >> p.ns_log2;
-      if (!hc_wait(&ctl->acc_full[slot], use & 1, p, ctl)) { stop = true; break; }
-      tc_fence_after();
-      const int ho = tc.h0 + sl;
-      const uint32_t tb = tmem + slot * p.acc_cols + ((uint32_t)(q * 32) << 16);
-      for (int c0 = 16 * half; c0 < 256; c0 += 32) {
-        uint32_t rr[16];
-        tmem_ld16(tb + c0, rr);
-        tmem_wait_ld();
-        float y[16];
-#pragma unroll
-        for (int jj = 0; jj < 16; jj += 2)
-          mul2(__uint_as_float(rr[jj]), __uint_as_float(rr[jj + 1]), f, y[jj], y[jj + 1]);
-#pragma unroll
-        for (int gi = 0; gi < 2; ++gi) {
-          const int grp = c0 / 8 + gi, pp = grp / p.G, j = grp - pp * p.G;
-          const int wo = tc.w0 + pp, ng = tc.g0 + j;
-          const bool valid = ho < p.outH && wo < p.outW;
-          const int64_t pos = (int64_t)ho * p.outW + wo;
-          if (p.out && valid && ch_ok) {
-            float4 *o = reinterpret_cast<float4 *>(p.out + (pos * p.NC + ch) * (int64_t)p.N + ng * 8);
-            o[0] = make_float4(y[8 * gi], y[8 * gi + 1], y[8 * gi + 2], y[8 * gi + 3]);
-            o[1] = make_float4(y[8 * gi + 4], y[8 * gi + 5], y[8 * gi + 6], y[8 * gi + 7]);
-          }
-          if constexpr (FR != 0) {
-            float v[8];
-#pragma unroll
-            for (int n = 0; n < 8; ++n) v[n] = y[8 * gi + n];
-            wide_requant_block<FR, TINY>(p, v, (pos * p.NG + ng) * p.NCG + ch / 8, valid && ch_ok, rq_stq, rq_inv,
-                                         amax_acc);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && !(inject && ring == 0)) mbar_arrive(&ctl->acc_empty[slot]);
-    }
-    if (stop) break;
-  }
-  if (FR) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) amax_acc = max(amax_acc, __shfl_xor_sync(0xFFFFFFFFu, amax_acc, o));
-    if (lane == 0 && amax_acc && p.rq.amax_out_bits) atomicMax(p.rq.amax_out_bits, amax_acc);
-    if (blockIdx.x == 0 && q == 0 && lane == 0 && half == 0) *p.rq.s_t_out = rq_st;
-  }
-}
-
-template <int FR>
-__device__ __noinline__ void hc_epilogue_wide_tiny(const HaloConv &p, HcCtl *ctl, uint32_t tmem, int warp, int lane) {
-  hc_epilogue_wide<FR, true>(p, ctl, tmem, warp, lane);
-}
-
-template <int FR>
-__device__ __forceinline__ void hc_epilogue_wide_entry(const HaloConv &p, HcCtl *ctl, uint32_t tmem, int warp,
-                                                       int lane) {
-  if constexpr (FR != 0) {
-    if (is_tiny_scale(__fdiv_rn(*p.rq.amax_in, Fmt<FR ? FR : 4>::DENOM))) {
-      hc_epilogue_wide_tiny<FR>(p, ctl, tmem, warp, lane);
-      return;
-    }
-  }
-  hc_epilogue_wide<FR, false>(p, ctl, tmem, warp, lane);
-}
-
 // FA: format of the input blocks (X or dY), FB: of the weights, FR: format of
-// the fused requantization of the output (0 = none); WIDE: the wide form
-// (stride 1, N = 256 MMAs, FA = FB, stochastic requantization not included).
-template <int OP, int FA, int FB, int FR, bool WIDE = false>
+// the fused requantization of the output (0 = none).
+template <int OP, int FA, int FB, int FR>
 __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
     halo_conv_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_w,
                      const HaloConv p) {
@@ -896,12 +683,10 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
       }
     }
   } else if (warp == HC_MMA_WARP || warp == HC_MMA_WARP2) {
-    if constexpr (WIDE) hc_issue_wide<OP>(p, ctl, smem, tmem, warp, lane);
-    else if (OP == OP_DGRAD && p.QD) hc_issue<OP, true>(p, ctl, smem, tmem, warp, lane);
+    if (OP == OP_DGRAD && p.QD) hc_issue<OP, true>(p, ctl, smem, tmem, warp, lane);
     else hc_issue<OP, false>(p, ctl, smem, tmem, warp, lane);
   } else if (warp >= HC_EPI_WARP0 && warp < HC_EPI_WARP0 + HC_EPI_WARPS) {
-    if constexpr (WIDE) hc_epilogue_wide_entry<FR>(p, ctl, tmem, warp, lane);
-    else if (OP == OP_DGRAD && p.QD) hc_epilogue_entry<FR, true>(p, ctl, tmem, warp, lane);
+    if (OP == OP_DGRAD && p.QD) hc_epilogue_entry<FR, true>(p, ctl, tmem, warp, lane);
     else hc_epilogue_entry<FR, false>(p, ctl, tmem, warp, lane);
   }
 
@@ -918,15 +703,6 @@ template <int OP, int FA, int FB, int FR>
 cudaError_t hc_launch(const CUtensorMap &a, const CUtensorMap &b, const HaloConv &h, int grid,
                       cudaStream_t st) {
   auto k = halo_conv_kernel<OP, FA, FB, FR>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem);
-  if (e != cudaSuccess) return e;
-  k<<<grid, HC_CONV_THREADS, h.smem, st>>>(a, b, h);
-  return cudaGetLastError();
-}
-
-template <int OP, int F, int FR>
-cudaError_t hc_launch_wide(const CUtensorMap &a, const CUtensorMap &b, const HaloConv &h, int grid, cudaStream_t st) {
-  auto k = halo_conv_kernel<OP, F, F, FR, true>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem);
   if (e != cudaSuccess) return e;
   k<<<grid, HC_CONV_THREADS, h.smem, st>>>(a, b, h);

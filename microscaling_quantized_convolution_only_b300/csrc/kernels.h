@@ -89,8 +89,6 @@ struct HaloConv {
   int PHP;                       // halo positions per phase: RH * WP, padded so that every phase's
                                  // packed box starts 128-byte aligned
   int HKh, HKw;                  // halo extent in taps (Kh, Kw except for QD)
-  int wide;                      // wide form: MMAs of M = 128 output channels x N = 256 positions x batch
-                                 // (stride 1; P G = 32, BN = 128, two 256-column accumulators)
   int QD;                        // stride-2 data gradient: a tile covers R rows x P positions of output
                                  // quads (2 x 2 dX pixels), one accumulator per (row, output phase)
   int NPHS, RT;                  // accumulator phases per row (4 with QD, else 1); accumulators per tile R NPHS
@@ -163,11 +161,6 @@ MQ_HALO_DISPATCH(halo_dispatch_fwd_68)
 MQ_HALO_DISPATCH(halo_dispatch_dgrad_04)
 MQ_HALO_DISPATCH(halo_dispatch_dgrad_68)
 #undef MQ_HALO_DISPATCH
-// the wide form (conv_halo_wide.cu): op OP_FWD / OP_DGRAD, operand format f,
-// requantized-output format fr (0 or f)
-cudaError_t halo_dispatch_wide(int op, int f, int fr, const CUtensorMap &a, const CUtensorMap &b, const HaloConv &h,
-                               int grid, cudaStream_t st);
-
 // Tiled TMA descriptor of a row-major tensor (dims[0] innermost, elements of
 // esize bytes) with box `box`, zero fill outside; `map` is a 64-byte aligned
 // CUtensorMap.  False if the driver entry point or the encode fails.

@@ -149,22 +149,21 @@ def test_requant_tiny_tensor_scale(cuda_device, fmt, L, stat_factor):
         _check(out, ref_np, fmt, role, stat, aout, f"{op} requant tiny T_scale x{stat_factor} {fmt} {L.name()}")
 
 
-WIDE_LAYERS = [
-    Layer(16, 128, 9, 7, 128, 3, 1, 1),    # wide form both ways, ragged positions (7 of 8 / 32-row tiles)
+CHANNEL_LAYERS = [
+    Layer(16, 128, 9, 7, 128, 3, 1, 1),    # 128 channels both ways, ragged positions
     Layer(8, 128, 6, 10, 256, 3, 1, 1),    # two output-channel tiles forward, one batch group
     Layer(32, 256, 5, 5, 128, 1, 1, 0),    # 1x1, four batch groups, more input channels than a tile
 ]
 
 
 @pytest.mark.parametrize("fmt", ["e2m1", "e2m3", "e4m3"])
-@pytest.mark.parametrize("L", WIDE_LAYERS, ids=lambda L: L.name())
+@pytest.mark.parametrize("L", CHANNEL_LAYERS, ids=lambda L: L.name())
 @pytest.mark.parametrize("scale", [1.0, 1e-20], ids=["unit", "tiny-Tscale"])
-def test_wide_requant(cuda_device, fmt, L, scale):
-    """Layers with at least 128 output channels at stride 1 run through the
-    wide form (MMAs of 128 channels x 256 positions x batch, channels on the
-    accumulator lanes): fp32 outputs against the oracle, and the fused
-    requantizations (codes transposed across lanes before they are stored)
-    bit-exact against the oracle quantizer on the unfused fp32 outputs."""
+def test_requant_many_channels(cuda_device, fmt, L, scale):
+    """Stride-1 layers with 128 or more channels (several output-channel
+    tiles, several input-channel chunks): fp32 outputs against the oracle, and
+    the fused requantizations bit-exact against the oracle quantizer on the
+    unfused fp32 outputs, at unit scale and with T_scale below 2^-62."""
     X, W, dY = _inputs(L, 11 + L.N)
     run = LayerRun(L, fmt, "f32", (X * np.float32(scale)).astype(np.float32), W,
                    (dY * np.float32(scale)).astype(np.float32), cuda_device, check_quant=True)
@@ -185,7 +184,7 @@ def test_wide_requant(cuda_device, fmt, L, scale):
             mq.dgrad(L, run.wq, run.gq, y2, rq_out=out, rq_amax_in=ain, rq_amax_out=aout)
         mq.check_device_status()
         assert torch.equal(y2, ref), f"{op}: fp32 output beside the fused epilogue differs from the unfused one"
-        _check(out, ref_np, fmt, role, stat, aout, f"wide {op} requant {fmt} {L.name()} x{scale}")
+        _check(out, ref_np, fmt, role, stat, aout, f"{op} requant {fmt} {L.name()} x{scale}")
 
 
 EMAXV = {"e2m1": 6.0, "e2m3": 7.5, "e4m3": 448.0}
