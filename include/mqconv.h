@@ -247,11 +247,11 @@ mq_status mqconv_device_status(mq_stream stream, int32_t *host_status);
  * frees its tensor memory and returns, so the CUDA context stays usable and
  * the host learns of it from mqconv_device_status().
  *   what  MQ_INJECT_NONE, or MQ_INJECT_WITHHOLD_ACC_RELEASE: in every later
- *         launch of the halo forward / data-gradient kernel, one epilogue
- *         warp of CTA 0 skips its release of the first accumulator slot, so
- *         the MMA issuer's wait for that slot (on a second tile of CTA 0) can
- *         only expire.  Nothing traps or faults; only a plain barrier
- *         arrival is withheld.
+ *         launch of the halo forward / data-gradient kernel, the barrier of
+ *         CTA 0's first accumulator slot expects one release more than its
+ *         epilogue warps give, so the MMA issuer's wait to reuse that slot
+ *         (on a second tile of CTA 0) can only expire.  Nothing traps or
+ *         faults; only a plain barrier arrival is withheld.
  * The setting is process-wide and applies until changed; MQ_ERR_INVALID_ARG
  * for an unknown value.  Call with MQ_INJECT_NONE to restore normal
  * operation.

@@ -557,10 +557,12 @@ __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs,
 #pragma unroll
   for (int j = 0; j < 8; ++j) q[j] = tie_quotient(ql[j], qh[j], v[j], bs, s_t);
   const uint64_t row = F == 4 ? (uint64_t)cvt_row_e2m1(q) : F == 8 ? cvt_row_e4m3(q) : cvt_row_e2m3(q);
-  if (F != 6 || !PLACE) return row;
+  if constexpr (F == 6 && PLACE) {
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) lo[jj] = (uint32_t)((row >> (SH * jj)) & M);
-  return place_row<F>(lo);
+    for (int jj = 0; jj < 4; ++jj) lo[jj] = (uint32_t)((row >> (SH * jj)) & M);
+    return place_row<F>(lo);
+  }
+  return row;
 }
 
 // E2M3 codes in byte containers (element j in byte j) -> the packed 6-bit row

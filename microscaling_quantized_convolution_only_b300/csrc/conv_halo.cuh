@@ -415,8 +415,6 @@ __device__ __forceinline__ void hc_epilogue(const HaloConv &p, HcCtl *ctl, uint3
     rq_stq = rq_tiny ? rq_st * TINY_MULT : rq_st;
     rq_inv = __frcp_rn(Fmt<FR ? FR : 4>::EMAX * rq_stq);
   }
-  // test support: this warp of CTA 0 never releases the first accumulator slot
-  const bool inject = p.inject == INJECT_WITHHOLD_ACC_RELEASE && blockIdx.x == 0 && warp == HC_EPI_WARP0;
   uint32_t amax_acc = 0;
   int k = 0;
   for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++k) {
@@ -456,7 +454,7 @@ __device__ __forceinline__ void hc_epilogue(const HaloConv &p, HcCtl *ctl, uint3
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && !(inject && ring == 0)) mbar_arrive(&ctl->acc_empty[slot]);
+      if (lane == 0) mbar_arrive(&ctl->acc_empty[slot]);
     }
     if (stop) break;
   }
@@ -513,9 +511,14 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
       mbar_init(&ctl->sfull[s], 64);
       mbar_init(&ctl->sempty[s], HC_DEC_WARPS);
     }
+    // test support (INJECT_WITHHOLD_ACC_RELEASE): CTA 0's first accumulator
+    // slot expects one release more than its epilogue warps give, so the
+    // issuer's wait to reuse it can only expire; set here, the injection
+    // costs the loops nothing
+    const int extra = p.inject == INJECT_WITHHOLD_ACC_RELEASE && blockIdx.x == 0 ? 1 : 0;
     for (int s = 0; s < p.NS; ++s) {
       mbar_init(&ctl->acc_full[s], 1);
-      mbar_init(&ctl->acc_empty[s], HC_EPI_WARPS);
+      mbar_init(&ctl->acc_empty[s], HC_EPI_WARPS + (s == 0 ? extra : 0));
     }
     mbar_init(&ctl->done, p.RT >= 2 ? 2 : 1);
     ctl->abort_flag = 0;

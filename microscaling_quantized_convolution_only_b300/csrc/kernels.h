@@ -68,10 +68,11 @@ struct ConvParams {
   int inject;                      // fault injection for the failure-detection tests (0: none)
 };
 
-// Fault injections (test support): INJECT_WITHHOLD_ACC_RELEASE makes one
-// epilogue warp of CTA 0 of the halo forward / data-gradient kernel skip its
-// release of the first accumulator slot, so the MMA issuer's bounded wait for
-// that slot expires (no copy or MMA is left waiting on it).
+// Fault injections (test support): INJECT_WITHHOLD_ACC_RELEASE makes the
+// first accumulator slot of CTA 0 of the halo forward / data-gradient kernel
+// expect one release more than its epilogue warps give, so the MMA issuer's
+// bounded wait to reuse that slot expires (no copy or MMA is left waiting on
+// it).
 constexpr int INJECT_WITHHOLD_ACC_RELEASE = 1;
 
 // Forward / data-gradient convolution (stride 1 or 2) with per-tile halo

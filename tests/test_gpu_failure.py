@@ -1,9 +1,9 @@
 """Failure detection on the GPU without a GPU fault.
 
 Every wait inside the convolution kernels is bounded.  The test withholds one
-plain barrier arrival (an epilogue warp of CTA 0 skips its release of the
-first accumulator slot: no copy and no MMA is waiting on it), with a short
-wait limit, and checks that
+plain barrier arrival (the barrier of CTA 0's first accumulator slot expects
+one release more than its epilogue warps give: no copy and no MMA is waiting
+on it), with the kernels' 2 s wait limit, and checks that
 
   * the call returns and the device status word reports MQ_ERR_TIMEOUT,
   * nothing else is reported and the status word is cleared by the read,
