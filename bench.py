@@ -815,15 +815,22 @@ def oracle_sample_step(wl, budget_s, state):
 # bound (output lines still in L2 when a launch ends are not counted).  Valid
 # only while the kernel sources are the captured ones.
 TRAFFIC = {
+    # one step's four launches (three with the fused requantization of dX,
+    # whose 13 MB packed output is still in L2 when the launch ends, and the
+    # plain one of layer 0 writing 45 MB of fp32 dX)
     ("stack4-56x56-c128-nvfp4", "conv_dgrad"): {
-        "bytes_per_launch": (13.43997e6 + 13.44e6 + 13.440256e6 + 13.432832e6 + 48.087552e6) / 4, "batch": 64,
-        "sources_sha1": "5df95795b2ec964a749f526e18051c440709cd37"},
-    # one launch (the four are alike); its small write term (the split-K
-    # partials, 0.17 MB) does not grow with the batch but is scaled with it
+        "bytes_per_launch": (13.433344e6 + 13.434624e6 + 13.433344e6 + (13.423616e6 + 45.231872e6)) / 4,
+        "batch": 64, "sources_sha1": "6262f6cf422a1569072b014770058a9ef2c309e2"},
+    ("stack4-56x56-c128-nvfp4", "conv_fwd"): {
+        "bytes_per_launch": (13.430784e6 + 13.430528e6 + 13.430528e6 + (13.424128e6 + 45.320192e6)) / 4,
+        "batch": 64, "sources_sha1": "6262f6cf422a1569072b014770058a9ef2c309e2"},
+    # the four launches alike; the small write term (split-K partials,
+    # 0.07-0.08 MB) does not grow with the batch but is scaled with it
     ("stack4-56x56-c128-nvfp4", "conv_wgrad"): {
-        "bytes_per_launch": 26.64192e6 + 0.166144e6, "batch": 64,
-        "sources_sha1": "5df95795b2ec964a749f526e18051c440709cd37"},
+        "bytes_per_launch": (26.625792e6 + 26.629632e6 + 26.654208e6 + 26.634496e6) / 4 + 0.077e6, "batch": 64,
+        "sources_sha1": "6262f6cf422a1569072b014770058a9ef2c309e2"},
 }
+
 
 def kernel_sources_sha1(root=None):
     """SHA-1 of the library sources with comments and blank space removed
