@@ -454,7 +454,8 @@ __device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int s = it % QT_STAGES;
     if (!qt_wait(&ctl->full[s], (it / QT_STAGES) & 1, ctl, p.status)) break;
-    const int hwt = t % hw_tiles, rest = t / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
+    const int tr = ntiles - 1 - t;                       // tiles in reverse memory order (see the producer)
+    const int hwt = tr % hw_tiles, rest = tr / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
     const int64_t hw0 = (int64_t)hwt * HWT;
     const int gb0 = gbt * GBT;
     const int ngb = min(GBT, GB - gb0);
@@ -545,7 +546,10 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
       for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
         const int s = it % QT_STAGES;
         if (!qt_wait(&ctl->empty[s], ((it / QT_STAGES) & 1) ^ 1, ctl, p.status)) break;
-        const int hwt = t % hw_tiles, rest = t / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
+        // last tile first: after the exact-statistic pass, which reads the
+        // tensor front to back, its tail is the part still in L2
+        const int tr = ntiles - 1 - t;
+        const int hwt = tr % hw_tiles, rest = tr / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
         mbar_expect_tx(&ctl->full[s], STAGE);
         tma_load_3d(ring + s * STAGE, &tm, &ctl->full[s], hwt * HWT, gbt * GBT * 8, ga * 8);
       }
