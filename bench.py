@@ -813,33 +813,41 @@ def oracle_sample_step(wl, budget_s, state):
 # capture of the same workload at a smaller batch (profiles/, command there),
 # scaled by the batch.  The writes of the captured launches are a lower
 # bound (output lines still in L2 when a launch ends are not counted).  Valid
-# only while the kernel sources are the captured ones.
+# only while the conv kernels' sources (CONV_SOURCES) are the captured ones.
 TRAFFIC = {
     # one step's four launches (three with the fused requantization of dX,
     # whose 13 MB packed output is still in L2 when the launch ends, and the
     # plain one of layer 0 writing 45 MB of fp32 dX)
     ("stack4-56x56-c128-nvfp4", "conv_dgrad"): {
         "bytes_per_launch": (13.433344e6 + 13.434624e6 + 13.433344e6 + (13.423616e6 + 45.231872e6)) / 4,
-        "batch": 64, "sources_sha1": "6262f6cf422a1569072b014770058a9ef2c309e2"},
+        "batch": 64, "sources_sha1": "ca1094d1a38861cc47d2f04dcc10d53674eafb93"},
     ("stack4-56x56-c128-nvfp4", "conv_fwd"): {
         "bytes_per_launch": (13.430784e6 + 13.430528e6 + 13.430528e6 + (13.424128e6 + 45.320192e6)) / 4,
-        "batch": 64, "sources_sha1": "6262f6cf422a1569072b014770058a9ef2c309e2"},
+        "batch": 64, "sources_sha1": "ca1094d1a38861cc47d2f04dcc10d53674eafb93"},
     # the four launches alike; the small write term (split-K partials,
     # 0.07-0.08 MB) does not grow with the batch but is scaled with it
     ("stack4-56x56-c128-nvfp4", "conv_wgrad"): {
         "bytes_per_launch": (26.625792e6 + 26.629632e6 + 26.654208e6 + 26.634496e6) / 4 + 0.077e6, "batch": 64,
-        "sources_sha1": "6262f6cf422a1569072b014770058a9ef2c309e2"},
+        "sources_sha1": "ca1094d1a38861cc47d2f04dcc10d53674eafb93"},
 }
 
 
-def kernel_sources_sha1(root=None):
-    """SHA-1 of the library sources with comments and blank space removed
-    (editing a comment does not invalidate a capture, editing code does)."""
+# the sources the conv kernels are built from (device code, the parameter
+# structs, the planners and the launch set-up)
+CONV_SOURCES = ["api.cu", "common.cuh", "kernels.h", "conv_halo.cuh", "conv_halo.cu", "conv_halo_fwd_a.cu",
+                "conv_halo_fwd_b.cu", "conv_halo_dgrad_a.cu", "conv_halo_dgrad_b.cu"]
+
+
+def kernel_sources_sha1(root=None, names=None):
+    """SHA-1 of the library sources (all of csrc/, or the files `names`) and
+    mqconv.h, with comments and blank space removed (editing a comment does
+    not invalidate a capture, editing code does)."""
     import glob
     import hashlib
     import re
     here = root or os.path.dirname(os.path.abspath(__file__))
-    files = sorted(glob.glob(os.path.join(here, "microscaling_quantized_convolution_only_b300", "csrc", "*")))
+    csrc = os.path.join(here, "microscaling_quantized_convolution_only_b300", "csrc")
+    files = sorted(os.path.join(csrc, n) for n in names) if names else sorted(glob.glob(os.path.join(csrc, "*")))
     files.append(os.path.join(here, "include", "mqconv.h"))
     h = hashlib.sha1()
     for f in files:
@@ -855,7 +863,7 @@ def kernel_sources_sha1(root=None):
 
 def captured_traffic(workload, kernel, batch):
     t = TRAFFIC.get((workload, kernel))
-    if t is None or t["sources_sha1"] != kernel_sources_sha1():
+    if t is None or t["sources_sha1"] != kernel_sources_sha1(names=CONV_SOURCES):
         return None
     return t["bytes_per_launch"] * batch / t["batch"]
 

@@ -39,8 +39,23 @@ def test_traffic_scales_with_batch_and_needs_matching_sources():
     b = _bench()
     key = ("stack4-56x56-c128-nvfp4", "conv_dgrad")
     t = b.TRAFFIC[key]
-    if t["sources_sha1"] == b.kernel_sources_sha1():
+    if t["sources_sha1"] == b.kernel_sources_sha1(names=b.CONV_SOURCES):
         assert b.captured_traffic(*key, t["batch"] * 4) == t["bytes_per_launch"] * 4
     else:
         assert b.captured_traffic(*key, t["batch"]) is None
     assert b.captured_traffic("no-such-workload", "conv_dgrad", 64) is None
+
+
+def test_conv_key_covers_the_conv_sources_only(tmp_path):
+    """The conv traffic key follows the conv kernels' sources: an edit to
+    the quantizer leaves it, an edit to a conv source changes it."""
+    b = _bench()
+    ref = b.kernel_sources_sha1(names=b.CONV_SOURCES)
+    f = _copy_sources(str(tmp_path))
+    csrc = os.path.dirname(f)
+    q = os.path.join(csrc, "quantize.cu")
+    open(q, "w").write(open(q).read().replace("constexpr int QT_STAGES = 2;", "constexpr int QT_STAGES = 3;"))
+    assert b.kernel_sources_sha1(str(tmp_path), names=b.CONV_SOURCES) == ref
+    assert b.kernel_sources_sha1(str(tmp_path)) != b.kernel_sources_sha1()
+    open(f, "w").write(open(f).read().replace("constexpr int DSTAGES = 2;", "constexpr int DSTAGES = 3;"))
+    assert b.kernel_sources_sha1(str(tmp_path), names=b.CONV_SOURCES) != ref
