@@ -38,6 +38,13 @@ template <> struct Fmt<8> {   // E4M3 element (8-bit variant)
   static constexpr uint32_t SBIT = 0x80, MAG = 0x7F;
 };
 
+// max(a, b) that returns NaN when either is NaN (max.NaN.f32)
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
 // (a0 * b, a1 * b), each rounded to nearest even: one packed f32x2 multiply
 __device__ __forceinline__ void mul2(float a0, float a1, float b, float &d0, float &d1) {
   uint64_t a, bb, d;

@@ -160,23 +160,38 @@ __device__ __forceinline__ TileCoord hc_tile(const HaloConv &p, int t) {
 template <int F, int NBK, bool TINY>
 __device__ __forceinline__ void hc_requant(const HaloConv &p, const float *y, int64_t blk_pos_ng, int n_in, int co0,
                                            bool row_ok, float s_t, float inv_den, uint32_t &amax_acc) {
-  uint32_t m[NBK];
+  static_assert(NBK == 2 || NBK == 4, "blocks side by side per chunk");
+  // block amax of this lane's row: the fp32 max of |y|, a NaN (only from an
+  // overflowed scale product) propagating, so that its bit pattern orders
+  // above every finite value and Inf as the |y| bit patterns do
+  float m[NBK];
 #pragma unroll
   for (int h = 0; h < NBK; ++h) {
-    uint32_t mm = 0;
+    float mm = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) mm = max(mm, __float_as_uint(y[8 * h + j]) & 0x7FFFFFFFu);
-    m[h] = (row_ok && co0 + 8 * h < p.NC) ? mm : 0u;
+    for (int j = 0; j < 8; ++j) mm = fmax_nan(mm, fabsf(y[8 * h + j]));
+    m[h] = (row_ok && co0 + 8 * h < p.NC) ? mm : 0.0f;
   }
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1)
-#pragma unroll
-    for (int h = 0; h < NBK; ++h) m[h] = max(m[h], __shfl_xor_sync(0xFFFFFFFFu, m[h], o));
-  // this lane's block: hb = n_in % NBK
-  const int hb = n_in & (NBK - 1);
-  uint32_t mine = m[0];
-#pragma unroll
-  for (int h = 1; h < NBK; ++h) mine = hb == h ? m[h] : mine;
+  // reduce-scatter over the 8 lanes (8 rows) of each block: lane j ends with
+  // the amax of block j mod NBK, the block whose scale it computes
+  const int lj = threadIdx.x & 7;
+  float k;
+  if constexpr (NBK == 4) {
+    const bool b0 = lj & 1, b1 = lj & 2;
+    float a = b0 ? m[1] : m[0], c = b0 ? m[3] : m[2];
+    const float a_out = b0 ? m[0] : m[1], c_out = b0 ? m[2] : m[3];
+    a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a_out, 1));
+    c = fmax_nan(c, __shfl_xor_sync(0xFFFFFFFFu, c_out, 1));
+    k = b1 ? c : a;
+    k = fmax_nan(k, __shfl_xor_sync(0xFFFFFFFFu, b1 ? a : c, 2));
+  } else {
+    const bool b0 = lj & 1;
+    k = fmax_nan(b0 ? m[1] : m[0], __shfl_xor_sync(0xFFFFFFFFu, b0 ? m[0] : m[1], 1));
+    k = fmax_nan(k, __shfl_xor_sync(0xFFFFFFFFu, k, 2));
+  }
+  k = fmax_nan(k, __shfl_xor_sync(0xFFFFFFFFu, k, 4));
+  const uint32_t mine = __float_as_uint(k);
+  amax_acc = max(amax_acc, mine);
   const float amax_mine = TINY ? up64(__uint_as_float(mine)) : __uint_as_float(mine);
   const uint32_t bsc_mine = block_scale_code_r<F>(amax_mine, s_t, inv_den);
   float lo_mine, hi_mine;
@@ -184,7 +199,6 @@ __device__ __forceinline__ void hc_requant(const HaloConv &p, const float *y, in
   const int src0 = (threadIdx.x & 31) & ~7;
 #pragma unroll
   for (int h = 0; h < NBK; ++h) {
-    amax_acc = max(amax_acc, m[h]);
     const int co = co0 + 8 * h;
     const uint32_t bsc = __shfl_sync(0xFFFFFFFFu, bsc_mine, src0 + h);
     const float inv_lo = __shfl_sync(0xFFFFFFFFu, lo_mine, src0 + h);
