@@ -819,17 +819,18 @@ TRAFFIC = {
     # whose 13 MB packed output is still in L2 when the launch ends, and the
     # plain one of layer 0 writing 45 MB of fp32 dX)
     ("stack4-56x56-c128-nvfp4", "conv_dgrad"): {
-        "bytes_per_launch": (13.433344e6 + 13.434624e6 + 13.433344e6 + (13.423616e6 + 45.231872e6)) / 4,
-        "batch": 64, "sources_sha1": "ca1094d1a38861cc47d2f04dcc10d53674eafb93"},
+        "bytes_per_launch": ((13.432832e6 + 0.002048e6) + 13.432832e6 + 13.432832e6 + (13.426688e6 + 45.298688e6)) / 4,
+        "batch": 64, "sources_sha1": "1120dfb761e44fe722d3c632f1d4ee60682ce981"},
     ("stack4-56x56-c128-nvfp4", "conv_fwd"): {
-        "bytes_per_launch": (13.430784e6 + 13.430528e6 + 13.430528e6 + (13.424128e6 + 45.320192e6)) / 4,
-        "batch": 64, "sources_sha1": "ca1094d1a38861cc47d2f04dcc10d53674eafb93"},
+        "bytes_per_launch": (13.43616e6 + 13.430272e6 + 13.453824e6 + (13.424896e6 + 45.202944e6)) / 4,
+        "batch": 64, "sources_sha1": "1120dfb761e44fe722d3c632f1d4ee60682ce981"},
     # the four launches alike; the small write term (split-K partials,
     # 0.07-0.08 MB) does not grow with the batch but is scaled with it
     ("stack4-56x56-c128-nvfp4", "conv_wgrad"): {
-        "bytes_per_launch": (26.625792e6 + 26.629632e6 + 26.654208e6 + 26.634496e6) / 4 + 0.077e6, "batch": 64,
-        "sources_sha1": "ca1094d1a38861cc47d2f04dcc10d53674eafb93"},
+        "bytes_per_launch": (26.631168e6 + 26.629120e6 + 26.624256e6 + 26.648320e6) / 4 + 0.078e6, "batch": 64,
+        "sources_sha1": "1120dfb761e44fe722d3c632f1d4ee60682ce981"},
 }
+
 
 
 # the sources the conv kernels are built from (device code, the parameter
