@@ -438,9 +438,11 @@ __device__ __forceinline__ void copy_runs_rt(int gran, uint8_t *dst, int nruns, 
 namespace mq {
 
 // Codes of eight fp32 values (one block row) for block scale value bs and
-// T_scale s_t: exact RN of the real quotient x / (bs * s_t) with the bracket
-// and fma-sign tie test of resolve_tie.  Returns the packed row: element j at
-// bits 4j (E2M1), 6j (E2M3) or 8j (E4M3).
+// T_scale s_t (encode_row8 / encode_row8_b below): exact RN of the real
+// quotient x / (bs * s_t), from the bracket and the fma-sign test of
+// tie_quotient.  Returns the packed row: element j at bits 4j (E2M1), 6j
+// (E2M3) or 8j (E4M3).
+//
 // Bracket multipliers of the quotient x / (bs * s_t) (0 when bs is 0).  The
 // reciprocal is the hardware approximation (relative error below 2^-22);
 // with the product bs * s_t and the three later roundings (each 2^-24) the

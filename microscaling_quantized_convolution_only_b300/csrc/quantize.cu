@@ -6,14 +6,16 @@
 // (C_out, C_in) for weights and (N, C_out) for output gradients and are stored
 // channel-batch-first (§IV-A): block order [H][W][N/8][C/8], element i = 8n + c.
 //
-// One thread owns one block: it loads the block's 64 inputs straight from
-// global memory (for NCHW inputs consecutive lanes own consecutive spatial
-// positions, so each of the 64 loads is a coalesced warp-wide row segment; for
-// HWCN inputs each lane reads eight 8-element rows), reduces the block amax in
-// registers, derives the E4M3 block scale exactly, converts the codes with the
-// hardware RN conversions on a bracket [q(1-eps), q(1+eps)] of the quotient
-// and resolves the rare bracket that straddles a rounding midpoint with an
-// exact fma-sign test.  Codes and the scale byte are written once.
+// One thread owns one block: it gathers the block's 64 inputs (for NCHW
+// inputs consecutive lanes own consecutive spatial positions, so each of the
+// 64 loads is a coalesced warp-wide row segment, from a TMA-filled shared
+// stage or straight from global memory; for HWCN inputs each lane reads eight
+// 8-element rows), reduces the block amax in registers, derives the E4M3
+// block scale exactly, converts the codes with the hardware RN conversions on
+// a bracket [q(1-eps), q(1+eps)] of the quotient and settles a row whose
+// bracket straddles a rounding midpoint with an exact fma-sign test
+// (tie_quotient).  Codes and the scale byte are written once, straight to
+// their place in global memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
