@@ -648,6 +648,9 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
         uint8_t *dec = smem + p.off_dec + ds * p.dec_stage;
         // input halo: block (hr, wc, j, kc) at index ((hr * WP + wc) * G + j) * CGC + kc
         const int nh = p.nh_blocks * 8;
+        // unrolled: two (halo) and four (weight) rows' shared loads in flight
+        // per thread ahead of their conversions (measured: fwd 3%, dgrad 4%)
+#pragma unroll 2
         for (int i = tid; i < nh; i += HC_DEC_THREADS) {
           const int blk = i >> 3, r = i & 7;
           const int hp = blk / CGC, kc = blk - hp * CGC;
@@ -667,6 +670,7 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
         const int tap_span = CGC * p.NB, step_blk = HC_DEC_THREADS / 8;
         const int q_step = step_blk / tap_span, r_step = step_blk - q_step * tap_span;
         int d_tap = (tid >> 3) / tap_span, d_rem = (tid >> 3) - d_tap * tap_span;
+#pragma unroll 4
         for (int i = tid; i < nbr; i += HC_DEC_THREADS) {
           const int blk = i >> 3, r = i & 7;
           int si;
