@@ -819,17 +819,18 @@ TRAFFIC = {
     # whose 13 MB packed output is still in L2 when the launch ends, and the
     # plain one of layer 0 writing 45 MB of fp32 dX)
     ("stack4-56x56-c128-nvfp4", "conv_dgrad"): {
-        "bytes_per_launch": ((13.432832e6 + 0.002048e6) + 13.432832e6 + 13.432832e6 + (13.426688e6 + 45.298688e6)) / 4,
-        "batch": 64, "sources_sha1": "1120dfb761e44fe722d3c632f1d4ee60682ce981"},
+        "bytes_per_launch": (13.437696e6 + 13.440256e6 + 13.444096e6 + (13.457152e6 + 45.473024e6)) / 4,
+        "batch": 64, "sources_sha1": "e9e621ec1c59f7f504b02308dbd58f2e0499c28a"},
     ("stack4-56x56-c128-nvfp4", "conv_fwd"): {
-        "bytes_per_launch": (13.43616e6 + 13.430272e6 + 13.453824e6 + (13.424896e6 + 45.202944e6)) / 4,
-        "batch": 64, "sources_sha1": "1120dfb761e44fe722d3c632f1d4ee60682ce981"},
+        "bytes_per_launch": (13.435392e6 + 13.435392e6 + 13.44896e6 + (13.433856e6 + 45.340928e6)) / 4,
+        "batch": 64, "sources_sha1": "e9e621ec1c59f7f504b02308dbd58f2e0499c28a"},
     # the four launches alike; the small write term (split-K partials,
     # 0.07-0.08 MB) does not grow with the batch but is scaled with it
     ("stack4-56x56-c128-nvfp4", "conv_wgrad"): {
-        "bytes_per_launch": (26.631168e6 + 26.629120e6 + 26.624256e6 + 26.648320e6) / 4 + 0.078e6, "batch": 64,
-        "sources_sha1": "1120dfb761e44fe722d3c632f1d4ee60682ce981"},
+        "bytes_per_launch": (26.627072e6 + 26.626816e6 + 26.621184e6 + 26.6304e6) / 4 + 0.075e6, "batch": 64,
+        "sources_sha1": "e9e621ec1c59f7f504b02308dbd58f2e0499c28a"},
 }
+
 
 
 

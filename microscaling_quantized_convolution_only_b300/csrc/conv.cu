@@ -555,10 +555,7 @@ __global__ void wgrad_reduce_kernel(const ConvParams p, float *__restrict__ dw) 
   const int KK = p.Kh * p.Kw;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     float s = 0.0f;
-    // unrolled so that eight loads are in flight ahead of the adds, which
-    // still run in split order
-#pragma unroll 8
-    for (int k = 0; k < p.k_splits; ++k) s += __ldg(p.out + (int64_t)k * total + i);
+    for (int k = 0; k < p.k_splits; ++k) s += p.out[(int64_t)k * total + i];
     const int64_t co = i / p.ncols;
     const int col = (int)(i - co * p.ncols);
     const int tap = col / p.Cin, ci = col - tap * p.Cin;
