@@ -412,10 +412,11 @@ def time_quantizer(mq, torch, src, layout, role, fmt, dims, flush, reps=8):
     """Median CUDA-event time (ms) of quantizing `src` in single-pass mode
     (statistic supplied: the tensor's own amax) and in exact two-pass mode,
     L2 flushed before each rep; returns {mode: ms}.  Each mode is captured
-    once as a CUDA graph and timed by its replay, so that the host's launch
-    path (argument marshalling, tensor-map encoding) cannot leave the GPU
-    idle between the events: an eager launch that reaches the GPU after the
-    flush has drained counts its host delay as kernel time."""
+    once as a CUDA graph holding the flush, the start event, the quantizer
+    call and the end event, and timed by replaying it: nothing the host does
+    (argument marshalling, tensor-map encoding, a late launch) can fall
+    between the events, as it can for an eager launch that reaches the GPU
+    after the flush has drained."""
     dev = src.device
     p = mq.Packed(fmt, role, dims, device=dev)
     stat = torch.zeros(1, device=dev)
@@ -424,19 +425,20 @@ def time_quantizer(mq, torch, src, layout, role, fmt, dims, flush, reps=8):
     torch.cuda.synchronize()
     out = {}
     for mode in ("single_pass", "two_pass"):
+        e0 = torch.cuda.Event(enable_timing=True, external=True)
+        e1 = torch.cuda.Event(enable_timing=True, external=True)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
+            flush.zero_()
+            e0.record()
             if mode == "single_pass":
                 mq.quantize_cbf(src, layout, p, amax_in=stat, amax_out=aout)
             else:
                 mq.quantize_cbf(src, layout, p, amax_out=aout)
+            e1.record()
         ts = []
         for i in range(reps + 2):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
             g.replay()
-            e1.record()
             torch.cuda.synchronize()
             if i >= 2:
                 ts.append(e0.elapsed_time(e1))
@@ -494,16 +496,19 @@ def extra_workload(name, device, peaks, steps, flush):
     for _ in range(3):
         step.run()
     torch.cuda.synchronize()
+    # flush, start event, the step (CUDA events around each op group), end
+    # event: one graph, so no host work falls between the events
     graph, tm = torch.cuda.CUDAGraph(), OpTimer()
+    e0 = torch.cuda.Event(enable_timing=True, external=True)
+    e1 = torch.cuda.Event(enable_timing=True, external=True)
     with torch.cuda.graph(graph):
+        flush.zero_()
+        e0.record()
         step.run(tm)
+        e1.record()
     per_op, per_layer, step_ms = {}, {}, []
     for _ in range(steps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
         graph.replay()
-        e1.record()
         torch.cuda.synchronize()
         step_ms.append(e0.elapsed_time(e1))
         for g, v in tm.times().items():
@@ -564,7 +569,7 @@ def run_gpu(args):
     # ---- the step as CUDA graphs: a plain one (timed as a whole) and one with
     #      CUDA events around each op group (per-op times without host gaps)
     graph = None
-    timed_graph, tm_graph = None, None
+    timed_graph, tm_graph, whole_graph = None, None, None
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
@@ -572,8 +577,19 @@ def run_gpu(args):
         timed_graph, tm_graph = torch.cuda.CUDAGraph(), OpTimer()
         with torch.cuda.graph(timed_graph):
             step.run(tm_graph)
+        # the timed step as one graph: L2 flush, start event, the step, end
+        # event (no host work can fall between the events)
+        s0g = torch.cuda.Event(enable_timing=True, external=True)
+        s1g = torch.cuda.Event(enable_timing=True, external=True)
+        whole_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(whole_graph):
+            flush.zero_()
+            s0g.record()
+            step.run()
+            s1g.record()
         graph.replay()
         timed_graph.replay()
+        whole_graph.replay()
         torch.cuda.synchronize()
 
     def one_step():
@@ -606,6 +622,11 @@ def run_gpu(args):
     # ---- device-timed steps (inputs resident in HBM)
     step_ms = []
     for _ in range(args.steps):
+        if whole_graph is not None:
+            whole_graph.replay()
+            torch.cuda.synchronize()
+            step_ms.append(s0g.elapsed_time(s1g))
+            continue
         flush.zero_()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record()
@@ -743,8 +764,9 @@ def run_gpu(args):
                    "input_dtype": wl.dtype, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed (256 MB write) before every timed step; inputs also exceed L2",
                    "execution": "eager launches" if graph is None else
-                                "one CUDA graph per step; per-op times from a copy of the graph with CUDA events "
-                                "around each op group",
+                                "one CUDA graph per step holding the L2 flush, the start event, the step and the "
+                                "end event; per-op times from a copy of the step's graph with CUDA events around "
+                                "each op group",
                    "e2e_inputs": "double-buffered: each step copies the next step's inputs from pinned host "
                                  "memory on a copy stream while it computes" if hasattr(step, "new_staging") else
                                  "copied from pinned host memory at the start of each step",
