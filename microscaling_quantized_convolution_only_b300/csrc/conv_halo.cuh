@@ -128,8 +128,12 @@ __device__ __forceinline__ bool hc_drain(uint64_t *bar, uint32_t parity, uint32_
 template <int F> __device__ __forceinline__ uint2 lds_row(const uint8_t *blk, int r) {
   if (F == 4) return make_uint2(*reinterpret_cast<const uint32_t *>(blk + 4 * r), 0u);
   if (F == 8) return *reinterpret_cast<const uint2 *>(blk + 8 * r);
-  const uint16_t *h = reinterpret_cast<const uint16_t *>(blk + 6 * r);
-  return make_uint2((uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2]);
+  // E2M3: row r is bytes 6r .. 6r+5 of the (16-byte aligned) 48-byte block;
+  // two aligned 32-bit loads from byte 6r rounded down to a multiple of 4
+  // (at most byte 47 read) and a funnel shift by 0 or 16 bits
+  const uint32_t *w = reinterpret_cast<const uint32_t *>(blk + ((6 * r) & ~3));
+  const uint32_t w0 = w[0], w1 = w[1], sh = (uint32_t)((6 * r) & 2) * 8u;
+  return make_uint2(__funnelshift_r(w0, w1, sh), (w1 >> sh) & 0xFFFFu);
 }
 
 struct TileCoord {
