@@ -490,19 +490,20 @@ __device__ __forceinline__ float tie_quotient(float ql, float qh, float x, float
   return r > 0.0f ? qh : (r < 0.0f ? ql : m);
 }
 
-// four code pairs (containers as cvt2 returns them) -> one packed row
-template <int F> __device__ __forceinline__ uint64_t place_row(const uint32_t (&pr)[4]) {
-  uint64_t bits = 0;
-#pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    if (F == 4) bits |= (uint64_t)pr[jj] << (8 * jj);                                  // two nibbles
-    else if (F == 8) bits |= (uint64_t)pr[jj] << (16 * jj);                            // two bytes
-    else bits |= (uint64_t)((pr[jj] & 0x3Fu) | ((pr[jj] >> 8) << 6)) << (12 * jj);     // two 6-bit codes
-  }
-  return bits;
+// E2M3 codes in byte containers (element j in byte j, the code in its low
+// 6 bits) -> the packed 6-bit row (element j at bits 6j): four codes of a
+// 32-bit half are compacted in two shift-and-mask steps (pairs into 12-bit
+// fields, then the two fields into 24 bits)
+__device__ __forceinline__ uint32_t compact_e2m3x4(uint32_t x) {
+  x = (x & 0x003F003Fu) | ((x >> 2) & 0x0FC00FC0u);
+  return (x & 0x00000FFFu) | ((x >> 4) & 0x00FFF000u);
+}
+__device__ __forceinline__ uint64_t pack_e2m3_row(uint64_t b) {
+  return (uint64_t)compact_e2m3x4((uint32_t)b) | ((uint64_t)compact_e2m3x4((uint32_t)(b >> 32)) << 24);
 }
 
-// eight quotients -> one packed row (containers as place_row); E2M1: four
+// eight quotients -> one row of codes in containers (E2M1: nibbles, E2M3 /
+// E4M3: bytes, element j in container j); E2M1: four
 // byte pairs packed in one step, E4M3: four 16-bit pairs
 __device__ __forceinline__ uint32_t cvt_row_e2m1(const float (&q)[8]) {
   uint32_t r;
@@ -552,33 +553,18 @@ __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs,
     mul2(v[2 * jj], v[2 * jj + 1], inv_lo, ql[2 * jj], ql[2 * jj + 1]);
     mul2(v[2 * jj], v[2 * jj + 1], inv_hi, qh[2 * jj], qh[2 * jj + 1]);
   }
-  // whole rows at once (pairs in byte / 16-bit containers); the pairs are
-  // unpacked only for the E2M3 bit packing or when the ends differ
+  // whole rows at once (codes in nibble / byte containers), compared once
   const uint64_t row_lo = F == 4 ? (uint64_t)cvt_row_e2m1(ql) : F == 8 ? cvt_row_e4m3(ql) : cvt_row_e2m3(ql);
   const uint64_t row_hi = F == 4 ? (uint64_t)cvt_row_e2m1(qh) : F == 8 ? cvt_row_e4m3(qh) : cvt_row_e2m3(qh);
-  constexpr int SH = F == 4 ? 8 : 16;
-  constexpr uint64_t M = F == 4 ? 0xFFu : 0xFFFFu;
-  uint32_t lo[4];
+  uint64_t row = row_lo;
+  if (row_lo != row_hi) {   // some element near a midpoint: convert the row again from the picked quotients
+    float q[8];
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) lo[jj] = (uint32_t)((row_lo >> (SH * jj)) & M);
-  if (row_lo == row_hi) return F == 6 && PLACE ? place_row<F>(lo) : row_lo;   // common case: no element near a midpoint
-  float q[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) q[j] = tie_quotient(ql[j], qh[j], v[j], bs, s_t);
-  const uint64_t row = F == 4 ? (uint64_t)cvt_row_e2m1(q) : F == 8 ? cvt_row_e4m3(q) : cvt_row_e2m3(q);
-  if constexpr (F == 6 && PLACE) {
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) lo[jj] = (uint32_t)((row >> (SH * jj)) & M);
-    return place_row<F>(lo);
+    for (int j = 0; j < 8; ++j) q[j] = tie_quotient(ql[j], qh[j], v[j], bs, s_t);
+    row = F == 4 ? (uint64_t)cvt_row_e2m1(q) : F == 8 ? cvt_row_e4m3(q) : cvt_row_e2m3(q);
   }
+  if constexpr (F == 6 && PLACE) return pack_e2m3_row(row);
   return row;
-}
-
-// E2M3 codes in byte containers (element j in byte j) -> the packed 6-bit row
-__device__ __forceinline__ uint64_t place_row_e2m3_bytes(uint64_t b) {
-  const uint32_t pr[4] = {(uint32_t)(b & 0xFFFFu), (uint32_t)((b >> 16) & 0xFFFFu), (uint32_t)((b >> 32) & 0xFFFFu),
-                          (uint32_t)(b >> 48)};
-  return place_row<6>(pr);
 }
 
 // store one packed row (8 codes) at byte offset 4r / 6r / 8r of its block
