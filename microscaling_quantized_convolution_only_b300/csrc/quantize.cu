@@ -251,12 +251,19 @@ template <typename T> __device__ __forceinline__ uint32_t to_bits32(uint32_t raw
 // bits).  The packed rows go to the sink `ob` (SmemRows or RegRows); returns
 // the E4M3 scale code.  TINY:
 // T_scale below 2^-62, encoded from x 2^64 and T_scale 2^64 (see up64).
+// inv_den: block_den_rcp<FMT, TINY>(s_t), the reciprocal the block-scale
+// quotient is formed with (the same for every block; the bracket test keeps
+// the decision exact).
+template <int FMT, bool TINY> __device__ __forceinline__ float block_den_rcp(float s_t) {
+  return __frcp_rn(Fmt<FMT>::EMAX * (TINY ? s_t * TINY_MULT : s_t));
+}
+
 template <int FMT, typename T, bool TINY, class Sink>
 __device__ __forceinline__ uint32_t encode_raw_block(const uint32_t (&raw)[sizeof(T) == 2 ? 32 : 64], uint32_t mb,
-                                                     float s_t, Sink &ob) {
+                                                     float s_t, float inv_den, Sink &ob) {
   const float st = TINY ? s_t * TINY_MULT : s_t;
   const float amax_b = TINY ? up64(__uint_as_float(mb)) : __uint_as_float(mb);
-  const uint32_t bs_code = block_scale_code<FMT>(amax_b, st);
+  const uint32_t bs_code = block_scale_code_r<FMT>(amax_b, st, inv_den);
   const float bs = code_value<8>(bs_code);
   float inv_lo, inv_hi;
   quot_bracket(bs, st, inv_lo, inv_hi);
@@ -370,7 +377,7 @@ __device__ __forceinline__ void nchw_body(const T *__restrict__ src, const Quant
     const int64_t blk = ((hw0 + hl) * GA + ga) * (int64_t)GB + gb0 + wl;
     RegRows<FMT> rows;
     const uint32_t bs_code = SR ? encode_raw_block_sr<FMT, T>(raw, mb, s_t, rows, blk, p.sr_seed)
-                                : encode_raw_block<FMT, T, TINY>(raw, mb, s_t, rows);
+                                : encode_raw_block<FMT, T, TINY>(raw, mb, s_t, block_den_rcp<FMT, TINY>(s_t), rows);
     rows.store(p.codes + blk * BB);
     p.scales[blk] = (uint8_t)bs_code;
   }
@@ -451,6 +458,7 @@ __device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl
   const int64_t HW = p.d2 * p.d3;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wl = warp % GBT, hl = (warp / GBT) * 32 + lane;
+  const float inv_den = block_den_rcp<FMT, TINY>(s_t);
   uint32_t my_amax = 0;
   int it = 0;
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
@@ -499,7 +507,7 @@ __device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl
       if (mb >= 0x7F800000u) atomicOr(p.status, ST_NONFINITE);
       const int64_t blk = ((hw0 + hl) * GA + ga) * (int64_t)GB + gb0 + wl;
       RegRows<FMT> rows;
-      const uint32_t bs_code = encode_raw_block<FMT, T, TINY>(raw, mb, s_t, rows);
+      const uint32_t bs_code = encode_raw_block<FMT, T, TINY>(raw, mb, s_t, inv_den, rows);
       rows.store(p.codes + blk * BB);
       p.scales[blk] = (uint8_t)bs_code;
     }
