@@ -841,17 +841,18 @@ TRAFFIC = {
     # whose 13 MB packed output is still in L2 when the launch ends, and the
     # plain one of layer 0 writing 45 MB of fp32 dX)
     ("stack4-56x56-c128-nvfp4", "conv_dgrad"): {
-        "bytes_per_launch": (13.437696e6 + 13.440256e6 + 13.444096e6 + (13.457152e6 + 45.473024e6)) / 4,
-        "batch": 64, "sources_sha1": "e9e621ec1c59f7f504b02308dbd58f2e0499c28a"},
+        "bytes_per_launch": (13.43744e6 + 13.43744e6 + 13.437952e6 + (13.428224e6 + 45.29536e6)) / 4,
+        "batch": 64, "sources_sha1": "7ef614e480f2ca7e7b7fabef90ab5a1358bf3688"},
     ("stack4-56x56-c128-nvfp4", "conv_fwd"): {
-        "bytes_per_launch": (13.435392e6 + 13.435392e6 + 13.44896e6 + (13.433856e6 + 45.340928e6)) / 4,
-        "batch": 64, "sources_sha1": "e9e621ec1c59f7f504b02308dbd58f2e0499c28a"},
+        "bytes_per_launch": (13.435648e6 + 13.434624e6 + 13.434624e6 + (13.43104e6 + 45.230848e6)) / 4,
+        "batch": 64, "sources_sha1": "7ef614e480f2ca7e7b7fabef90ab5a1358bf3688"},
     # the four launches alike; the small write term (split-K partials,
     # 0.07-0.08 MB) does not grow with the batch but is scaled with it
     ("stack4-56x56-c128-nvfp4", "conv_wgrad"): {
-        "bytes_per_launch": (26.627072e6 + 26.626816e6 + 26.621184e6 + 26.6304e6) / 4 + 0.075e6, "batch": 64,
-        "sources_sha1": "e9e621ec1c59f7f504b02308dbd58f2e0499c28a"},
+        "bytes_per_launch": (26.660352e6 + 26.64064e6 + 26.632192e6 + 26.631424e6) / 4 + 0.079e6, "batch": 64,
+        "sources_sha1": "7ef614e480f2ca7e7b7fabef90ab5a1358bf3688"},
 }
+
 
 
 
