@@ -839,19 +839,14 @@ def oracle_sample_step(wl, budget_s, state):
 TRAFFIC = {
     # one step's four launches (three with the fused requantization of dX,
     # whose 13 MB packed output is still in L2 when the launch ends, and the
-    # plain one of layer 0 writing 45 MB of fp32 dX)
-    ("stack4-56x56-c128-nvfp4", "conv_dgrad"): {
-        "bytes_per_launch": (13.43744e6 + 13.43744e6 + 13.437952e6 + (13.428224e6 + 45.29536e6)) / 4,
-        "batch": 64, "sources_sha1": "7ef614e480f2ca7e7b7fabef90ab5a1358bf3688"},
-    ("stack4-56x56-c128-nvfp4", "conv_fwd"): {
-        "bytes_per_launch": (13.435648e6 + 13.434624e6 + 13.434624e6 + (13.43104e6 + 45.230848e6)) / 4,
-        "batch": 64, "sources_sha1": "7ef614e480f2ca7e7b7fabef90ab5a1358bf3688"},
+    # plain one of layer 0 writing 45 MB of fp32 dX); bytes per launch
+    ("stack4-56x56-c128-nvfp4", "conv_dgrad"): {"bytes_per_launch": 24840576.0, "batch": 64, "sources_sha1": "973bf1c65ca0a5c03fe34bc8fa163a3055c4a2ef"},
+    ("stack4-56x56-c128-nvfp4", "conv_fwd"): {"bytes_per_launch": 24782848.0, "batch": 64, "sources_sha1": "973bf1c65ca0a5c03fe34bc8fa163a3055c4a2ef"},
     # the four launches alike; the small write term (split-K partials,
     # 0.07-0.08 MB) does not grow with the batch but is scaled with it
-    ("stack4-56x56-c128-nvfp4", "conv_wgrad"): {
-        "bytes_per_launch": (26.660352e6 + 26.64064e6 + 26.632192e6 + 26.631424e6) / 4 + 0.079e6, "batch": 64,
-        "sources_sha1": "7ef614e480f2ca7e7b7fabef90ab5a1358bf3688"},
+    ("stack4-56x56-c128-nvfp4", "conv_wgrad"): {"bytes_per_launch": 26711744.0, "batch": 64, "sources_sha1": "973bf1c65ca0a5c03fe34bc8fa163a3055c4a2ef"},
 }
+
 
 
 

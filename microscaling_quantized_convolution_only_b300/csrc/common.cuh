@@ -458,7 +458,7 @@ __device__ __forceinline__ void quot_bracket(float bs, float s_t, float &inv_lo,
   }
 }
 
-template <int F, bool PLACE = true>
+template <int F>
 __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs, float s_t, float inv_lo, float inv_hi);
 
 template <int F> __device__ __forceinline__ uint64_t encode_row8(const float (&v)[8], float bs, float s_t) {
@@ -543,9 +543,7 @@ __device__ __forceinline__ uint64_t cvt_row_e2m3(const float (&q)[8]) {
   return r;
 }
 
-// PLACE = false: E2M3 codes are returned in byte containers (element j in
-// byte j) instead of the packed 6-bit stream; other formats are unaffected.
-template <int F, bool PLACE>
+template <int F>
 __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs, float s_t, float inv_lo, float inv_hi) {
   float ql[8], qh[8];
 #pragma unroll
@@ -563,7 +561,7 @@ __device__ __forceinline__ uint64_t encode_row8_b(const float (&v)[8], float bs,
     for (int j = 0; j < 8; ++j) q[j] = tie_quotient(ql[j], qh[j], v[j], bs, s_t);
     row = F == 4 ? (uint64_t)cvt_row_e2m1(q) : F == 8 ? cvt_row_e4m3(q) : cvt_row_e2m3(q);
   }
-  if constexpr (F == 6 && PLACE) return pack_e2m3_row(row);
+  if constexpr (F == 6) return pack_e2m3_row(row);
   return row;
 }
 

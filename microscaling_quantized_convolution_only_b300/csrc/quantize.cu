@@ -68,15 +68,9 @@ __global__ void __launch_bounds__(256) amax_kernel(const T *__restrict__ src, in
 }
 
 // ------------------------------------------------------------- codes
-// Row sinks of the block encoders: packed rows written to a staging buffer
-// in shared memory, or collected in registers and written to the block's place
-// in global memory with 32- or 16-byte stores (block payload layout in
-// mqconv.h).
-template <int F> struct SmemRows {
-  uint8_t *ob;
-  __device__ __forceinline__ void put(int r, uint64_t bits) { store_row8<F>(ob, r, bits); }
-};
-
+// Row sink of the block encoders: the packed rows of one block collected in
+// registers and written to the block's place in global memory with 32- or
+// 16-byte stores (block payload layout in mqconv.h).
 template <int F> struct RegRows {
   static constexpr int NW = Fmt<F>::BLOCK_BYTES / 4;
   uint32_t w[NW];
@@ -248,7 +242,7 @@ template <typename T> __device__ __forceinline__ uint32_t to_bits32(uint32_t raw
 // Block scale and codes of one block whose 64 inputs are held as raw bits
 // (bf16 inputs two to a register, element 2k in the low half), row a of the
 // block (8 consecutive b) at raw[8a / PK ...]; `mb` is the block amax (fp32
-// bits).  The packed rows go to the sink `ob` (SmemRows or RegRows); returns
+// bits).  The packed rows go to the sink `ob` (a RegRows); returns
 // the E4M3 scale code.  TINY:
 // T_scale below 2^-62, encoded from x 2^64 and T_scale 2^64 (see up64).
 // inv_den: block_den_rcp<FMT, TINY>(s_t), the reciprocal the block-scale
