@@ -217,3 +217,32 @@ def test_tie_dense_inputs(cuda_device, fmt, exact, path):
     ref = oracle.quantize(x, fmt, role, layout)
     assert a == ref["amax"]
     assert_packed_equal(p, ref, f"tie-dense {path} {fmt} {'exact' if exact else 'near'}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("path", ["nchw-bf16-tma", "nchw-bf16-direct", "hwcn-f32"])
+def test_codes_buffer_16_byte_aligned_only(cuda_device, fmt, path):
+    """A codes buffer that starts 16 bytes past a 32-byte boundary (the
+    alignment the ABI requires): every block payload then takes the 16-byte
+    store path instead of the 32-byte one; codes and scales still bit-exact,
+    and the bytes around the buffer untouched."""
+    layout, dtype, shape = {"nchw-bf16-tma": ("nchw", "bf16", (16, 32, 8, 8)),
+                            "nchw-bf16-direct": ("nchw", "bf16", (16, 32, 7, 5)),
+                            "hwcn-f32": ("hwcn", "f32", (5, 6, 32, 16))}[path]
+    x = rand(shape, 31)
+    if dtype == "bf16":
+        x = S.to_bf16_rne(x)
+    role = "act" if layout == "nchw" else "grad"
+    dims = shape if layout == "nchw" else (shape[3], shape[2], shape[0], shape[1])
+    import microscaling_quantized_convolution_only_b300 as mq
+    nc = mq.packed_code_bytes(fmt, dims)
+    backing = torch.full((nc + 64,), 0xA5, dtype=torch.uint8, device=cuda_device)
+    assert backing.data_ptr() % 32 == 0
+    codes = backing[16:16 + nc]
+    p = mq.Packed(fmt, role, dims, device=cuda_device, codes=codes)
+    amax = torch.zeros(1, device=cuda_device)
+    mq.quantize_cbf(to_dev(x, dtype, cuda_device), layout, p, amax_out=amax)
+    mq.check_device_status()
+    assert_packed_equal(p, oracle.quantize(x, fmt, role, layout), f"16-byte-aligned codes {path} {fmt}")
+    rest = torch.cat([backing[:16], backing[16 + nc:]]).cpu()
+    assert bool((rest == 0xA5).all()), "bytes outside the codes buffer were written"
