@@ -415,6 +415,7 @@ constexpr int QT_THREADS = (QT_CWARPS + 1) * 32;
 
 struct QtCtl {
   uint64_t full[QT_STAGES], empty[QT_STAGES];
+  int coord[QT_STAGES][4];   // tile of each stage: position tile, b-group tile, a-group (set by the producer)
   int abort;
 };
 
@@ -458,8 +459,9 @@ __device__ __forceinline__ uint32_t tma_compute(const QuantParams &p, QtCtl *ctl
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int s = it % QT_STAGES;
     if (!qt_wait(&ctl->full[s], (it / QT_STAGES) & 1, ctl, p.status)) break;
-    const int tr = ntiles - 1 - t;                       // tiles in reverse memory order (see the producer)
-    const int hwt = tr % hw_tiles, rest = tr / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
+    // the stage's tile, written by the producer before the copy's arrival
+    // (read before this warp releases the stage)
+    const int hwt = ctl->coord[s][0], gbt = ctl->coord[s][1], ga = ctl->coord[s][2];
     const int64_t hw0 = (int64_t)hwt * HWT;
     const int gb0 = gbt * GBT;
     const int ngb = min(GBT, GB - gb0);
@@ -554,6 +556,11 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
         // tensor front to back, its tail is the part still in L2
         const int tr = ntiles - 1 - t;
         const int hwt = tr % hw_tiles, rest = tr / hw_tiles, gbt = rest % gb_tiles, ga = rest / gb_tiles;
+        // the quantizing warps read the tile from here, not by dividing
+        // themselves; the arrival below releases these writes
+        ctl->coord[s][0] = hwt;
+        ctl->coord[s][1] = gbt;
+        ctl->coord[s][2] = ga;
         mbar_expect_tx(&ctl->full[s], STAGE);
         tma_load_3d(ring + s * STAGE, &tm, &ctl->full[s], hwt * HWT, gbt * GBT * 8, ga * 8);
       }
