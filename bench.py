@@ -170,9 +170,11 @@ class OpTimer:
 
 # --------------------------------------------------------------- workloads
 class StackStep:
-    """The chained-stack training step (see module docstring)."""
+    """The chained-stack training step (see module docstring).  wdec: the
+    packed weights carry the decoded fp16 copy (written by the quantizer), so
+    fwd and dgrad copy the weight operand instead of decoding it per tile."""
 
-    def __init__(self, wl, device):
+    def __init__(self, wl, device, wdec=True):
         import torch
         import microscaling_quantized_convolution_only_b300 as mq
         self.mq, self.torch, self.wl, self.dev = mq, torch, wl, device
@@ -190,7 +192,7 @@ class StackStep:
         self.w = [t.to(device) for t in self.h_w]
         self.dy = self.h_dy.to(device)
         self.xq = [mq.Packed(fmt, "act", L.x_shape(), device=device) for _ in range(nl)]
-        self.wq = [mq.Packed(fmt, "weight", L.w_shape(), device=device) for _ in range(nl)]
+        self.wq = [mq.Packed(fmt, "weight", L.w_shape(), device=device, decoded=wdec) for _ in range(nl)]
         self.gq = [mq.Packed(fmt, "grad", L.y_shape(), device=device) for _ in range(nl)]
         self.y_last = torch.empty((L.Ho, L.Wo, L.Cout, L.N), dtype=torch.float32, device=device)
         self.dx = torch.empty((L.H, L.W, L.Cin, L.N), dtype=torch.float32, device=device)
@@ -207,19 +209,22 @@ class StackStep:
         w_el = int(np.prod(L.w_shape()))
         self.flops = {"fwd": nl * L.flops, "dgrad": nl * L.flops, "wgrad": nl * L.flops}
         in_b = 2 if wl.dtype == "bf16" else 4
-        self.qbytes = {   # algorithmic bytes: one read of the input + the packed output
-            "quant_bf16": 2 * (n_el * in_b + packed_bytes(fmt, n_el)) + nl * (w_el * in_b + packed_bytes(fmt, w_el)),
+        # weight operand bytes of one conv launch: the decoded copy (2 bytes an
+        # element) or the packed blocks
+        wb = 2 * w_el if wdec else packed_bytes(fmt, w_el)
+        self.qbytes = {   # algorithmic bytes: one read of the input + the packed output (+ the decoded copy)
+            "quant_bf16": 2 * (n_el * in_b + packed_bytes(fmt, n_el)) +
+                          nl * (w_el * in_b + packed_bytes(fmt, w_el) + (2 * w_el if wdec else 0)),
         }
         self.conv_bytes = {
-            "fwd": (nl - 1) * (2 * packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el)) +
-                   (packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el) + 4 * n_el),
-            "dgrad": (nl - 1) * (2 * packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el)) +
-                     (packed_bytes(fmt, n_el) + packed_bytes(fmt, w_el) + 4 * n_el),
+            "fwd": (nl - 1) * (2 * packed_bytes(fmt, n_el) + wb) + (packed_bytes(fmt, n_el) + wb + 4 * n_el),
+            "dgrad": (nl - 1) * (2 * packed_bytes(fmt, n_el) + wb) + (packed_bytes(fmt, n_el) + wb + 4 * n_el),
             "wgrad": nl * (2 * packed_bytes(fmt, n_el) + 4 * w_el),
         }
-        # amax + quantize of X0 and each W, fwd per layer, amax + quantize of dY,
-        # wgrad + split-K reduction and dgrad per layer
-        self.launches_per_step = (2 + 2 * nl) + nl + 2 + 2 * nl + nl
+        # amax + quantize of X0 and each W (+ the decoded copy of each W), fwd
+        # per layer, amax + quantize of dY, wgrad + split-K reduction and dgrad
+        # per layer
+        self.launches_per_step = (2 + 2 * nl) + (nl if wdec else 0) + nl + 2 + 2 * nl + nl
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in [self.h_x0, self.h_dy] + self.h_w)
         self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.dw)
 
@@ -298,9 +303,10 @@ class StackStep:
 
 class LayersStep:
     """Per-layer workloads (configs 0-3): every layer's X, W, dY quantized once
-    from fp32/bf16 NCHW/OIHW, then fwd, dgrad and wgrad of every layer."""
+    from fp32/bf16 NCHW/OIHW, then fwd, dgrad and wgrad of every layer.  wdec
+    as for StackStep."""
 
-    def __init__(self, wl, device):
+    def __init__(self, wl, device, wdec=True):
         import torch
         import microscaling_quantized_convolution_only_b300 as mq
         self.mq, self.torch, self.wl, self.dev = mq, torch, wl, device
@@ -316,7 +322,7 @@ class LayersStep:
             h = [torch.from_numpy(a).to(tdt) for a in (S.draw_x(wl, li), S.draw_w(wl, li), S.draw_dy(wl, li))]
             d = dict(L=L, h=h, x=h[0].to(device), w=h[1].to(device), dy=h[2].to(device),
                      xq=mq.Packed(fmt, "act", L.x_shape(), device=device),
-                     wq=mq.Packed(fmt, "weight", L.w_shape(), device=device),
+                     wq=mq.Packed(fmt, "weight", L.w_shape(), device=device, decoded=wdec),
                      gq=mq.Packed(fmt, "grad", L.y_shape(), device=device),
                      y=torch.empty((L.Ho, L.Wo, L.Cout, L.N), device=device),
                      dx=torch.empty((L.H, L.W, L.Cin, L.N), device=device),
@@ -327,13 +333,14 @@ class LayersStep:
             xe, we, ye = (int(np.prod(s)) for s in (L.x_shape(), L.w_shape(), L.y_shape()))
             for k in self.flops:
                 self.flops[k] += L.flops
-            self.conv_bytes["fwd"] += packed_bytes(fmt, xe) + packed_bytes(fmt, we) + 4 * ye
-            self.conv_bytes["dgrad"] += packed_bytes(fmt, we) + packed_bytes(fmt, ye) + 4 * xe
+            wb = 2 * we if wdec else packed_bytes(fmt, we)
+            self.conv_bytes["fwd"] += packed_bytes(fmt, xe) + wb + 4 * ye
+            self.conv_bytes["dgrad"] += wb + packed_bytes(fmt, ye) + 4 * xe
             self.conv_bytes["wgrad"] += packed_bytes(fmt, ye) + packed_bytes(fmt, xe) + 4 * we
-            self.qbytes["quant"] += (xe + we + ye) * in_b + packed_bytes(fmt, xe + we + ye)
+            self.qbytes["quant"] += (xe + we + ye) * in_b + packed_bytes(fmt, xe + we + ye) + (2 * we if wdec else 0)
             self.h2d_bytes += (xe + we + ye) * in_b
             self.d2h_bytes += we * 4
-        self.launches_per_step = len(self.layers) * (6 + 1 + 1 + 2)
+        self.launches_per_step = len(self.layers) * (6 + (1 if wdec else 0) + 1 + 1 + 2)
 
     def run(self, tm=None):
         mq = self.mq
@@ -380,8 +387,8 @@ def workload(args):
     return wl
 
 
-def make_step(wl, device):
-    return StackStep(wl, device) if wl.chained else LayersStep(wl, device)
+def make_step(wl, device, wdec=True):
+    return StackStep(wl, device, wdec) if wl.chained else LayersStep(wl, device, wdec)
 
 
 # -------------------------------------------------------------- GPU arm
@@ -485,14 +492,14 @@ def layer_rows(wl, per_layer, peaks, launch_bound_us=5.0):
     return rows
 
 
-def extra_workload(name, device, peaks, steps, flush):
+def extra_workload(name, device, peaks, steps, flush, wdec=True):
     """One more workload after the headline: its whole step as a CUDA graph
     (per-op and per-layer CUDA-event times), and the quantizer alone on each
     of its activation and output-gradient tensors of 8 MB or more."""
     import torch
     import microscaling_quantized_convolution_only_b300 as mq
     wl = S.WORKLOADS[WORKLOADS[name]]
-    step = make_step(wl, device)
+    step = make_step(wl, device, wdec)
     for _ in range(3):
         step.run()
     torch.cuda.synchronize()
@@ -557,7 +564,7 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     wl = workload(args)
-    step = make_step(wl, device)
+    step = make_step(wl, device, not args.packed_weights)
     peaks = load_peaks()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)   # > 126 MB L2
 
@@ -767,6 +774,9 @@ def run_gpu(args):
                                 "one CUDA graph per step holding the L2 flush, the start event, the step and the "
                                 "end event; per-op times from a copy of the step's graph with CUDA events around "
                                 "each op group",
+                   "weights": "packed blocks, decoded per tile" if args.packed_weights else
+                              "packed blocks + the decoded fp16 copy the quantizer writes beside them; fwd and "
+                              "dgrad copy it as their weight operand",
                    "e2e_inputs": "double-buffered: each step copies the next step's inputs from pinned host "
                                  "memory on a copy stream while it computes" if hasattr(step, "new_staging") else
                                  "copied from pinned host memory at the start of each step",
@@ -788,7 +798,8 @@ def run_gpu(args):
         extras = {}
         for name in ("tiny-3x3", "resnet32-cifar", "resnet18-224", "yolov8n-640-fp8", "stack4-fp6"):
             if WORKLOADS[name] != WORKLOADS[args.workload]:
-                extras[S.WORKLOADS[WORKLOADS[name]].name] = extra_workload(name, device, peaks, 3, flush)
+                extras[S.WORKLOADS[WORKLOADS[name]].name] = extra_workload(name, device, peaks, 3, flush,
+                                                                            not args.packed_weights)
         result["workloads"] = extras
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
@@ -947,6 +958,9 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of one CUDA graph per step")
     ap.add_argument("--no-extra-workloads", action="store_true",
                     help="time only the headline workload (the default also times the other workloads after it)")
+    ap.add_argument("--packed-weights", action="store_true",
+                    help="convolutions decode the packed weight blocks per tile instead of copying the decoded "
+                         "fp16 copy that the quantizer writes beside them")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch N (multiple of 8) for small profiling captures; "
                          "the default runs the workload as specified")

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define MQCONV_ABI_VERSION 2
+#define MQCONV_ABI_VERSION 3
 
 /* cudaStream_t without including CUDA headers */
 typedef struct CUstream_st *mq_stream;
@@ -96,7 +96,25 @@ typedef struct {
   void *codes;       /* device, mqconv_packed_code_bytes() bytes */
   uint8_t *scales;   /* device, mqconv_packed_scale_bytes() bytes */
   float *s_t;        /* device, one float: T_scale */
+  void *decoded;     /* WEIGHT only, optional (else NULL): device fp16 copy of the
+                        block values, mqconv_weight_decoded_bytes() bytes (below) */
 } mq_packed;
+
+/* Decoded weight copy (optional; role WEIGHT only).
+ *   Blocks in the packed order [Kh][Kw][Cout/8][Cin/8], 128 bytes each: row r
+ *   of a block (output channel 8*cog + r) holds eight fp16 values, input
+ *   channels 8*cig .. 8*cig+7, each code * B_scale -- times 1/4 for E4M3
+ *   codes, whose products can exceed the fp16 range -- without T_scale, which
+ *   the convolutions apply in fp32.  Every value is exact in fp16.
+ *   The convolutions decode the packed weight blocks on chip once per output
+ *   tile; a small, deep layer has few output positions per weight block, so
+ *   every tile repeats the same decode.  With the copy, mqconv_fwd,
+ *   mqconv_dgrad and mqconv_dgrad_requant copy the weight operand straight
+ *   into shared memory instead (same results, bit for bit).  It is a cache of
+ *   codes and scales: mqconv_quantize_cbf rewrites it with them, and a caller
+ *   that changes codes or scales otherwise calls mqconv_weight_decode.
+ *   Must be 16-byte aligned (MQ_ERR_ALIGNMENT); non-NULL on a tensor of
+ *   another role is MQ_ERR_INVALID_ARG. */
 
 /* One convolution layer: cross-correlation, zero padding, square stride/pad.
  * Ho = (H + 2 pad - Kh) / stride + 1, Wo likewise (paperlayer summary of the
@@ -128,6 +146,13 @@ const char *mqconv_status_string(mq_status status);
  * mq_packed.  Returns 0 for invalid arguments. */
 size_t mqconv_packed_code_bytes(int32_t fmt, const int64_t dims[4]);
 size_t mqconv_packed_scale_bytes(const int64_t dims[4]);
+/* Bytes of the decoded weight copy of a packed weight tensor with dims
+ * (Cout, Cin, Kh, Kw): 128 per block.  Returns 0 for invalid arguments. */
+size_t mqconv_weight_decoded_bytes(const int64_t dims[4]);
+
+/* (Re)write wq->decoded from wq's codes and scales (see "Decoded weight
+ * copy").  wq: role WEIGHT, decoded non-NULL. */
+mq_status mqconv_weight_decode(const mq_packed *wq, mq_stream stream);
 
 /*
  * Quantize one dense tensor once (MicroQonv §III-A, §IV-B).
@@ -138,6 +163,7 @@ size_t mqconv_packed_scale_bytes(const int64_t dims[4]);
  *            tensor's own amax (amax_out must then be non-NULL; it receives
  *            that amax).  Non-NULL: one pass, T_scale from *amax_in; amax_out,
  *            if non-NULL, receives the measured amax.
+ *   A WEIGHT dst with a decoded copy gets it rewritten after the codes.
  *   Non-finite input sets MQ_ERR_NONFINITE in the device status word (the
  *   output is then unspecified).
  */
@@ -158,7 +184,8 @@ mq_status mqconv_quantize_cbf_sr(const void *src, int32_t dtype, int32_t layout,
  * channel-batch-first im2col of Xq (MicroQonv §IV-A:
  * Y_{fCout,N} = W_{fCout,Cin} . X'_{Cin,N}).
  *   xq  packed activations, role ACT, dims (N, Cin, H, W).
- *   wq  packed weights, role WEIGHT, dims (Cout, Cin, Kh, Kw).
+ *   wq  packed weights, role WEIGHT, dims (Cout, Cin, Kh, Kw); with a
+ *       decoded copy, that copy is the weight operand (same results).
  *   y   device fp32 [Ho][Wo][Cout][N] (HWCN), or NULL when rq is given.
  *   rq  NULL, or the fused requantizing epilogue (see mq_requant).
  */
@@ -170,7 +197,8 @@ mq_status mqconv_fwd(const mq_conv_desc *desc, const mq_packed *xq, const mq_pac
  * convolution, i.e. G_Y correlated with the spatially flipped, channel-
  * transposed kernels (paperlayer summary §II-A "Backward Pass"; MicroQonv §IV-A:
  * G_X'_{Cin,N} = W^T_{fCout,Cin} . G_Y_{fCout,N}).
- *   wq   packed weights, role WEIGHT, dims (Cout, Cin, Kh, Kw).
+ *   wq   packed weights, role WEIGHT, dims (Cout, Cin, Kh, Kw); with a
+ *        decoded copy, that copy is the weight operand (same results).
  *   dyq  packed output gradient, role GRAD, dims (N, Cout, Ho, Wo).
  *   dx   device fp32 [H][W][Cin][N] (HWCN).
  */

@@ -34,7 +34,8 @@ class MQError(RuntimeError):
 
 class _Packed(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("role", ctypes.c_int32), ("dims", ctypes.c_int64 * 4),
-                ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("s_t", ctypes.c_void_p)]
+                ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("s_t", ctypes.c_void_p),
+                ("decoded", ctypes.c_void_p)]
 
 
 class _Desc(ctypes.Structure):
@@ -72,6 +73,9 @@ def lib() -> ctypes.CDLL:
         L.mqconv_packed_code_bytes.restype = ctypes.c_size_t
         L.mqconv_packed_scale_bytes.argtypes = [P]
         L.mqconv_packed_scale_bytes.restype = ctypes.c_size_t
+        L.mqconv_weight_decoded_bytes.argtypes = [P]
+        L.mqconv_weight_decoded_bytes.restype = ctypes.c_size_t
+        L.mqconv_weight_decode.argtypes = [ctypes.POINTER(_Packed), P]
         L.mqconv_quantize_cbf.argtypes = [P, i32, i32, ctypes.POINTER(_Packed), P, P, P]
         L.mqconv_quantize_cbf_sr.argtypes = [P, i32, i32, ctypes.POINTER(_Packed), P, P, ctypes.c_uint64, P]
         L.mqconv_fwd.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(_Packed), ctypes.POINTER(_Packed), P,
@@ -88,7 +92,7 @@ def lib() -> ctypes.CDLL:
                                            P]
         L.mqconv_test_fault_inject.argtypes = [i32]
         for f in ("mqconv_quantize_cbf", "mqconv_quantize_cbf_sr", "mqconv_fwd", "mqconv_dgrad", "mqconv_dgrad_requant", "mqconv_wgrad",
-                  "mqconv_device_status", "mqconv_wgrad_noalloc", "mqconv_test_fault_inject"):
+                  "mqconv_device_status", "mqconv_wgrad_noalloc", "mqconv_test_fault_inject", "mqconv_weight_decode"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -128,12 +132,19 @@ def packed_scale_bytes(dims: Sequence[int]) -> int:
     return int(lib().mqconv_packed_scale_bytes(ctypes.cast(_dims(dims), ctypes.c_void_p)))
 
 
+def weight_decoded_bytes(dims: Sequence[int]) -> int:
+    return int(lib().mqconv_weight_decoded_bytes(ctypes.cast(_dims(dims), ctypes.c_void_p)))
+
+
 class Packed:
     """A packed 8x8-block tensor whose buffers are torch device tensors.
 
-    dims: act/grad (N, C, H, W); weight (Cout, Cin, Kh, Kw)."""
+    dims: act/grad (N, C, H, W); weight (Cout, Cin, Kh, Kw).  decoded (weights
+    only): True to allocate the decoded fp16 copy (mq_packed.decoded), or a
+    uint8 device tensor of weight_decoded_bytes(dims) bytes to use as it."""
 
-    def __init__(self, fmt: str, role: str, dims: Sequence[int], device="cuda", codes=None, scales=None, s_t=None):
+    def __init__(self, fmt: str, role: str, dims: Sequence[int], device="cuda", codes=None, scales=None, s_t=None,
+                 decoded=None):
         self.fmt, self.role, self.dims = fmt, role, tuple(int(v) for v in dims)
         nc, ns = packed_code_bytes(fmt, self.dims), packed_scale_bytes(self.dims)
         if nc == 0:
@@ -141,10 +152,20 @@ class Packed:
         self.codes = codes if codes is not None else torch.empty(nc, dtype=torch.uint8, device=device)
         self.scales = scales if scales is not None else torch.empty(ns, dtype=torch.uint8, device=device)
         self.s_t = s_t if s_t is not None else torch.zeros(1, dtype=torch.float32, device=device)
+        if decoded is True:
+            decoded = torch.empty(weight_decoded_bytes(self.dims), dtype=torch.uint8, device=device)
+        self.decoded = decoded if decoded is not None and decoded is not False else None
 
     def c(self) -> _Packed:
         return _Packed(FMT[self.fmt], ROLE[self.role], _dims(self.dims), self.codes.data_ptr(),
-                       self.scales.data_ptr(), self.s_t.data_ptr())
+                       self.scales.data_ptr(), self.s_t.data_ptr(),
+                       None if self.decoded is None else self.decoded.data_ptr())
+
+
+def weight_decode(wq: Packed, stream=None) -> None:
+    """mqconv_weight_decode: rewrite wq.decoded from wq's codes and scales."""
+    c = wq.c()
+    _check(lib().mqconv_weight_decode(ctypes.byref(c), _stream(stream)), "mqconv_weight_decode")
 
 
 def desc(layer) -> _Desc:

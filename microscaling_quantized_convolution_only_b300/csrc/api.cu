@@ -56,6 +56,8 @@ mq_status check_packed(const mq_packed *t, int32_t role, int64_t d0, int64_t d1,
   if (t->dims[0] != d0 || t->dims[1] != d1 || t->dims[2] != d2 || t->dims[3] != d3) return MQ_ERR_INVALID_ARG;
   if (!aligned16(t->codes) || !aligned16(t->scales) || (reinterpret_cast<uintptr_t>(t->s_t) & 3u))
     return MQ_ERR_ALIGNMENT;
+  if (t->decoded && t->role != MQ_ROLE_WEIGHT) return MQ_ERR_INVALID_ARG;
+  if (!aligned16(t->decoded)) return MQ_ERR_ALIGNMENT;
   return MQ_OK;
 }
 
@@ -229,6 +231,7 @@ mq_status conv_fwd_or_dgrad(int op, const mq_conv_desc *desc, const mq_packed *a
   p.b = operand(wq);
   p.pre_mult = pre_mult(a->fmt, wq->fmt);
   p.out = out;
+  p.wdec = wq->decoded;
   if (rq) {
     p.rq.codes = static_cast<uint8_t *>(rq->out->codes);
     p.rq.scales = rq->out->scales;
@@ -271,6 +274,24 @@ size_t mqconv_packed_code_bytes(int32_t fmt, const int64_t dims[4]) {
          (size_t)mq::block_bytes(fmt);
 }
 
+size_t mqconv_weight_decoded_bytes(const int64_t dims[4]) { return 128 * mqconv_packed_scale_bytes(dims); }
+
+mq_status mqconv_weight_decode(const mq_packed *wq, mq_stream stream) {
+  if (!wq || !wq->decoded || wq->role != MQ_ROLE_WEIGHT) return MQ_ERR_INVALID_ARG;
+  const int64_t *d = wq->dims;
+  if (d[0] <= 0 || d[1] <= 0 || d[2] <= 0 || d[3] <= 0) return MQ_ERR_INVALID_ARG;
+  if (d[0] % 8 || d[1] % 8) return MQ_ERR_UNSUPPORTED;
+  mq_status st = check_packed(wq, MQ_ROLE_WEIGHT, d[0], d[1], d[2], d[3]);
+  if (st != MQ_OK) return st;
+  DevInfo *di = nullptr;
+  if ((st = dev_info(&di)) != MQ_OK) return st;
+  return mq::launch_weight_decode(static_cast<const uint8_t *>(wq->codes), wq->scales, wq->fmt,
+                                  (d[0] / 8) * (d[1] / 8) * d[2] * d[3], wq->decoded, di->num_sms,
+                                  reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MQ_OK
+             : MQ_ERR_CUDA;
+}
+
 size_t mqconv_packed_scale_bytes(const int64_t dims[4]) {
   if (!dims || dims[0] <= 0 || dims[1] <= 0 || dims[2] <= 0 || dims[3] <= 0 || dims[0] % 8 || dims[1] % 8) return 0;
   return (size_t)(dims[0] / 8) * (size_t)(dims[1] / 8) * (size_t)dims[2] * (size_t)dims[3];
@@ -284,11 +305,13 @@ mq_status quantize_cbf(const void *src, int32_t dtype, int32_t layout, const mq_
   if (dst->role != MQ_ROLE_ACT && dst->role != MQ_ROLE_WEIGHT && dst->role != MQ_ROLE_GRAD) return MQ_ERR_INVALID_ARG;
   if (layout != MQ_LAYOUT_NCHW && layout != MQ_LAYOUT_HWCN && layout != MQ_LAYOUT_OIHW) return MQ_ERR_INVALID_ARG;
   if ((dst->role == MQ_ROLE_WEIGHT) != (layout == MQ_LAYOUT_OIHW)) return MQ_ERR_INVALID_ARG;
+  if (dst->decoded && dst->role != MQ_ROLE_WEIGHT) return MQ_ERR_INVALID_ARG;
   const int64_t *d = dst->dims;
   if (d[0] <= 0 || d[1] <= 0 || d[2] <= 0 || d[3] <= 0) return MQ_ERR_INVALID_ARG;
   if (d[0] % 8 || d[1] % 8) return MQ_ERR_UNSUPPORTED;
   if (!amax_in && !amax_out) return MQ_ERR_INVALID_ARG;
-  if (!aligned16(src) || !aligned16(dst->codes) || (reinterpret_cast<uintptr_t>(dst->s_t) & 3u) ||
+  if (!aligned16(src) || !aligned16(dst->codes) || !aligned16(dst->decoded) ||
+      (reinterpret_cast<uintptr_t>(dst->s_t) & 3u) ||
       (amax_in && (reinterpret_cast<uintptr_t>(amax_in) & 3u)) ||
       (amax_out && (reinterpret_cast<uintptr_t>(amax_out) & 3u)))
     return MQ_ERR_ALIGNMENT;
@@ -323,6 +346,10 @@ mq_status quantize_cbf(const void *src, int32_t dtype, int32_t layout, const mq_
     if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), s) != cudaSuccess) return MQ_ERR_CUDA;
   }
   if (mq::launch_quantize(src, dtype, layout, dst->fmt, p, di->num_sms, s) != cudaSuccess) return MQ_ERR_CUDA;
+  if (dst->decoded &&
+      mq::launch_weight_decode(p.codes, p.scales, dst->fmt, (d[0] / 8) * (d[1] / 8) * d[2] * d[3], dst->decoded,
+                               di->num_sms, s) != cudaSuccess)
+    return MQ_ERR_CUDA;
   return MQ_OK;
 }
 }  // namespace

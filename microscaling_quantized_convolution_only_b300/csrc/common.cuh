@@ -358,6 +358,19 @@ template <int F> __device__ __forceinline__ uint4 decode_raw(uint2 w, uint32_t s
   }
 }
 
+// raw bits of row r (8 codes) of a packed block (shared or global memory,
+// 16-byte aligned)
+template <int F> __device__ __forceinline__ uint2 row8_bits(const uint8_t *blk, int r) {
+  if (F == 4) return make_uint2(*reinterpret_cast<const uint32_t *>(blk + 4 * r), 0u);
+  if (F == 8) return *reinterpret_cast<const uint2 *>(blk + 8 * r);
+  // E2M3: row r is bytes 6r .. 6r+5 of the 48-byte block; two aligned 32-bit
+  // loads from byte 6r rounded down to a multiple of 4 (at most byte 47
+  // read) and a funnel shift by 0 or 16 bits
+  const uint32_t *w = reinterpret_cast<const uint32_t *>(blk + ((6 * r) & ~3));
+  const uint32_t w0 = w[0], w1 = w[1], sh = (uint32_t)((6 * r) & 2) * 8u;
+  return make_uint2(__funnelshift_r(w0, w1, sh), (w1 >> sh) & 0xFFFFu);
+}
+
 // fp16 pair holding the E4M3 block scale (times 1/4 for E4M3-coded operands,
 // whose code * scale can exceed the fp16 range; the epilogue multiplies back).
 template <int F> __device__ __forceinline__ uint32_t scale_pair(uint8_t sc) {

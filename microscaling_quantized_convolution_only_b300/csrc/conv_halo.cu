@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         const int na = p.na_blocks * 8;
         for (int i = tid; i < na; i += WG_DEC_THREADS) {
           const int blk = i >> 3, r = i & 7;
-          const uint4 v = decode_raw<FA>(lds_row<FA>(pk + blk * BBA, r), scale_pair<FA>(sc[blk]));
+          const uint4 v = decode_raw<FA>(row8_bits<FA>(pk + blk * BBA, r), scale_pair<FA>(sc[blk]));
           *reinterpret_cast<uint4 *>(dec + i * 16) = v;
         }
         const int nb = p.nb_blocks * 8;
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         uint8_t *decb = dec + p.dec_b_off;
         for (int i = tid; i < nb; i += WG_DEC_THREADS) {
           const int blk = i >> 3, r = i & 7;
-          const uint4 v = decode_raw<FB>(lds_row<FB>(pkb + blk * BBB, r), scale_pair<FB>(sc[p.na_blocks + blk]));
+          const uint4 v = decode_raw<FB>(row8_bits<FB>(pkb + blk * BBB, r), scale_pair<FB>(sc[p.na_blocks + blk]));
           *reinterpret_cast<uint4 *>(decb + i * 16) = v;
         }
         fence_async_smem();
@@ -374,12 +374,16 @@ size_t halo_smem(HaloConv &h, int bba, int bbb) {
   h.dec_b_off = (uint32_t)h.nh_blocks * 128;
   h.dec_stage = (uint32_t)(h.nh_blocks + h.nb_blocks) * 128;
   h.pk_b_off = (uint32_t)((h.nh_blocks * bba + 127) / 128 * 128);
+  // with the decoded weight copy the packed stages hold the halo only, and the
+  // weights go by TMA straight into the decoded stages (wd_bytes per chunk)
+  const int nbp = h.wd ? 0 : h.nb_blocks;
+  h.wd_bytes = h.wd ? (uint32_t)h.nb_blocks * 128 : 0u;
   // bytes the boxes deliver per chunk (the phase padding is not written)
-  h.pk_bytes = (uint32_t)(h.NPH * h.RH * h.WP * h.G * CGC * bba + h.nb_blocks * bbb);
-  h.pk_stage = (uint32_t)((h.pk_b_off + h.nb_blocks * bbb + 127) / 128 * 128);
+  h.pk_bytes = (uint32_t)(h.NPH * h.RH * h.WP * h.G * CGC * bba + nbp * bbb);
+  h.pk_stage = (uint32_t)((h.pk_b_off + nbp * bbb + 127) / 128 * 128);
   h.sc_bytes = (uint32_t)(h.NPH * h.PHP * h.G * h.CGin);
   h.scw_off = (h.sc_bytes + 15) / 16 * 16;
-  const uint32_t scw = h.op == OP_FWD ? (uint32_t)(taps * h.NB * h.CIG) : (uint32_t)(taps * h.COG * h.NB);
+  const uint32_t scw = h.wd ? 0u : h.op == OP_FWD ? (uint32_t)(taps * h.NB * h.CIG) : (uint32_t)(taps * h.COG * h.NB);
   h.sc_stride = (h.scw_off + scw + 127) / 128 * 128;
   const size_t fixed = 1024 + (size_t)DSTAGES * h.dec_stage + 2 * h.sc_stride + sizeof(HcCtl) + 128;
   if (fixed + 2 * (size_t)h.pk_stage > SMEM_LIMIT) return 0;
@@ -526,10 +530,15 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
       const int64_t tiles = (int64_t)(h.NG / h.G) * ((h.Wout + h.P - 1) / h.P) * ((h.Hout + R - 1) / R) *
                             ((h.NC + BN - 1) / BN);
       // per chunk the MMAs and the decode of its halo + weight blocks
-      // overlap; measured in this kernel (two issuers, 8 decode warps):
-      // ~2x the isolated MMA cost and ~7.7 cycles per decoded block
+      // overlap; measured in this kernel (8 decode warps): ~2x the isolated
+      // MMA cost with both issuers busy, ~1.6x that per MMA for one issuer
+      // on its own (a tile's accumulators are split between the two issuers,
+      // so one accumulator leaves one of them idle and three give one of
+      // them two), and ~7.7 cycles per decoded block
       const double mma = 2.0 * std::max(BN / 2.0, BN == 64 ? 48.0 : 40.0);
-      const double chunk_t = std::max((double)R * taps * mma, 7.7 * (c.nh_blocks + c.nb_blocks));
+      const double mmas = (double)R * taps, per_issuer = mmas * ((c.RT + 1) / 2) / c.RT;
+      const double chunk_t = std::max(std::max(mmas * mma, 1.6 * per_issuer * mma),
+                                      7.7 * (c.nh_blocks + c.nb_blocks));
       const double tile_t = (h.nchunks + 2.0) * chunk_t;
       const double rounds = (double)((tiles + num_sms - 1) / num_sms);
       // the epilogue of a tile (measured: ~8.5 cycles per accumulator
@@ -550,6 +559,20 @@ bool halo_plan(const ConvParams &cp, HaloConv &h, int num_sms) {
   }
   if (!found) return false;
   h = best_h;
+  // The decoded weight copy keeps the tile plan (its benefit is the weight
+  // decode saved per chunk; a plan chosen for it would trade that against
+  // tile overheads the cost model does not see) and frees the shared memory
+  // of the packed weights.  Its box spans all taps in one dimension (at most
+  // 256).
+  if (cp.wdec && taps <= 256) {
+    HaloConv w = h;
+    w.wd = 1;
+    const size_t sm = halo_smem(w, bba, bbb);
+    if (sm) {
+      w.smem = sm;
+      h = w;
+    }
+  }
   h.gran_h = pow2_part(h.G * h.CGin);
   h.gran_w = h.op == OP_FWD ? pow2_part(h.CIG * std::gcd(h.COG, h.NB)) : pow2_part(std::gcd(h.CIG, h.NB));
   h.tiles_g = h.NG / h.G;
@@ -590,7 +613,18 @@ cudaError_t halo_launch(const ConvParams &cp, HaloConv &h, int num_sms, cudaStre
     const uint32_t bx[5] = {(uint32_t)(CGC * bba / 8), (uint32_t)h.G, 1u, (uint32_t)h.WP, (uint32_t)h.RH};
     if (!make_tensor_map_strided(&ma, cp.a.codes, 8, 5, d, gs, bx)) return cudaErrorInvalidValue;
   }
-  {
+  if (h.wd) {
+    // decoded weights [taps][COG][CIG][128 bytes] as 8-byte units; box: a
+    // chunk's CGC input-channel groups x the tile's NB output-channel groups
+    // (fwd), or the tile's NB input-channel groups x CGC output-channel
+    // groups (dgrad), all taps -- the order the decode warps would write
+    const uint64_t d[4] = {16, (uint64_t)h.CIG, (uint64_t)h.COG, (uint64_t)(h.Kh * h.Kw)};
+    const uint64_t gs[3] = {128, (uint64_t)h.CIG * 128, (uint64_t)h.COG * h.CIG * 128};
+    uint32_t bx[4] = {16u, 0u, 0u, (uint32_t)(h.Kh * h.Kw)};
+    bx[1] = (uint32_t)(cp.op == OP_FWD ? CGC : h.NB);
+    bx[2] = (uint32_t)(cp.op == OP_FWD ? h.NB : CGC);
+    if (!make_tensor_map_strided(&mb, cp.wdec, 8, 4, d, gs, bx)) return cudaErrorInvalidValue;
+  } else {
     // weights [taps][COG][CIG * BBB]
     const uint64_t d[3] = {(uint64_t)h.CIG * bbb / 8, (uint64_t)h.COG, (uint64_t)(h.Kh * h.Kw)};
     uint32_t bx[3];

@@ -83,6 +83,7 @@ constexpr int MAX_R = 8;
 struct HcCtl {
   uint64_t pfull[MAX_PS], pempty[MAX_PS];
   uint64_t dfull[DSTAGES], dempty[DSTAGES];
+  uint64_t wfull[DSTAGES];   // decoded weight copy landed in the decoded stage (wd only)
   uint64_t sfull[2], sempty[2];
   uint64_t acc_full[MAX_R], acc_empty[MAX_R];
   uint64_t done;
@@ -122,18 +123,6 @@ __device__ __forceinline__ bool hc_drain(uint64_t *bar, uint32_t parity, uint32_
       return false;
     }
   }
-}
-
-// raw bits of row r (8 codes) of a packed block in shared memory
-template <int F> __device__ __forceinline__ uint2 lds_row(const uint8_t *blk, int r) {
-  if (F == 4) return make_uint2(*reinterpret_cast<const uint32_t *>(blk + 4 * r), 0u);
-  if (F == 8) return *reinterpret_cast<const uint2 *>(blk + 8 * r);
-  // E2M3: row r is bytes 6r .. 6r+5 of the (16-byte aligned) 48-byte block;
-  // two aligned 32-bit loads from byte 6r rounded down to a multiple of 4
-  // (at most byte 47 read) and a funnel shift by 0 or 16 bits
-  const uint32_t *w = reinterpret_cast<const uint32_t *>(blk + ((6 * r) & ~3));
-  const uint32_t w0 = w[0], w1 = w[1], sh = (uint32_t)((6 * r) & 2) * 8u;
-  return make_uint2(__funnelshift_r(w0, w1, sh), (w1 >> sh) & 0xFFFFu);
 }
 
 struct TileCoord {
@@ -359,6 +348,7 @@ __device__ __forceinline__ void hc_issue(const HaloConv &p, HcCtl *ctl, uint8_t 
       for (int c = 0; c < p.nchunks; ++c, ++dit) {
         const int ds = dit % DSTAGES;
         if (!hc_wait(&ctl->dfull[ds], (dit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
+        if (p.wd && !hc_wait(&ctl->wfull[ds], (dit / DSTAGES) & 1, p, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t a_stage = (uint32_t)a_desc + (uint32_t)ds * d_stage;
         const uint32_t b_stage = (uint32_t)b_desc + (uint32_t)ds * d_stage;
@@ -524,6 +514,7 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
     for (int s = 0; s < DSTAGES; ++s) {
       mbar_init(&ctl->dfull[s], HC_DEC_WARPS);
       mbar_init(&ctl->dempty[s], p.RT >= 2 ? 2 : 1);   // one commit per issuer
+      mbar_init(&ctl->wfull[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl->sfull[s], 64);
@@ -553,8 +544,9 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
     // Per tile the whole warp copies the halo block scales (zero outside the
     // image, where the TMA zero-fills the codes too) and the weight block
     // scales asynchronously into the tile's scale buffer (64 arrivals: two
-    // per lane); lane 0 then streams the packed codes of every chunk.
-    int pit = 0, k = 0;
+    // per lane); lane 0 then streams the packed codes of every chunk, and
+    // with the decoded weight copy lane 1 streams the chunks' weights.
+    int pit = 0, wit = 0, k = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++k) {
       const TileCoord tc = hc_tile(p, t);
@@ -579,15 +571,16 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
               return p.in_scales + (((int64_t)hi * p.Win + wi) * p.NG + tc.g0) * p.CGin;
             },
             [&](int) { return run; }, p.in_scales, lane);
-        // weight block scales of the tile's output channels
+        // weight block scales of the tile's output channels (none with the
+        // decoded copy, which has them applied)
         const int nb0 = tc.n0 / 8;
-        if (OP == OP_FWD) {
+        if (OP == OP_FWD && !p.wd) {
           const int nbv = min(p.NB, p.COG - nb0), fill = p.NB * p.CIG;
           copy_runs_rt(
               p.gran_w, scd + p.scw_off, p.Kh * p.Kw, fill, fill,
               [&](int tap) -> const uint8_t * { return p.w_scales + ((int64_t)tap * p.COG + nb0) * p.CIG; },
               [&](int) { return nbv * p.CIG; }, p.w_scales, lane);
-        } else {
+        } else if (!p.wd) {
           const int nbv = min(p.NB, p.CIG - nb0);
           copy_runs_rt(
               p.gran_w, scd + p.scw_off, p.Kh * p.Kw * p.COG, p.NB, p.NB,
@@ -615,14 +608,30 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
                           (wc0 - gph) / 2, 2 * tc.h0 - p.padh);
             }
           }
-          if (OP == OP_FWD)
+          if (OP == OP_FWD && !p.wd)
             tma_load_3d(dst + p.pk_b_off, &tm_w, &ctl->pfull[ps], c * CGC * BBB / 8, tc.n0 / 8, 0);
-          else
+          else if (!p.wd)
             tma_load_3d(dst + p.pk_b_off, &tm_w, &ctl->pfull[ps], (tc.n0 / 8) * BBB / 8, c * CGC, 0);
         }
+      } else if (lane == 1 && p.wd) {
+        // the decoded weight copy, straight into the weight half of each
+        // decoded stage once the MMAs have released it (its own barrier, so
+        // that it can be drained whatever the decode warps do)
+        for (int c = 0; c < p.nchunks; ++c, ++wit) {
+          const int ds = wit % DSTAGES;
+          if (!hc_wait(&ctl->dempty[ds], ((wit / DSTAGES) & 1) ^ 1, p, ctl)) { ok = false; break; }
+          mbar_expect_tx(&ctl->wfull[ds], p.wd_bytes);
+          uint8_t *dst = smem + p.off_dec + ds * p.dec_stage + p.dec_b_off;
+          if (OP == OP_FWD)
+            tma_load_4d(dst, &tm_w, &ctl->wfull[ds], 0, c * CGC, tc.n0 / 8, 0);
+          else
+            tma_load_4d(dst, &tm_w, &ctl->wfull[ds], 0, tc.n0 / 8, c * CGC, 0);
+        }
       }
-      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      const int okv = ok ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, okv, 0) != 0 && __shfl_sync(0xFFFFFFFFu, okv, 1) != 0;
       pit = __shfl_sync(0xFFFFFFFFu, pit, 0);
+      wit = __shfl_sync(0xFFFFFFFFu, wit, 1);
     }
     // let the copies in flight land before the CTA can exit: the last boxes
     // (whatever the abort flag says) and this warp's scale copies
@@ -630,6 +639,11 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
       for (int i = 0; i < p.PS && i < pit; ++i) {
         const int q = pit - 1 - i;
         hc_drain(&ctl->pfull[q % p.PS], (q / p.PS) & 1, p.status);
+      }
+    } else if (lane == 1) {
+      for (int i = 0; i < DSTAGES && i < wit; ++i) {
+        const int q = wit - 1 - i;
+        hc_drain(&ctl->wfull[q % DSTAGES], (q / DSTAGES) & 1, p.status);
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -659,12 +673,12 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
           const int blk = i >> 3, r = i & 7;
           const int hp = blk / CGC, kc = blk - hp * CGC;
           const uint8_t s = sc[hp * p.CGin + c * CGC + kc];
-          const uint4 v = decode_raw<FA>(lds_row<FA>(pk + blk * BBA, r), scale_pair<FA>(s));
+          const uint4 v = decode_raw<FA>(row8_bits<FA>(pk + blk * BBA, r), scale_pair<FA>(s));
           *reinterpret_cast<uint4 *>(dec + i * 16) = v;
         }
         // weights: fwd block (tap, nb, kc) at (tap * NB + nb) * CGC + kc;
         //          dgrad block (tap, kc, nb) at (tap * CGC + kc) * NB + nb
-        const int nbr = p.nb_blocks * 8;
+        const int nbr = p.wd ? 0 : p.nb_blocks * 8;   // the decoded copy arrives by TMA
         uint8_t *decb = dec + p.dec_b_off;
         const uint8_t *pkb = pk + p.pk_b_off;
         const uint8_t *scw = sc + p.scw_off;
@@ -692,7 +706,7 @@ __global__ void __launch_bounds__(HC_CONV_THREADS, 1)
             d_tap += wrap ? 1 : 0;
           }
           const uint8_t s = scw[si];
-          const uint4 v = decode_raw<FB>(lds_row<FB>(pkb + blk * BBB, r), scale_pair<FB>(s));
+          const uint4 v = decode_raw<FB>(row8_bits<FB>(pkb + blk * BBB, r), scale_pair<FB>(s));
           *reinterpret_cast<uint4 *>(decb + i * 16) = v;
         }
         fence_async_smem();

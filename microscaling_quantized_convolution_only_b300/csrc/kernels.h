@@ -56,6 +56,8 @@ struct ConvParams {
   float pre_mult;                  // undoes the operand pre-scaling of the decode
   float *out;                      // fwd: Y HWCN (nullable with rq); dgrad: dX HWCN; wgrad: partial sums
   Requant rq;                      // rq.codes == nullptr: no fused epilogue
+  const void *wdec;                // fwd / dgrad: decoded weight copy (128 bytes per block, packed order)
+                                   // or nullptr
   // tiling
   int BN;                          // columns per tile (multiple of 16, <= 256)
   int acc_stride;                  // TMEM columns per accumulator buffer (power of two)
@@ -102,6 +104,9 @@ struct HaloConv {
   int nchunks;                   // CGin / 2
   int tiles_g, tiles_w, tiles_h, tiles_n, num_tiles;
   int PS;                        // packed ring depth
+  int wd;                        // 1: the weight operand is copied decoded (ConvParams::wdec) by TMA
+                                 // into the decoded stages, and the decode warps convert the halo only
+  uint32_t wd_bytes;             // decoded weight bytes per chunk (nb_blocks * 128)
   const uint8_t *w_scales, *in_scales;
   int COG, CIG;                  // weight block groups: W is [Kh*Kw][COG][CIG]
   const float *sa, *sb;
@@ -171,6 +176,9 @@ bool make_tensor_map_strided(void *map, const void *base, int esize, int rank, c
                              const uint64_t *strides, const uint32_t *box);
 
 cudaError_t launch_amax(const void *src, int dtype, int64_t n, uint32_t *amax_bits, int num_sms, cudaStream_t s);
+// the decoded weight copy: nblocks packed blocks of format fmt -> 128 bytes each
+cudaError_t launch_weight_decode(const uint8_t *codes, const uint8_t *scales, int fmt, int64_t nblocks, void *out,
+                                 int num_sms, cudaStream_t s);
 cudaError_t launch_quantize(const void *src, int dtype, int layout, int fmt, const QuantParams &p, int num_sms,
                             cudaStream_t s);
 

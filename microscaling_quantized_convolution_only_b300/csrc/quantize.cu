@@ -646,6 +646,32 @@ static cudaError_t launch_q(const void *src, int layout, const QuantParams &p, i
   return cudaGetLastError();
 }
 
+// The decoded weight copy: row r of block b (eight codes) becomes the 16 bytes
+// out[8 b + r], eight fp16 values code * B_scale (x 1/4 for E4M3 codes) --
+// the conversion the convolutions' decode warps apply on chip (decode_raw,
+// scale_pair), so a convolution that copies these rows computes exactly what
+// it computes from the packed blocks.  One thread per row.
+template <int F>
+__global__ void __launch_bounds__(256) weight_decode_kernel(const uint8_t *__restrict__ codes,
+                                                            const uint8_t *__restrict__ scales, int64_t rows,
+                                                            uint4 *__restrict__ out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < rows; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i >> 3;
+    out[i] = decode_raw<F>(row8_bits<F>(codes + b * Fmt<F>::BLOCK_BYTES, (int)(i & 7)), scale_pair<F>(scales[b]));
+  }
+}
+
+cudaError_t launch_weight_decode(const uint8_t *codes, const uint8_t *scales, int fmt, int64_t nblocks, void *out,
+                                 int num_sms, cudaStream_t s) {
+  const int64_t rows = nblocks * 8;
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>((rows + 255) / 256, (int64_t)num_sms * 8));
+  uint4 *o = static_cast<uint4 *>(out);
+  if (fmt == 4) weight_decode_kernel<4><<<grid, 256, 0, s>>>(codes, scales, rows, o);
+  else if (fmt == 6) weight_decode_kernel<6><<<grid, 256, 0, s>>>(codes, scales, rows, o);
+  else weight_decode_kernel<8><<<grid, 256, 0, s>>>(codes, scales, rows, o);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_amax(const void *src, int dtype, int64_t n, uint32_t *amax_bits, int num_sms, cudaStream_t s) {
   const int64_t per = dtype == 0 ? 4 : 8;
   int64_t want = (n / per + 255) / 256;

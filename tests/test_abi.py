@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert mq.abi_version() == 2
+    assert mq.abi_version() == 3
     assert mq.status_string(0) == "ok"
     assert "multiples of 8" in mq.status_string(2)
 
@@ -94,3 +94,22 @@ def test_fault_inject_validates_its_arguments(lib):
     assert lib.mqconv_test_fault_inject(7) == 1               # unknown injection
     assert lib.mqconv_test_fault_inject(1) == 0
     assert lib.mqconv_test_fault_inject(0) == 0               # back to normal operation
+
+
+def test_decoded_weight_copy_sizes_and_checks(lib):
+    """The decoded weight copy: 128 bytes per block; a copy on a tensor of another
+    role, a misaligned copy and a decode request without one are argument errors,
+    reported before any CUDA call."""
+    assert mq.weight_decoded_bytes((64, 128, 3, 3)) == 8 * 16 * 9 * 128
+    assert mq.weight_decoded_bytes((12, 16, 3, 3)) == 0
+    P = mq._Packed
+    good = mq.desc(Layer(8, 16, 8, 8, 16, 3, 1, 1))
+    x_dec = P(4, 0, (ctypes.c_int64 * 4)(8, 16, 8, 8), 16, 16, 16, 16)       # ACT with a decoded copy
+    x = P(4, 0, (ctypes.c_int64 * 4)(8, 16, 8, 8), 16, 16, 16, None)
+    w = P(4, 1, (ctypes.c_int64 * 4)(16, 16, 3, 3), 16, 16, 16, None)
+    w_mis = P(4, 1, (ctypes.c_int64 * 4)(16, 16, 3, 3), 16, 16, 16, 24)     # decoded not 16-byte aligned
+    assert lib.mqconv_fwd(ctypes.byref(good), ctypes.byref(x_dec), ctypes.byref(w), 16, None, None) == 1
+    assert lib.mqconv_fwd(ctypes.byref(good), ctypes.byref(x), ctypes.byref(w_mis), 16, None, None) == 3
+    assert lib.mqconv_weight_decode(ctypes.byref(w), None) == 1                # no decoded copy
+    assert lib.mqconv_weight_decode(ctypes.byref(x_dec), None) == 1            # not a weight tensor
+    assert lib.mqconv_weight_decode(ctypes.byref(w_mis), None) == 3
