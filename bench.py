@@ -853,16 +853,12 @@ TRAFFIC = {
     # one step's four launches (three with the fused requantization of dX,
     # whose 13 MB packed output is still in L2 when the launch ends, and the
     # plain one of layer 0 writing 45 MB of fp32 dX); bytes per launch
-    ("stack4-56x56-c128-nvfp4", "conv_dgrad"): {"bytes_per_launch": 24840576.0, "batch": 64, "sources_sha1": "973bf1c65ca0a5c03fe34bc8fa163a3055c4a2ef"},
-    ("stack4-56x56-c128-nvfp4", "conv_fwd"): {"bytes_per_launch": 24782848.0, "batch": 64, "sources_sha1": "973bf1c65ca0a5c03fe34bc8fa163a3055c4a2ef"},
+    ("stack4-56x56-c128-nvfp4", "conv_dgrad"): {"bytes_per_launch": 24978752.0, "batch": 64, "sources_sha1": "800ddd799aaf12c3197c5b536c2f9b783181d5c7"},
+    ("stack4-56x56-c128-nvfp4", "conv_fwd"): {"bytes_per_launch": 24996160.0, "batch": 64, "sources_sha1": "800ddd799aaf12c3197c5b536c2f9b783181d5c7"},
     # the four launches alike; the small write term (split-K partials,
-    # 0.07-0.08 MB) does not grow with the batch but is scaled with it
-    ("stack4-56x56-c128-nvfp4", "conv_wgrad"): {"bytes_per_launch": 26711744.0, "batch": 64, "sources_sha1": "973bf1c65ca0a5c03fe34bc8fa163a3055c4a2ef"},
+    # 0.07 MB) does not grow with the batch but is scaled with it
+    ("stack4-56x56-c128-nvfp4", "conv_wgrad"): {"bytes_per_launch": 26687360.0, "batch": 64, "sources_sha1": "800ddd799aaf12c3197c5b536c2f9b783181d5c7"},
 }
-
-
-
-
 
 
 # the sources the conv kernels are built from (device code, the parameter
